@@ -1,0 +1,336 @@
+"""Pins of the oracle to facts outside itself (CPU only).
+
+Each test checks an oracle routine against something the pages or the
+mathematics fix: a table printed on a page (tests/golden, each file citing
+its passage), a library routine (torch's bf16 rounding, numpy's float64
+matmul, math.fsum), brute-force integer sums, closed forms, invariants.
+Plausible mistakes -- a dropped term, a wrong sign or index, an operand
+transposed -- fail at least one of them; the comments say which.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.conftest import GOLDEN
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+def _tokens(P, n, dtype=np.int32):
+    """Slot r filled with 1000*r + i, so every cell names its origin (rank, index)."""
+    return (np.arange(P)[:, None] * 1000 + np.arange(n)[None, :]).astype(dtype)
+
+
+# ---------------------------------------------------------------- bf16 rounding
+def test_bf16_rne_matches_torch_on_random_and_special_values():
+    """bf16_rne == torch's CPU fp32->bf16 conversion (round to nearest even)."""
+    g = torch.Generator().manual_seed(123)
+    bits = torch.randint(0, 2**32, (200_000,), generator=g, dtype=torch.int64).to(torch.int64)
+    f = bits.to(torch.int32).view(torch.float32)
+    f = f[~torch.isnan(f)]
+    special = []
+    for e in (1, 2, 100, 126, 127, 128, 200, 254):
+        for low in (0x0000, 0x7FFF, 0x8000, 0x8001, 0xFFFF):
+            for keep_odd in (0, 1):
+                special.append((e << 23) | (keep_odd << 16) | low)
+    special += [0x00000001, 0x00008000, 0x00018000, 0x007FFFFF, 0x7F7FFFFF, 0x7F7F8000, 0x7F7F7FFF,
+                0x7F800000, 0x80000000, 0xFF800000, 0x00000000, 0x80008000, 0x3F808000, 0x3F818000]
+    sp = torch.tensor([s if s < 2**31 else s - 2**32 for s in special], dtype=torch.int32).view(torch.float32)
+    f = torch.cat([f, sp, -sp])
+    want = f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_from_f32(f.numpy())
+    assert np.array_equal(got, want)
+
+
+def test_bf16_nan_stays_nan_and_roundtrip():
+    f = np.array([np.nan, -np.nan, np.float32(1.5), np.float32(-2.25)], dtype=np.float32)
+    h = oracle.bf16_from_f32(f)
+    back = oracle.f32_from_bf16(h)
+    assert np.isnan(back[0]) and np.isnan(back[1])
+    assert back[2] == 1.5 and back[3] == -2.25
+
+
+# ---------------------------------------------------------------- ppermute
+def test_ppermute_matches_pallas_table_p4():
+    """The 4-device right-shift table: D0:x3, D1:x0, D2:x1, D3:x2."""
+    rows = _golden_lines("ppermute_p4.txt")
+    P, n = 4, 1024
+    x = _tokens(P, n)
+    out = oracle.ppermute_right(x, "i32")
+    for dev, _inp, _to, final in rows:
+        r = int(dev[1:])
+        src = int(final[1:])
+        assert np.array_equal(out[r], x[src]), (dev, final)
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 5, 8])
+def test_ppermute_is_a_rotation(P):
+    """Applying the right shift P times is the identity; once moves slot r-1 to r."""
+    x = _tokens(P, 37)
+    y = x.copy()
+    for _ in range(P):
+        y = oracle.ppermute_right(y, "i32")
+    assert np.array_equal(y, x)
+    once = oracle.ppermute_right(x, "i32")
+    assert np.array_equal(once, np.roll(x, 1, axis=0))
+
+
+# ---------------------------------------------------------------- all_gather
+def test_all_gather_ring_matches_pallas_slot_table_p4():
+    """Per-step slot state of the 4-device all-gather ([PALLAS] s2.5)."""
+    rows = _golden_lines("all_gather_p4_steps.txt")
+    P, n = 4, 3
+    x = _tokens(P, n)
+    for row in rows:
+        label, states = row[0], row[1:]
+        nsteps = None if label == "init" else int(label[4:]) + 1
+        out = np.full((P, P * n), -1, dtype=np.int32)
+        if nsteps is not None:
+            oracle.all_gather_ring(x, out, "i32", nsteps=nsteps)
+        for r, st in enumerate(states):
+            cells = st.strip("[]").split(",")
+            for k, cell in enumerate(cells):
+                got = out[r, k * n:(k + 1) * n]
+                if cell == "-":
+                    assert np.all(got == -1), (label, r, k)
+                else:
+                    assert np.array_equal(got, x[int(cell[1:])]), (label, r, k)
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 16])
+def test_all_gather_ring_equals_definition(P):
+    x = _tokens(P, 19)
+    ring = oracle.all_gather_ring(x, np.zeros((P, P * 19), dtype=np.int32), "i32")
+    assert np.array_equal(ring, oracle.all_gather(x, "i32"))
+    # definition against numpy's concatenation: every row is in_0 | in_1 | ... | in_{P-1}
+    assert np.array_equal(oracle.all_gather(x, "i32"), np.tile(x.reshape(1, -1), (P, 1)))
+
+
+# ---------------------------------------------------------------- ring all-reduce: order
+def _check_order_table(name, P):
+    rows = _golden_lines(name)
+    for row in rows:
+        g, r, cells = int(row[0]), int(row[1]), row[2:]
+        got = oracle.ring_allreduce_trace(P, P, nsteps=g)
+        assert got[r] == cells, (g, r, got[r], cells)
+
+
+def test_ring_allreduce_order_table_p4():
+    """Every intermediate state of the P=4 schedule (hand-derived from the
+    pages' index rules).  A wrong recv_add_idx / left_send_idx, a missing +P,
+    RS and AG rows swapped, or an operand order flip all change a cell."""
+    _check_order_table("ring_allreduce_p4_order.txt", 4)
+
+
+def test_ring_allreduce_order_table_p2():
+    """The P=2 edge case: left of rank 0 is rank 1, one round per phase."""
+    _check_order_table("ring_allreduce_p2_order.txt", 2)
+
+
+@pytest.mark.parametrize("P", [2, 3, 4, 5, 8, 13])
+def test_ring_fold_closed_form_equals_schedule_symbolically(P):
+    """The closed form R[k] = ((x_{k+1}+x_{k+2})+...)+x_k is what the schedule
+    produces on every rank for every chunk (association tree and all)."""
+    res = oracle.ring_allreduce_trace(P, P)
+    fold = oracle.ring_fold_trace(P, P)
+    for r in range(P):
+        assert res[r] == fold
+    for k in range(P):
+        terms = [(k + j) % P for j in range(1, P + 1)]
+        expect = str(terms[0])
+        for t in terms[1:]:
+            expect = f"({expect}+{t})"
+        assert fold[k] == expect
+
+
+# ---------------------------------------------------------------- ring all-reduce: values
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 16, 31])
+def test_ring_allreduce_i32_bitmask(P):
+    """x_r = 1<<r: every output is 2^P - 1 (each contributor exactly once)."""
+    N = P * 7
+    x = np.zeros((P, N), dtype=np.int32)
+    for r in range(P):
+        x[r] = np.int32(np.uint32(1 << r).astype(np.int32))
+    out = oracle.ring_allreduce(x.copy(), "i32")
+    assert np.all(out.view(np.uint32) == np.uint32((1 << P) - 1))
+
+
+@pytest.mark.parametrize("P", [2, 3, 4, 8, 16, 32])
+def test_ring_allreduce_i32_positional(P):
+    """x_r[i] = i + (r<<16): result P*i + 2^16*P(P-1)/2 (mod 2^32), so a chunk
+    stored at the wrong offset shows up (the "chunks misplaced" symptom)."""
+    c = 11
+    N = P * c
+    i = np.arange(N, dtype=np.int64)
+    x = ((i[None, :] + (np.arange(P, dtype=np.int64)[:, None] << 16)) & 0xFFFFFFFF).astype(np.uint32).view(np.int32)
+    out = oracle.ring_allreduce(x.copy(), "i32")
+    want = ((P * i + (1 << 16) * P * (P - 1) // 2) & 0xFFFFFFFF).astype(np.uint32)
+    for r in range(P):
+        assert np.array_equal(out[r].view(np.uint32), want)
+
+
+def test_ring_allreduce_i32_wraps():
+    P, N = 4, 8
+    x = np.full((P, N), 2**31 - 1, dtype=np.int32)
+    out = oracle.ring_allreduce(x.copy(), "i32")
+    assert np.all(out == np.int32(np.uint32((4 * (2**31 - 1)) % 2**32).astype(np.int32)))
+
+
+@pytest.mark.parametrize("P", [2, 3, 4, 8])
+def test_ring_allreduce_integer_valued_floats_exact(P):
+    """Integer-valued fp32 in [-1000,1000]: every order is exact, so the
+    result equals the brute-force int64 sum on every rank."""
+    g = np.random.default_rng(7)
+    N = P * 1000
+    xi = g.integers(-1000, 1001, size=(P, N))
+    out = oracle.ring_allreduce(xi.astype(np.float32), "f32")
+    want = xi.sum(axis=0).astype(np.float32)
+    for r in range(P):
+        assert np.array_equal(out[r], want)
+
+
+def test_ring_allreduce_p1_identity_and_p2_plain_sum():
+    g = np.random.default_rng(1)
+    x = g.standard_normal((1, 64)).astype(np.float32)
+    assert np.array_equal(oracle.ring_allreduce(x.copy(), "f32"), x)
+    x2 = g.standard_normal((2, 64)).astype(np.float32)
+    out = oracle.ring_allreduce(x2.copy(), "f32")
+    s = (x2[0] + x2[1]).astype(np.float32)   # one IEEE add: no order question at P=2
+    assert np.array_equal(out[0], s) and np.array_equal(out[1], s)
+
+
+@pytest.mark.parametrize("P,dtype", [(3, "f32"), (4, "f32"), (5, "f32"), (8, "f32"), (4, "bf16"), (8, "bf16")])
+def test_ring_allreduce_values_equal_closed_form_and_ranks_identical(P, dtype):
+    g = np.random.default_rng(P)
+    N = P * 513
+    xf = g.standard_normal((P, N)).astype(np.float32)
+    x = oracle.bf16_from_f32(xf * 0.01) if dtype == "bf16" else xf
+    out = oracle.ring_allreduce(x.copy(), dtype)
+    fold = oracle.ring_fold_at(x, dtype, np.arange(N))
+    for r in range(P):
+        assert np.array_equal(out[r], fold)
+    assert all(np.array_equal(out[0], out[r]) for r in range(P))
+
+
+@pytest.mark.parametrize("P", [2, 4, 8, 16])
+def test_ring_allreduce_f32_error_bound_vs_fsum(P):
+    """|ring - exact| <= (P-1) 2^-24 sum|x| (+ final rounding); the same bound
+    holds for the naive sum.  A dropped term or a sign error breaks it."""
+    g = np.random.default_rng(100 + P)
+    N = P * 200
+    x = g.standard_normal((P, N)).astype(np.float32)
+    out = oracle.ring_allreduce(x.copy(), "f32")[0].astype(np.float64)
+    naive = oracle.naive_sum(x, "f32").astype(np.float64)
+    exact = np.array([math.fsum(x[:, i].astype(np.float64)) for i in range(N)])
+    bound = (P - 1) * 2.0**-24 * np.abs(x).astype(np.float64).sum(axis=0) + 1e-45
+    assert np.all(np.abs(out - exact) <= bound)
+    assert np.all(np.abs(naive - exact) <= bound)
+
+
+def test_ring_allreduce_bf16_error_bound_vs_exact():
+    """Per-hop bf16 rounding: |ring - exact| <= (P-1) 2^-8 sum|x|."""
+    P = 8
+    g = np.random.default_rng(5)
+    N = P * 300
+    x = oracle.bf16_from_f32(g.standard_normal((P, N)).astype(np.float32) * 0.01)
+    xf = oracle.f32_from_bf16(x).astype(np.float64)
+    out = oracle.f32_from_bf16(oracle.ring_allreduce(x.copy(), "bf16")[0]).astype(np.float64)
+    exact = xf.sum(axis=0)
+    assert np.all(np.abs(out - exact) <= (P - 1) * 2.0**-8 * np.abs(xf).sum(axis=0))
+
+
+def test_ring_allreduce_rejects_indivisible_size():
+    with pytest.raises(ValueError):
+        oracle.ring_allreduce(np.zeros((4, 10), dtype=np.float32), "f32")
+
+
+# ---------------------------------------------------------------- reduce-scatter
+@pytest.mark.parametrize("P,dtype", [(2, "f32"), (4, "f32"), (8, "f32"), (5, "i32"), (8, "bf16")])
+def test_reduce_scatter_equals_allreduce_chunk_and_state(P, dtype):
+    """out_r = chunk r of the all-reduce; bufs afterwards = the all-reduce
+    state after P-2 rounds (the last round writes to out, not the slot)."""
+    g = np.random.default_rng(11 + P)
+    c = 257
+    N = P * c
+    if dtype == "i32":
+        x = g.integers(-2**31, 2**31, size=(P, N)).astype(np.int32)
+    else:
+        xf = g.standard_normal((P, N)).astype(np.float32)
+        x = oracle.bf16_from_f32(xf) if dtype == "bf16" else xf
+    bufs = x.copy()
+    out = oracle.reduce_scatter(bufs, dtype)
+    full = oracle.ring_allreduce(x.copy(), dtype)
+    for r in range(P):
+        assert np.array_equal(out[r], full[r, r * c:(r + 1) * c])
+    assert np.array_equal(bufs, oracle.ring_allreduce(x.copy(), dtype, nsteps=P - 2))
+
+
+def test_reduce_scatter_semantics_brute_force():
+    """D_b = sum over devices of block b ([PALLAS] s4.1), exact in integers."""
+    P, c = 4, 64
+    g = np.random.default_rng(3)
+    xi = g.integers(-1000, 1001, size=(P, P * c))
+    out = oracle.reduce_scatter(xi.astype(np.float32), "f32")
+    for b in range(P):
+        assert np.array_equal(out[b], xi[:, b * c:(b + 1) * c].sum(axis=0).astype(np.float32))
+
+
+def test_reduce_scatter_trace_p4():
+    outs, _ = oracle.reduce_scatter_trace(4, 4)
+    assert [o[0] for o in outs] == ["(((1+2)+3)+0)", "(((2+3)+0)+1)", "(((3+0)+1)+2)", "(((0+1)+2)+3)"]
+
+
+def test_reduce_scatter_p1_copies():
+    x = np.arange(8, dtype=np.float32).reshape(1, 8)
+    assert np.array_equal(oracle.reduce_scatter(x.copy(), "f32")[0], x[0])
+
+
+# ---------------------------------------------------------------- naive sum
+def test_naive_sum_integer_exact_and_i32():
+    g = np.random.default_rng(9)
+    xi = g.integers(-1000, 1001, size=(8, 333))
+    assert np.array_equal(oracle.naive_sum(xi.astype(np.float32), "f32"), xi.sum(axis=0).astype(np.float32))
+    assert np.array_equal(oracle.naive_sum(xi.astype(np.int32), "i32"), xi.sum(axis=0).astype(np.int32))
+
+
+# ---------------------------------------------------------------- all-gather + matmul
+def test_ag_gather_rank_order():
+    P, M_r, K = 3, 4, 8
+    sh = np.arange(P * M_r * K, dtype=np.uint16).reshape(P, M_r, K)
+    assert np.array_equal(oracle.ag_gather(sh), sh.reshape(P * M_r, K))
+
+
+def test_gemm_tiny_hand_example():
+    """A = [[1,2],[3,4]], B (one output feature per row) = [[5,6],[7,8]]:
+    C = A B^T = [[17,23],[39,53]], all exactly representable in bf16."""
+    A = oracle.bf16_from_f32(np.array([[1, 2], [3, 4]], dtype=np.float32))
+    B = oracle.bf16_from_f32(np.array([[5, 6], [7, 8]], dtype=np.float32))
+    f64, b16, ab = oracle.gemm_bf16_at(A, B)
+    assert np.array_equal(f64, np.array([[17, 23], [39, 53]], dtype=np.float64))
+    assert np.array_equal(oracle.f32_from_bf16(b16), np.array([[17, 23], [39, 53]], dtype=np.float32))
+    assert np.array_equal(ab, f64)
+
+
+def test_gemm_matches_numpy_float64_and_sampling():
+    g = np.random.default_rng(4)
+    M, N, K = 96, 80, 200
+    A = oracle.bf16_from_f32(g.standard_normal((M, K)).astype(np.float32) * 0.02)
+    B = oracle.bf16_from_f32(g.standard_normal((N, K)).astype(np.float32) * 0.02)
+    Af = oracle.f32_from_bf16(A).astype(np.float64)
+    Bf = oracle.f32_from_bf16(B).astype(np.float64)
+    f64, b16, ab = oracle.gemm_bf16_at(A, B)
+    ref = Af @ Bf.T
+    assert np.allclose(f64, ref, rtol=0, atol=1e-12)
+    assert np.allclose(ab, np.abs(Af) @ np.abs(Bf).T, rtol=1e-12, atol=0)
+    assert np.array_equal(b16, oracle.bf16_from_f32(f64.astype(np.float32)))
+    rows, cols = np.array([0, 5, 95]), np.array([79, 1])
+    f64s, b16s, _ = oracle.gemm_bf16_at(A, B, rows, cols)
+    assert np.array_equal(f64s, f64[np.ix_(rows, cols)])
+    assert np.array_equal(b16s, b16[np.ix_(rows, cols)])
