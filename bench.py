@@ -1,0 +1,406 @@
+"""Benchmark: ring all-reduce on one GB300, P=8 logical ranks, 64 MiB per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload f32_64mib|bf16_64mib|weak] [--P P] [--no-secondary]
+
+One step = one ring all-reduce (reduce-scatter + all-gather, 2(P-1) ring
+steps) over the workload's synthetic inputs, which are resident in HBM when
+the timed region starts.  The in-place inputs are restored by a device copy
+before every step, outside the CUDA events that time the step.  The metric is
+GB/s of the ring schedule's algorithmic bytes 5(P-1)*N*e per all-reduce
+(roofline (a)); the fraction of the minimum-traffic roofline (b) = 2*P*N*e is
+reported beside it.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs an independent
+replica of the workload on its own GPU (the logical ranks already live in
+one GPU's HBM; there is no exchange between GPUs); value = the bytes all
+replicas processed / the slowest replica's time.
+
+--impl reference times the oracle (plain C on the host cores) on a bounded
+sample of the same workload; rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from ring_collectives_gb300 import synthetic  # noqa: E402
+
+ES = {"f32": 4, "bf16": 2}
+KERNEL_SOURCES = ["ring_collectives_gb300/csrc/ring_kernels.cu", "ring_collectives_gb300/csrc/dev.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="f32_64mib", choices=["f32_64mib", "bf16_64mib", "weak"])
+    ap.add_argument("--P", type=int, default=8)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--n-per-rank", type=int, default=0,
+                    help="override N per rank (a smaller case of the same workload, e.g. for profiling)")
+    return ap.parse_args()
+
+
+def workload_spec(name, P, n_override=0):
+    if name == "f32_64mib":
+        spec = dict(name=name, P=8, N=16 << 20, dtype="f32")
+    elif name == "bf16_64mib":
+        spec = dict(name=name, P=8, N=32 << 20, dtype="bf16")
+    else:
+        spec = dict(name=name, P=P, N=(4 << 20) * P, dtype="f32")
+    if n_override:
+        spec["N"] = n_override - n_override % spec["P"]
+    return spec
+
+
+def ring_bytes(P, N, e):
+    """Roofline (a): per rank, P-1 reduce-scatter steps of 2 reads + 1 write of
+    a chunk and P-1 all-gather steps of 1 read + 1 write: 5(P-1)*N*e in all."""
+    return 5 * (P - 1) * N * e
+
+
+def min_bytes(P, N, e):
+    """Roofline (b): read every input once, write every output once."""
+    return 2 * P * N * e
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the ring kernel from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"ring_allreduce_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    src_hash, traffic = None, None
+    with open(path, encoding="utf-8") as f:
+        for ln in f:
+            if ln.startswith("kernel_source_sha256_16:"):
+                src_hash = ln.split(":", 1)[1].strip()
+            if ln.startswith("dram_bytes_per_launch:"):
+                try:
+                    traffic = int(ln.split(":", 1)[1].strip())
+                except ValueError:
+                    traffic = None
+    return traffic if src_hash == kernel_hash() else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) == 8:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        pw = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_time(spec, seconds, warmup=0, steps=None, frac=16):
+    """Times the oracle all-reduce on the host (single thread) on a bounded
+    sample: the workload's P with N_s = N/frac elements per rank (the first N_s
+    of each slot's seeded values).  Returns (GB/s of ring bytes, sample text, runs)."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    P, N, dt = spec["P"], spec["N"], spec["dtype"]
+    Ns = N // frac
+    Ns -= Ns % P
+    x = synthetic.workload(spec["name"], P=P, N=Ns)
+    xn = x.view(torch.int16).numpy().view(np.uint16) if dt == "bf16" else x.numpy()
+    times = []
+    for _ in range(warmup):
+        oracle.ring_allreduce(xn.copy(), dt)
+    t_end = time.perf_counter() + seconds
+    while True:
+        buf = xn.copy()
+        t0 = time.perf_counter()
+        oracle.ring_allreduce(buf, dt)
+        times.append(time.perf_counter() - t0)
+        if (steps is not None and len(times) >= steps) or (steps is None and time.perf_counter() > t_end):
+            break
+    t = statistics.mean(times)
+    gbs = ring_bytes(P, Ns, ES[dt]) / t / 1e9
+    sample = (f"P={P}, {Ns} {dt} elements per rank (N/{frac} of the workload), single thread, "
+              f"{len(times)} runs, mean taken")
+    return gbs, sample, times
+
+
+def run_reference(args, spec, rank, world):
+    if rank != 0:
+        return 0
+    gbs, sample, times = oracle_time(spec, seconds=0, warmup=args.warmup, steps=args.steps, frac=1)
+    line = {
+        "impl": "reference", "metric": metric_name(spec), "value": round(gbs, 3), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.mean(times), 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": spec["dtype"], "data": "synthetic",
+        "config": config_dict(spec, args.gpus),
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def metric_name(spec):
+    return (f"ring_allreduce GB/s (ring-schedule bytes 5(P-1)*N*e / time) and % HBM roofline, "
+            f"P={spec['P']}, {spec['N'] * ES[spec['dtype']] >> 20} MiB/rank, {spec['dtype']}, 1xGB300 per replica")
+
+
+def config_dict(spec, ngpus):
+    return {"workload": f"ring_allreduce_{spec['name']}", "P": spec["P"], "N_per_rank": spec["N"],
+            "bytes_per_rank": spec["N"] * ES[spec["dtype"]], "chunk_elems": spec["N"] // spec["P"],
+            "replicas": ngpus, "parallelism": f"replicas{ngpus} (P logical ranks per GPU)",
+            "l2": "inputs (P*64 MiB) larger than L2; restored by a device copy before every step, outside the events"}
+
+
+# ------------------------------------------------------------------ GPU timing
+def time_allreduce(rc, bufs, pristine, N, steps, warmup, stream):
+    for _ in range(warmup):
+        bufs.copy_(pristine)
+        rc.ring_allreduce(bufs, N=N, stream=stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        bufs.copy_(pristine)
+        starts[i].record(stream)
+        rc.ring_allreduce(bufs, N=N, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def time_reduce_scatter(rc, bufs, out, pristine, N, steps, warmup, stream):
+    for _ in range(warmup):
+        bufs.copy_(pristine)
+        rc.ring_reduce_scatter(bufs, out, N=N, stream=stream)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        bufs.copy_(pristine)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        rc.ring_reduce_scatter(bufs, out, N=N, stream=stream)
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ts]
+
+
+def run_ours(args, spec, rank, world, dist):
+    import ring_collectives_gb300 as rc
+    import __graft_entry__
+    __graft_entry__.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    P, N, dt = spec["P"], spec["N"], spec["dtype"]
+    e = ES[dt]
+    x = synthetic.workload(spec["name"], P=P, N=N)
+    pristine = x.to(dev)
+    bufs = torch.empty_like(pristine)
+
+    # one untimed call checks that the library ran cleanly on this GPU
+    bufs.copy_(pristine)
+    rc.ring_allreduce(bufs, stream=stream)
+    if rc.ring_status(stream) != 0:
+        raise RuntimeError(rc.ring_last_error())
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        times = time_allreduce(rc, bufs, pristine, N, args.steps, args.warmup, stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    if rc.ring_status(stream) != 0:
+        raise RuntimeError(rc.ring_last_error())
+    ms = statistics.mean(times)
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # end to end through the host entry point: pinned host in -> device -> pinned host out
+    h_in = x.pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        rc.ring_allreduce_host(h_in, h_out, bufs, stream=stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        rc.ring_allreduce_host(h_in, h_out, bufs, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if rc.ring_status(stream) != 0:
+        raise RuntimeError(rc.ring_last_error())
+
+    secondary = {}
+    if not args.no_secondary and spec["name"] == "f32_64mib":
+        # bf16 gradient-bucket workload: all-reduce and standalone reduce-scatter
+        del h_in, h_out
+        xb = synthetic.workload("bf16_64mib")
+        pb = xb.to(dev)
+        bb = torch.empty_like(pb)
+        Nb = xb.shape[1]
+        tb = time_allreduce(rc, bb, pb, Nb, args.steps, args.warmup, stream)
+        out = torch.empty((8, Nb // 8), dtype=torch.bfloat16, device=dev)
+        trs = time_reduce_scatter(rc, bb, out, pb, Nb, args.steps, args.warmup, stream)
+        if rc.ring_status(stream) != 0:
+            raise RuntimeError(rc.ring_last_error())
+        mb, mrs = statistics.mean(tb), statistics.mean(trs)
+        secondary = {
+            "bf16_64mib_allreduce": {"ms": round(mb, 4), "GB/s": round(ring_bytes(8, Nb, 2) / mb / 1e6, 1),
+                                     "frac_a": round(ring_bytes(8, Nb, 2) / mb / 1e6 / peaks()[0], 4)},
+            "bf16_64mib_reduce_scatter": {"ms": round(mrs, 4),
+                                          "GB/s": round(3 * 7 * Nb * 2 / mrs / 1e6, 1),
+                                          "frac_a": round(3 * 7 * Nb * 2 / mrs / 1e6 / peaks()[0], 4)},
+        }
+        del pb, bb, out
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = peaks()
+    rb = ring_bytes(P, N, e)
+    achieved = rb / (ms * 1e-3) / 1e9
+    value = world * rb / (ms_max * 1e-3) / 1e9
+    cpu_gbs, cpu_sample, _ = oracle_time(spec, seconds=args.cpu_seconds, frac=1)
+    line = {
+        "metric": metric_name(spec), "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": config_dict(spec, world),
+        "frac_roofline_a": round(achieved / peak, 4),
+        "frac_roofline_b": round(min_bytes(P, N, e) / (ms * 1e-3) / 1e9 / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(spec["name"]),
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs, burst copy)",
+                     "algorithmic_bytes_per_launch": rb, "kernel": "k_ring (one launch per all-reduce)"},
+        "cpu_baseline": {"value": round(cpu_gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": cpu_sample},
+        "e2e": {"value": round(world * rb / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": P * N * e, "d2h_bytes_per_step": P * N * e,
+                "api": "ring_allreduce_host (pinned host slots in and out)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "ms_min": round(min(times), 4), "ms_median": round(statistics.median(times), 4),
+    }
+    if secondary:
+        line["secondary"] = secondary
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    spec = workload_spec(args.workload, args.P, args.n_per_rank)
+    if args.impl == "reference":
+        return run_reference(args, spec, rank, world)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
+        dist = dist_mod
+    try:
+        return run_ours(args, spec, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,197 @@
+/*
+ * ringcoll.h -- C ABI of libringcoll.so: ring collectives over P logical
+ * ranks that live in one GPU's HBM.
+ *
+ * Model.  The P ranks are P symmetric slots of device memory: slot r starts
+ * at base + r*stride bytes, so the symmetric-memory lookup symm_at(ptr, r) of
+ * "Triton-distributed 语义" (section "对称内存模型") is pointer arithmetic.
+ * Ranks form the ring of "Pallas TPU Distributed Collectives 复习文档",
+ * section 0.1: right = (r+1) % P, left = (r-1+P) % P.  A chunk is N/P
+ * consecutive elements of a slot; chunk k covers elements [k*N/P, (k+1)*N/P).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named *_base and the buffers of ag_gemm are DEVICE pointers
+ *     owned by the caller; the library never frees or keeps them.
+ *   - *_stride arguments are in BYTES; a stride must be at least the bytes
+ *     a slot uses (checked) and slots must not overlap each other.
+ *   - dtype is an rc_dtype value; element sizes: f32 4, bf16 2, i32 4 bytes.
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every call is asynchronous on it: the return value reports
+ *     argument validation and launch errors only; errors raised on the device
+ *     (a bounded wait that ran out) are read with ring_status().
+ *   - Alignment: when the base pointers and strides are 16-byte aligned and
+ *     the chunk size keeps chunk starts 16-byte aligned, kernels move data in
+ *     16-byte vectors; otherwise they fall back to element-wise access.
+ *     Misalignment is never an error.
+ *   - Degenerate sizes: n = 0 or N = 0 does nothing and returns RC_OK.
+ *   - The library owns one signal workspace per device, created on the first
+ *     call on that device (a cudaMalloc and a synchronous zeroing), grown on
+ *     demand and released by ring_finalize().  Make the first call (at the
+ *     largest P used) before capturing calls into a CUDA graph.  Calls that
+ *     share a device's workspace must not run concurrently: issue them on one
+ *     stream, or order the streams.
+ *   - Return values are rc_status codes; ring_last_error() describes the most
+ *     recent failure of the calling thread.
+ */
+#ifndef RINGCOLL_H
+#define RINGCOLL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { RC_F32 = 0, RC_BF16 = 1, RC_I32 = 2 } rc_dtype;
+
+typedef enum {
+    RC_OK = 0,
+    RC_ERR_INVALID = 1,     /* bad argument, detected on the host before any launch */
+    RC_ERR_CUDA = 2,        /* a CUDA runtime call failed (message in ring_last_error) */
+    RC_ERR_TIMEOUT = 3,     /* a device-side bounded wait ran out (from ring_status) */
+    RC_ERR_UNSUPPORTED = 4, /* no CUDA device, wrong architecture, or grid cannot be co-resident */
+    RC_ERR_NOMEM = 5        /* the signal workspace could not be allocated */
+} rc_status;
+
+#define RC_MAX_P 64 /* largest number of logical ranks */
+
+/*
+ * ring_ppermute_right -- right shift by one rank.
+ * "Pallas TPU Distributed Collectives 复习文档", section 1 (lax.ppermute):
+ * every rank sends its shard to its right neighbour, so rank r ends with
+ * the shard of its left neighbour:  dst_r[i] = src_{(r-1+P)%P}[i], i < n.
+ * src slots: [n] elements at src_base + r*src_stride (read only).
+ * dst slots: [n] elements at dst_base + r*dst_stride (written).
+ * The src and dst regions must not overlap (RC_ERR_INVALID otherwise).
+ * P = 1 copies slot 0 to slot 0 of dst.
+ */
+int ring_ppermute_right(const void *src_base, size_t src_stride, void *dst_base, size_t dst_stride,
+                        int P, size_t n, int dtype, void *stream);
+
+/*
+ * ring_all_gather -- every rank ends with every rank's shard, in rank order.
+ * "Pallas TPU Distributed Collectives 复习文档", section 2 (lax.all_gather),
+ * and "TPU 与分布式通信原语", section "reduce-scatter 与 all-gather": each rank
+ * first places its own shard, then in ring step t = 0..P-2 copies from its
+ * left neighbour the chunk (r-t-1+P)%P.
+ * Result: out_r[k*n + i] = in_k[i] for every k < P, i < n.
+ * in slots:  [n] elements at in_base + r*in_stride (read only).
+ * out slots: [P*n] elements at out_base + r*out_stride (written).
+ * in and out must not overlap.
+ */
+int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_t out_stride,
+                    int P, size_t n, int dtype, void *stream);
+
+/*
+ * ring_reduce_scatter -- rank r ends with the sum over ranks of chunk r.
+ * "TPU 与分布式通信原语", section "reduce-scatter 与 all-gather" (the ring
+ * reduce-scatter kernel, whose last step writes out_ref), with the round
+ * indices of "全归约 3：Ring——每步大小恒定", section "走读": in round
+ * s = 0..P-2 rank r adds its left neighbour's chunk (r-s-2+P)%P into its own
+ * chunk of that index; the last round writes the sum to out_r instead.
+ * Result: out_r = R[r], where for chunk k
+ *     R[k] = ((x_{k+1} + x_{k+2}) + ... + x_{k+P-1}) + x_k   (indices mod P)
+ * with "+" the element type's hop add (f32: IEEE binary32 add; bf16: add in
+ * binary32, round the partial sum to bf16 at every hop; i32: wrapping add).
+ * bufs slots: [N] elements at bufs_base + r*bufs_stride; CLOBBERED: they are
+ *     left holding the partial sums of rounds 0..P-3.
+ * out slots:  [N/P] elements at out_base + r*out_stride (written); out must
+ *     not overlap bufs.
+ * N must be a multiple of P ("SIZE 必须能被 rank 数量整除", same page);
+ * RC_ERR_INVALID otherwise.  P = 1 copies chunk 0 to out.
+ */
+int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride,
+                        int P, size_t N, int dtype, void *stream);
+
+/*
+ * ring_allreduce -- in-place ring all-reduce: reduce-scatter (P-1 rounds)
+ * then all-gather (P-1 rounds), 2(P-1) steps of one chunk each.
+ * "全归约 3：Ring——每步大小恒定", sections "思路" and "走读":
+ *   left = (r-1+P)%P; round s of reduce-scatter (signal row s) waits for the
+ *   left neighbour, adds its chunk left_send_idx = (left-s-1+P)%P into the
+ *   local chunk recv_add_idx = (r-s-2+P)%P (the same index), then signals
+ *   the right neighbour on row s+1; all-gather round t (rows P-1..2P-3)
+ *   copies the left neighbour's chunk (r-1-t+P)%P into the local chunk.
+ * Synchronisation is neighbour-local (per-step signal rows, release/acquire),
+ * with no grid-wide barrier.
+ * Result: every slot holds R[0] | R[1] | ... | R[P-1] (R as for
+ * ring_reduce_scatter), bit-identical on every rank.
+ * bufs slots: [N] elements at bufs_base + r*stride, read and written in place.
+ * N must be a multiple of P (RC_ERR_INVALID otherwise).  P = 1 is a no-op.
+ */
+int ring_allreduce(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream);
+
+/*
+ * ring_allreduce_host -- ring_allreduce on inputs held in HOST memory:
+ * copies slot r of h_in (host, [N] elements at h_in + r*h_in_stride) into
+ * device slot r of d_bufs, runs the all-reduce there, and copies the result
+ * of every slot back to h_out (host, may equal h_in).  d_bufs is caller-owned
+ * device scratch of P slots (d_stride bytes apart).  Host buffers should be
+ * page-locked (cudaHostAlloc / pinned) for the copies to be asynchronous.
+ * The copies and the kernel run on `stream`; h_out is valid after the stream
+ * completes.  Same validation and result as ring_allreduce.
+ */
+int ring_allreduce_host(const void *h_in, size_t h_in_stride, void *h_out, size_t h_out_stride,
+                        void *d_bufs, size_t d_stride, int P, size_t N, int dtype, void *stream);
+
+/*
+ * ag_gemm -- all-gather of row shards fused with a matmul, seen from rank
+ * `rank`.  "TPU 与分布式通信原语", section "collective matmul" (all-gather then
+ * local matmul, bf16 result), with the producer/consumer tiles, per-tile
+ * wait and rank-swizzled tile order of "Triton-distributed 语义", sections
+ * "生产者-消费者模型", "AllGather + GEMM 重叠", "线程块交织".
+ * a_shards: bf16 [M_r][K] row-major per rank, slot r at a_shards + r*a_stride.
+ * a_gathered: bf16 [P*M_r][K] row-major (written): rows [r*M_r, (r+1)*M_r)
+ *     are shard r (the all-gather result, bit-exact copy).
+ * B: bf16 [N][K] row-major (one output feature per row, the nn.Linear weight
+ *     layout), read only.
+ * C: bf16 [P*M_r][N] row-major (written): C = A_g . B^T, products summed in
+ *     binary32, rounded once to bf16.
+ * Requirements (RC_ERR_INVALID otherwise): 0 <= rank < P, M_r % 128 == 0,
+ * N % 256 == 0, K % 64 == 0, all pointers 16-byte aligned, a_stride a
+ * multiple of 16, no overlap between outputs and inputs.
+ */
+int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C,
+            int P, int rank, int M_r, int N, int K, void *stream);
+
+/*
+ * ring_status -- waits for `stream`, then returns and clears the device
+ * status of the calling device's workspace: RC_OK, or RC_ERR_TIMEOUT when a
+ * bounded wait in a kernel ran out (ring_last_error() then names the rank,
+ * step and slice that gave up).  A timed-out call leaves its outputs
+ * undefined; later calls are unaffected.
+ */
+int ring_status(void *stream);
+
+/* Message describing the calling thread's most recent error ("" if none). */
+const char *ring_last_error(void);
+
+/* Bound on every device-side wait, in milliseconds (default 2000, 1..600000). */
+int ring_set_timeout_ms(unsigned ms);
+
+/*
+ * Slices per rank for the ring kernels (0 = automatic).  Slice j of every
+ * chunk is an independent ring with its own signals; the grid is P x slices
+ * co-resident thread blocks.  Values above the co-residency limit are capped.
+ */
+int ring_set_slices(int slices);
+
+/*
+ * Test hook for failure detection: the next ring launch (ring_all_gather,
+ * ring_reduce_scatter or ring_allreduce) on any thread skips the notify that
+ * rank `rank` would send after global step `step`, in every slice.  Its right
+ * neighbour's bounded wait then runs out and ring_status() reports
+ * RC_ERR_TIMEOUT; no fault is raised and the device stays usable.
+ * (-1, -1) cancels a pending skip.
+ */
+int ring_debug_skip_notify(int rank, int step);
+
+/* Frees the signal workspaces of all devices.  No call may be in flight. */
+int ring_finalize(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGCOLL_H */

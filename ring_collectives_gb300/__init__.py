@@ -1,0 +1,214 @@
+"""ring_collectives_gb300 -- ring collectives over P logical ranks in one GB300's HBM.
+
+A thin ctypes binding over ``libringcoll.so`` (the C ABI of
+``include/ringcoll.h``).  Every function here only marshals arguments: the
+work runs in the library's CUDA kernels.  PyTorch supplies device memory and
+the current stream.
+
+Slots are rows: a 2-D CUDA tensor ``t`` of shape ``[P, L]`` whose rows are
+contiguous (``t.stride(1) == 1``) holds slot r at row r, so the slot stride is
+``t.stride(0) * t.element_size()`` bytes.  Supported dtypes: float32,
+bfloat16, int32.  Each call is asynchronous on the current CUDA stream (or the
+``stream`` given); device-side errors are read with :func:`ring_status`.
+
+If the library has not been built (``__graft_entry__.build()`` or
+``python -m ring_collectives_gb300._build``) every call raises: there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "RingError", "ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_allreduce",
+    "ring_allreduce_host", "ag_gemm", "ring_status", "ring_last_error", "ring_set_timeout_ms",
+    "ring_set_slices", "ring_debug_skip_notify", "ring_finalize", "library_path", "load",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libringcoll.so")
+
+RC_OK, RC_ERR_INVALID, RC_ERR_CUDA, RC_ERR_TIMEOUT, RC_ERR_UNSUPPORTED, RC_ERR_NOMEM = range(6)
+_DTYPE = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
+
+_lib = None
+
+
+class RingError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[rc={code}] {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libringcoll.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        L.ring_ppermute_right.argtypes = [vp, sz, vp, sz, i, sz, i, vp]
+        L.ring_all_gather.argtypes = [vp, sz, vp, sz, i, sz, i, vp]
+        L.ring_reduce_scatter.argtypes = [vp, sz, vp, sz, i, sz, i, vp]
+        L.ring_allreduce.argtypes = [vp, sz, i, sz, i, vp]
+        L.ring_allreduce_host.argtypes = [vp, sz, vp, sz, vp, sz, i, sz, i, vp]
+        L.ag_gemm.argtypes = [vp, sz, vp, vp, vp, i, i, i, i, i, vp]
+        L.ring_status.argtypes = [vp]
+        L.ring_last_error.argtypes = []
+        L.ring_last_error.restype = ctypes.c_char_p
+        L.ring_set_timeout_ms.argtypes = [ctypes.c_uint]
+        L.ring_set_slices.argtypes = [i]
+        L.ring_debug_skip_notify.argtypes = [i, i]
+        L.ring_finalize.argtypes = []
+        for name in ("ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_allreduce",
+                     "ring_allreduce_host", "ag_gemm", "ring_status", "ring_set_timeout_ms", "ring_set_slices",
+                     "ring_debug_skip_notify", "ring_finalize"):
+            getattr(L, name).restype = i
+        _lib = L
+    return _lib
+
+
+def ring_last_error() -> str:
+    return load().ring_last_error().decode(errors="replace")
+
+
+def _check(rc: int) -> None:
+    if rc != RC_OK:
+        raise RingError(rc, ring_last_error())
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _slots(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2 or (t.size(1) > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be 2-D [P, L] with contiguous rows")
+    if t.dtype not in _DTYPE:
+        raise TypeError(f"{name}: unsupported dtype {t.dtype}")
+    return t.data_ptr(), t.stride(0) * t.element_size(), _DTYPE[t.dtype]
+
+
+def ring_ppermute_right(src: torch.Tensor, dst: torch.Tensor, n: int | None = None, stream=None) -> torch.Tensor:
+    """dst[r, :n] = src[(r-1+P) % P, :n]."""
+    sp, ss, dt = _slots(src, "src")
+    dp, ds, dt2 = _slots(dst, "dst")
+    if dt != dt2 or src.size(0) != dst.size(0):
+        raise ValueError("src and dst differ in dtype or rank count")
+    n = min(src.size(1), dst.size(1)) if n is None else n
+    with torch.cuda.device(src.device):
+        _check(load().ring_ppermute_right(sp, ss, dp, ds, src.size(0), n, dt, _stream(stream, src.device)))
+    return dst
+
+
+def ring_all_gather(inp: torch.Tensor, out: torch.Tensor, n: int | None = None, stream=None) -> torch.Tensor:
+    """out[r, k*n:(k+1)*n] = inp[k, :n] for every r, k."""
+    ip, is_, dt = _slots(inp, "inp")
+    op, os_, dt2 = _slots(out, "out")
+    if dt != dt2 or inp.size(0) != out.size(0):
+        raise ValueError("inp and out differ in dtype or rank count")
+    n = inp.size(1) if n is None else n
+    if out.size(1) < inp.size(0) * n:
+        raise ValueError("out rows are shorter than P*n")
+    with torch.cuda.device(inp.device):
+        _check(load().ring_all_gather(ip, is_, op, os_, inp.size(0), n, dt, _stream(stream, inp.device)))
+    return out
+
+
+def ring_reduce_scatter(bufs: torch.Tensor, out: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
+    """out[r, :N/P] = ring sum of chunk r; ``bufs`` is clobbered."""
+    bp, bs, dt = _slots(bufs, "bufs")
+    op, os_, dt2 = _slots(out, "out")
+    if dt != dt2 or bufs.size(0) != out.size(0):
+        raise ValueError("bufs and out differ in dtype or rank count")
+    N = bufs.size(1) if N is None else N
+    with torch.cuda.device(bufs.device):
+        _check(load().ring_reduce_scatter(bp, bs, op, os_, bufs.size(0), N, dt, _stream(stream, bufs.device)))
+    return out
+
+
+def ring_allreduce(bufs: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
+    """In-place ring all-reduce over the first N elements of every row."""
+    bp, bs, dt = _slots(bufs, "bufs")
+    N = bufs.size(1) if N is None else N
+    with torch.cuda.device(bufs.device):
+        _check(load().ring_allreduce(bp, bs, bufs.size(0), N, dt, _stream(stream, bufs.device)))
+    return bufs
+
+
+def ring_allreduce_host(h_in: torch.Tensor, h_out: torch.Tensor, d_bufs: torch.Tensor, N: int | None = None,
+                        stream=None) -> torch.Tensor:
+    """All-reduce of host slots ``h_in`` (pinned CPU [P, L]) through device slots
+    ``d_bufs``; the result lands in ``h_out`` once the stream completes."""
+    if h_in.is_cuda or h_out.is_cuda:
+        raise TypeError("h_in and h_out must be CPU tensors")
+    if h_in.dim() != 2 or h_out.dim() != 2 or h_in.stride(1) != 1 or h_out.stride(1) != 1:
+        raise ValueError("host slots must be 2-D [P, L] with contiguous rows")
+    dp, ds, dt = _slots(d_bufs, "d_bufs")
+    if _DTYPE.get(h_in.dtype) != dt or _DTYPE.get(h_out.dtype) != dt:
+        raise TypeError("host and device slots differ in dtype")
+    P = h_in.size(0)
+    N = h_in.size(1) if N is None else N
+    es = h_in.element_size()
+    with torch.cuda.device(d_bufs.device):
+        _check(load().ring_allreduce_host(h_in.data_ptr(), h_in.stride(0) * es, h_out.data_ptr(),
+                                          h_out.stride(0) * es, dp, ds, P, N, dt, _stream(stream, d_bufs.device)))
+    return h_out
+
+
+def ag_gemm(a_shards: torch.Tensor, a_gathered: torch.Tensor, B: torch.Tensor, C: torch.Tensor, rank: int,
+            stream=None) -> torch.Tensor:
+    """a_shards [P, M_r, K], a_gathered [P*M_r, K], B [N, K], C [P*M_r, N], all bf16:
+    gathers the shards and computes C = A_g . B^T (fp32 accumulate, bf16 out)."""
+    for name, t in (("a_shards", a_shards), ("a_gathered", a_gathered), ("B", B), ("C", C)):
+        if not t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+    if a_shards.dim() != 3 or a_shards.stride(2) != 1 or a_shards.stride(1) != a_shards.size(2):
+        raise ValueError("a_shards must be [P, M_r, K] with row-major shards")
+    P, M_r, K = a_shards.shape
+    N = B.size(0)
+    if tuple(a_gathered.shape) != (P * M_r, K) or not a_gathered.is_contiguous():
+        raise ValueError("a_gathered must be contiguous [P*M_r, K]")
+    if tuple(B.shape) != (N, K) or not B.is_contiguous():
+        raise ValueError("B must be contiguous [N, K]")
+    if tuple(C.shape) != (P * M_r, N) or not C.is_contiguous():
+        raise ValueError("C must be contiguous [P*M_r, N]")
+    with torch.cuda.device(a_shards.device):
+        _check(load().ag_gemm(a_shards.data_ptr(), a_shards.stride(0) * 2, a_gathered.data_ptr(), B.data_ptr(),
+                              C.data_ptr(), P, rank, M_r, N, K, _stream(stream, a_shards.device)))
+    return C
+
+
+def ring_status(stream=None, device=None) -> int:
+    """Waits for the stream and returns (and clears) the device status code."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return load().ring_status(_stream(stream, dev))
+
+
+def ring_set_timeout_ms(ms: int) -> None:
+    _check(load().ring_set_timeout_ms(ms))
+
+
+def ring_set_slices(slices: int) -> None:
+    _check(load().ring_set_slices(slices))
+
+
+def ring_debug_skip_notify(rank: int, step: int) -> None:
+    _check(load().ring_debug_skip_notify(rank, step))
+
+
+def ring_finalize() -> None:
+    _check(load().ring_finalize())

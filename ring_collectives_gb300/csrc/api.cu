@@ -1,0 +1,387 @@
+// api.cu -- the C ABI of libringcoll.so (declared in include/ringcoll.h):
+// argument validation, the per-device signal workspace, launch-shape choice,
+// device status read-back and error strings.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+#include "ringcoll.h"
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<unsigned> g_timeout_ms{2000};
+std::atomic<int> g_slices{0};
+std::atomic<int> g_skip_rank{-1}, g_skip_step{-1};
+std::mutex g_mu;
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kMinSliceBytes = 32 << 10; // a slice below this is not worth its own ring
+constexpr uint64_t kEpochResetAt = 1ull << 30; // re-zero the workspace long before 32-bit wrap
+
+struct DeviceState {
+    bool probed = false;
+    int supported = 0;  // 1 if sm_103 and cooperative launch are available
+    int sm_count = 0;
+    int max_blocks[3] = {0, 0, 0}; // co-resident ring blocks per dtype
+    void *ws = nullptr;  // WsHeader followed by the signal words
+    size_t ws_bytes = 0;
+    uint64_t launches = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(RC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t elem_size(int dtype)
+{
+    switch (dtype) {
+    case RC_F32: return 4;
+    case RC_BF16: return 2;
+    case RC_I32: return 4;
+    default: return 0;
+    }
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// [lo, hi) byte range spanned by P slots of `bytes` each.
+bool regions_overlap(const void *a, size_t a_stride, size_t a_bytes, const void *b, size_t b_stride,
+                     size_t b_bytes, int P)
+{
+    const uintptr_t a0 = (uintptr_t)a, a1 = a0 + (size_t)(P - 1) * a_stride + a_bytes;
+    const uintptr_t b0 = (uintptr_t)b, b1 = b0 + (size_t)(P - 1) * b_stride + b_bytes;
+    return a0 < b1 && b0 < a1;
+}
+
+// Current device, probed once: compute capability 10.3 and cooperative launch.
+int current_device(int *dev_out, DeviceState **st_out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(RC_ERR_UNSUPPORTED, "no CUDA device: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(RC_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    DeviceState &st = g_dev[dev];
+    if (!st.probed) {
+        int major = 0, minor = 0, coop = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+        cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        st.supported = (major == 10 && minor == 3 && coop) ? 1 : 0;
+        if (st.supported) {
+            for (int dt = 0; dt < 3; ++dt) {
+                e = rc::ring_max_coresident(dt, rc::kRingThreads, dev, &st.max_blocks[dt]);
+                if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+            }
+        }
+        st.probed = true;
+        if (!st.supported)
+            return fail(RC_ERR_UNSUPPORTED, "device %d is sm_%d%d (cooperative launch %d); this library is built "
+                        "for sm_103a", dev, major, minor, coop);
+    }
+    if (!st.supported) return fail(RC_ERR_UNSUPPORTED, "device %d is not an sm_103 GPU", dev);
+    *dev_out = dev;
+    *st_out = &st;
+    return RC_OK;
+}
+
+// Makes the workspace at least `sig_bytes` of signal words (after the header).
+int ensure_workspace(DeviceState &st, size_t sig_bytes)
+{
+    const size_t need = sizeof(rc::WsHeader) + sig_bytes;
+    cudaError_t e;
+    if (st.ws && (st.ws_bytes < need || st.launches >= kEpochResetAt)) {
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "synchronise before workspace resize");
+        if (st.ws_bytes < need) {
+            cudaFree(st.ws);
+            st.ws = nullptr;
+            st.ws_bytes = 0;
+        } else {
+            e = cudaMemset(st.ws, 0, st.ws_bytes);
+            if (e == cudaSuccess) e = cudaDeviceSynchronize();
+            if (e != cudaSuccess) return cuda_fail(e, "workspace reset");
+            st.launches = 0;
+        }
+    }
+    if (!st.ws) {
+        size_t bytes = (need + (1u << 20) - 1) & ~(size_t)((1u << 20) - 1);
+        e = cudaMalloc(&st.ws, bytes);
+        if (e != cudaSuccess) {
+            st.ws = nullptr;
+            return fail(RC_ERR_NOMEM, "signal workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+        }
+        e = cudaMemset(st.ws, 0, bytes);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "workspace zeroing");
+        st.ws_bytes = bytes;
+        st.launches = 0;
+    }
+    return RC_OK;
+}
+
+// Slices per rank for a chunk of chunk_bytes (see ring_set_slices).
+int choose_slices(const DeviceState &st, int dtype, int P, size_t chunk_elems, size_t chunk_bytes, int *S_out)
+{
+    const int cap = st.max_blocks[dtype] / P;
+    if (cap < 1)
+        return fail(RC_ERR_UNSUPPORTED, "P=%d ranks exceed the %d co-resident blocks of this device", P,
+                    st.max_blocks[dtype]);
+    long S;
+    const int user = g_slices.load();
+    if (user > 0) {
+        S = user;
+    } else {
+        S = (long)(2 * st.sm_count) / P; // about two blocks per SM in total
+        const long by_size = (long)(chunk_bytes / kMinSliceBytes);
+        if (S > by_size) S = by_size;
+    }
+    const long by_granule = (long)(chunk_elems / rc::kSliceGranule);
+    if (S > by_granule) S = by_granule;
+    if (S > cap) S = cap;
+    if (S < 1) S = 1;
+    *S_out = (int)S;
+    return RC_OK;
+}
+
+int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda)
+{
+    int dev;
+    DeviceState *st = nullptr;
+    int rc_ = current_device(&dev, &st);
+    if (rc_) return rc_;
+    const size_t es = elem_size(dtype);
+    rc_ = choose_slices(*st, dtype, p.P, p.chunk, p.chunk * es, &p.S);
+    if (rc_) return rc_;
+    const size_t sig_words = (size_t)p.S * p.P * (size_t)p.rows * p.P;
+    std::lock_guard<std::mutex> lock(g_mu);
+    rc_ = ensure_workspace(*st, sig_words * 4);
+    if (rc_) return rc_;
+    p.hdr = (rc::WsHeader *)st->ws;
+    p.sig = (uint32_t *)((char *)st->ws + sizeof(rc::WsHeader));
+    p.timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
+    p.skip_rank = g_skip_rank.exchange(-1);
+    p.skip_step = g_skip_step.exchange(-1);
+    cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, st_cuda);
+    if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
+    st->launches++;
+    return RC_OK;
+}
+
+int run_copy(const void *src, size_t src_stride, void *dst, size_t dst_stride, int P, size_t n, int dtype,
+             cudaStream_t s)
+{
+    int dev;
+    DeviceState *st = nullptr;
+    int rc_ = current_device(&dev, &st);
+    if (rc_) return rc_;
+    const size_t es = elem_size(dtype);
+    const int vec_ok = aligned16(src) && aligned16(dst) && (src_stride % 16 == 0) && (dst_stride % 16 == 0);
+    cudaError_t e = rc::launch_ppermute((const char *)src, src_stride, (char *)dst, dst_stride, P, n, (int)es,
+                                        vec_ok, st->sm_count, s);
+    if (e != cudaSuccess) return cuda_fail(e, "copy kernel launch");
+    return RC_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *ring_last_error(void) { return g_err.c_str(); }
+
+int ring_set_timeout_ms(unsigned ms)
+{
+    if (ms < 1 || ms > 600000) return fail(RC_ERR_INVALID, "timeout %u ms outside 1..600000", ms);
+    g_timeout_ms.store(ms);
+    return RC_OK;
+}
+
+int ring_set_slices(int slices)
+{
+    if (slices < 0 || slices > 4096) return fail(RC_ERR_INVALID, "slices %d outside 0..4096", slices);
+    g_slices.store(slices);
+    return RC_OK;
+}
+
+int ring_debug_skip_notify(int rank, int step)
+{
+    if (rank < -1 || step < -1) return fail(RC_ERR_INVALID, "bad skip_notify arguments");
+    g_skip_rank.store(rank);
+    g_skip_step.store(step);
+    return RC_OK;
+}
+
+int ring_ppermute_right(const void *src_base, size_t src_stride, void *dst_base, size_t dst_stride, int P,
+                        size_t n, int dtype, void *stream)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (n == 0) return RC_OK;
+    if (!src_base || !dst_base) return fail(RC_ERR_INVALID, "null slot base");
+    if (P > 1 && (src_stride < n * es || dst_stride < n * es))
+        return fail(RC_ERR_INVALID, "stride below the %zu bytes of a slot", n * es);
+    if (regions_overlap(src_base, src_stride, n * es, dst_base, dst_stride, n * es, P))
+        return fail(RC_ERR_INVALID, "src and dst slots overlap");
+    return run_copy(src_base, src_stride, dst_base, dst_stride, P, n, dtype, (cudaStream_t)stream);
+}
+
+int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_t out_stride, int P, size_t n,
+                    int dtype, void *stream)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (n == 0) return RC_OK;
+    if (!in_base || !out_base) return fail(RC_ERR_INVALID, "null slot base");
+    if (P > 1 && (in_stride < n * es || out_stride < (size_t)P * n * es))
+        return fail(RC_ERR_INVALID, "stride below a slot's bytes (in %zu, out %zu)", n * es, (size_t)P * n * es);
+    if (regions_overlap(in_base, in_stride, n * es, out_base, out_stride, (size_t)P * n * es, P))
+        return fail(RC_ERR_INVALID, "in and out slots overlap");
+    if (P == 1) return run_copy(in_base, in_stride, out_base, out_stride, 1, n, dtype, (cudaStream_t)stream);
+    rc::RingParams p{};
+    p.data = (char *)out_base;
+    p.data_stride = out_stride;
+    p.in = (const char *)in_base;
+    p.in_stride = in_stride;
+    p.chunk = n;
+    p.P = P;
+    p.rows = P - 1;
+    p.mode = rc::MODE_ALL_GATHER;
+    p.vec_ok = aligned16(in_base) && aligned16(out_base) && in_stride % 16 == 0 && out_stride % 16 == 0 &&
+               (n * es) % 16 == 0;
+    return run_ring(p, dtype, (cudaStream_t)stream);
+}
+
+int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P, size_t N,
+                        int dtype, void *stream)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
+    if (N == 0) return RC_OK;
+    if (!bufs_base || !out_base) return fail(RC_ERR_INVALID, "null slot base");
+    const size_t c = N / (size_t)P;
+    if (P > 1 && (bufs_stride < N * es || out_stride < c * es))
+        return fail(RC_ERR_INVALID, "stride below a slot's bytes (bufs %zu, out %zu)", N * es, c * es);
+    if (regions_overlap(bufs_base, bufs_stride, N * es, out_base, out_stride, c * es, P))
+        return fail(RC_ERR_INVALID, "bufs and out slots overlap");
+    if (P == 1) return run_copy(bufs_base, bufs_stride, out_base, out_stride, 1, c, dtype, (cudaStream_t)stream);
+    rc::RingParams p{};
+    p.data = (char *)bufs_base;
+    p.data_stride = bufs_stride;
+    p.out = (char *)out_base;
+    p.out_stride = out_stride;
+    p.chunk = c;
+    p.P = P;
+    p.rows = P - 1;
+    p.mode = rc::MODE_REDUCE_SCATTER;
+    p.vec_ok = aligned16(bufs_base) && aligned16(out_base) && bufs_stride % 16 == 0 && out_stride % 16 == 0 &&
+               (c * es) % 16 == 0;
+    return run_ring(p, dtype, (cudaStream_t)stream);
+}
+
+int ring_allreduce(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
+    if (N == 0 || P == 1) return RC_OK;
+    if (!bufs_base) return fail(RC_ERR_INVALID, "null slot base");
+    if (stride < N * es) return fail(RC_ERR_INVALID, "stride %zu below the %zu bytes of a slot", stride, N * es);
+    const size_t c = N / (size_t)P;
+    rc::RingParams p{};
+    p.data = (char *)bufs_base;
+    p.data_stride = stride;
+    p.chunk = c;
+    p.P = P;
+    p.rows = 2 * (P - 1);
+    p.mode = rc::MODE_ALLREDUCE;
+    p.vec_ok = aligned16(bufs_base) && stride % 16 == 0 && (c * es) % 16 == 0;
+    return run_ring(p, dtype, (cudaStream_t)stream);
+}
+
+int ring_allreduce_host(const void *h_in, size_t h_in_stride, void *h_out, size_t h_out_stride, void *d_bufs,
+                        size_t d_stride, int P, size_t N, int dtype, void *stream)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
+    if (N == 0) return RC_OK;
+    if (!h_in || !h_out || !d_bufs) return fail(RC_ERR_INVALID, "null pointer");
+    const size_t row = N * es;
+    if ((P > 1 && (h_in_stride < row || h_out_stride < row || d_stride < row)))
+        return fail(RC_ERR_INVALID, "stride below the %zu bytes of a slot", row);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpy2DAsync(d_bufs, P > 1 ? d_stride : row, h_in, P > 1 ? h_in_stride : row, row,
+                                      (size_t)P, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    int rc_ = ring_allreduce(d_bufs, P > 1 ? d_stride : row, P, N, dtype, stream);
+    if (rc_) return rc_;
+    e = cudaMemcpy2DAsync(h_out, P > 1 ? h_out_stride : row, d_bufs, P > 1 ? d_stride : row, row, (size_t)P,
+                          cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    return RC_OK;
+}
+
+int ring_status(void *stream)
+{
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RC_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.ws) return RC_OK;
+    rc::WsHeader h;
+    e = cudaMemcpy(&h, st.ws, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (h.status == 0) return RC_OK;
+    e = cudaMemset((char *)st.ws + offsetof(rc::WsHeader, status), 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    return fail((int)h.status, "device wait timed out: rank %u, step %u, slice %u", h.err_rank, h.err_step,
+                h.err_slice);
+}
+
+int ring_finalize(void)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    int prev = 0;
+    cudaGetDevice(&prev);
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_dev[d].ws) {
+            cudaSetDevice(d);
+            cudaDeviceSynchronize();
+            cudaFree(g_dev[d].ws);
+            g_dev[d].ws = nullptr;
+            g_dev[d].ws_bytes = 0;
+            g_dev[d].launches = 0;
+        }
+    }
+    cudaSetDevice(prev);
+    return RC_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,52 @@
+// internal.h -- declarations shared by the library's translation units
+// (not part of the public ABI; the public header is include/ringcoll.h).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rc {
+
+// Device-resident header at the start of a signal workspace (128 bytes).
+struct WsHeader {
+    uint32_t epoch;     // launches completed on this workspace; a launch signals with epoch+1
+    uint32_t done;      // thread blocks of the running launch that have finished
+    uint32_t status;    // 0, or the rc_status error code of the first failure
+    uint32_t err_rank;  // where the first failure happened
+    uint32_t err_step;
+    uint32_t err_slice;
+    uint32_t pad[26];
+};
+static_assert(sizeof(WsHeader) == 128, "header is one 128-byte line");
+
+enum RingMode { MODE_ALLREDUCE = 0, MODE_REDUCE_SCATTER = 1, MODE_ALL_GATHER = 2 };
+
+// Arguments of one launch of the ring step engine.
+struct RingParams {
+    char *data;          // slots the ring runs on: bufs (all-reduce, reduce-scatter) or out (all-gather)
+    size_t data_stride;  // bytes between slots
+    const char *in;      // all-gather: input shards
+    size_t in_stride;
+    char *out;           // reduce-scatter: output chunks
+    size_t out_stride;
+    uint32_t *sig;       // signal rows, [S][P][rows][P] words
+    WsHeader *hdr;
+    size_t chunk;        // elements per chunk (all-gather: the shard length n)
+    int P, S, rows, mode;
+    int vec_ok;          // 1: every slot/chunk start is 16-byte aligned -> 16-byte vectors
+    int skip_rank, skip_step; // test hook: this rank skips its notify after this step (-1: none)
+    unsigned long long timeout_ns;
+};
+
+// Launch helpers implemented in ring_kernels.cu.  They return a cudaError_t.
+cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_t st);
+cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks);
+cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P,
+                            size_t n, int esize, int vec_ok, int sm_count, cudaStream_t st);
+
+// Threads per block of the ring kernel.
+constexpr int kRingThreads = 512;
+// Slices start on multiples of this many elements (keeps 16-byte vectors aligned).
+constexpr size_t kSliceGranule = 64;
+
+} // namespace rc

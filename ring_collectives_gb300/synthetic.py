@@ -2,66 +2,97 @@
 
 This module only draws random numbers: it holds none of the collectives'
 arithmetic, so both the CUDA path and the oracle can take their inputs from
-it.  Every generator is a CPU ``torch.Generator`` seeded explicitly, drawing
-the whole ``[P, N]`` block in one call, so slot r is row r and the bytes are
-identical on every machine that runs the same torch build.  (The pages draw
-with ``jax.random.key(0)``; those bits are not reproduced -- the pages print
-no values that would need them.)
+it.  Slot r of a workload with seed s is drawn from its own numpy PCG64
+stream seeded with the sequence (s, r), so the slots can be filled in
+parallel and the bytes are the same on every machine.  (The pages draw with
+``jax.random.key(0)``; those bits are not reproduced -- the pages print no
+values that would need them.)  Results are CPU torch tensors ``[P, N]``.
 
 Workloads (the names used by the tests and the benchmark):
 
-* ``tiny``      -- P logical ranks, each shard fp32 (8,128) ~ U[0,1), seed 0
-                   (the (8,128) shard of the Pallas ppermute/all_gather/psum
-                   examples).
+* ``tiny``      -- P logical ranks, each shard fp32 (8,128) = 1024 elements
+                   ~ U[0,1), seed 0 (the shard of the Pallas examples).
 * ``f32_64mib`` -- P=8, 16M fp32 per rank (64 MiB) ~ N(0,1), seed 1.
-* ``f32_int``   -- the same shape, integer values uniform in [-1000, 1000]
-                   stored as fp32 (every order of addition is exact).
-* ``bf16_64mib``-- P=8, 32M bf16 per rank ~ N(0, 0.01^2) (std 0.01), seed 2,
-                   drawn in fp32 then rounded to bf16 by torch.
+* ``f32_int``   -- the same shape, integers uniform in [-1000, 1000] stored
+                   as fp32 (every order of addition is exact), seed 1.
+* ``bf16_64mib``-- P=8, 32M bf16 per rank ~ N(0, 0.01^2) (std 0.01), seed 2:
+                   drawn in fp32, scaled, rounded to bf16 by torch.
 * ``weak``      -- chunk N/P = 4M fp32 ~ U[-1,1), seed 3, P in {2,4,8,16,32}.
-* ``ag_gemm``   -- P=8 shards A_r [1024,4096] and B [4096,4096], bf16
-                   ~ N(0, 0.02^2), seed 4 (A drawn first, then B).
+* ``ag_gemm``   -- P=8 row shards A_r [1024,4096] and the weight B
+                   [4096,4096], bf16 ~ N(0, 0.02^2), seed 4 (A's slots use
+                   streams (4, r), B uses (4, P)).
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
 import torch
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
-    g.manual_seed(seed)
-    return g
+def _fill(P: int, N: int, seed: int, draw) -> np.ndarray:
+    out = np.empty((P, N), dtype=np.float32)
+
+    def one(r):
+        draw(np.random.default_rng([seed, r]), out[r])
+
+    workers = max(1, min(P, os.cpu_count() or 1))
+    if workers == 1 or P * N < (1 << 22):
+        for r in range(P):
+            one(r)
+    else:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, range(P)))
+    return out
+
+
+def _uniform01(g, row):
+    g.random(out=row, dtype=np.float32)
+
+
+def _uniform_pm1(g, row):
+    g.random(out=row, dtype=np.float32)
+    row *= np.float32(2.0)   # exact
+    row -= np.float32(1.0)
+
+
+def _normal(g, row):
+    g.standard_normal(out=row, dtype=np.float32)
 
 
 def uniform01(P: int, N: int, seed: int = 0) -> torch.Tensor:
     """[P, N] fp32 ~ U[0, 1)."""
-    return torch.rand((P, N), generator=_gen(seed), dtype=torch.float32)
+    return torch.from_numpy(_fill(P, N, seed, _uniform01))
 
 
 def uniform_pm1(P: int, N: int, seed: int = 3) -> torch.Tensor:
     """[P, N] fp32 ~ U[-1, 1)."""
-    return torch.rand((P, N), generator=_gen(seed), dtype=torch.float32) * 2.0 - 1.0
+    return torch.from_numpy(_fill(P, N, seed, _uniform_pm1))
 
 
 def normal(P: int, N: int, seed: int = 1, std: float = 1.0, dtype=torch.float32) -> torch.Tensor:
-    """[P, N] ~ N(0, std^2), drawn in fp32 and cast to ``dtype``."""
-    x = torch.randn((P, N), generator=_gen(seed), dtype=torch.float32)
+    """[P, N] ~ N(0, std^2), drawn in fp32, scaled, then cast to ``dtype``."""
+    x = _fill(P, N, seed, _normal)
     if std != 1.0:
-        x = x * std
-    return x.to(dtype)
+        x *= np.float32(std)
+    t = torch.from_numpy(x)
+    return t if dtype == torch.float32 else t.to(dtype)
 
 
 def int_valued(P: int, N: int, seed: int = 1, lo: int = -1000, hi: int = 1000,
                dtype=torch.float32) -> torch.Tensor:
     """[P, N] integers uniform in [lo, hi], stored as ``dtype``."""
-    return torch.randint(lo, hi + 1, (P, N), generator=_gen(seed), dtype=torch.int64).to(dtype)
+    def draw(g, row):
+        row[:] = g.integers(lo, hi + 1, size=row.shape[0], dtype=np.int32)
+    t = torch.from_numpy(_fill(P, N, seed, draw))
+    return t if dtype == torch.float32 else t.to(dtype)
 
 
 def workload(name: str, P: int | None = None, N: int | None = None) -> torch.Tensor:
     """Inputs of a named workload as a CPU tensor [P, N]."""
     if name == "tiny":
-        P = 4 if P is None else P
-        return uniform01(P, 8 * 128 if N is None else N, seed=0)
+        return uniform01(4 if P is None else P, 8 * 128 if N is None else N, seed=0)
     if name == "f32_64mib":
         return normal(8 if P is None else P, (16 << 20) if N is None else N, seed=1)
     if name == "f32_int":
@@ -77,12 +108,15 @@ def workload(name: str, P: int | None = None, N: int | None = None) -> torch.Ten
 
 def ag_gemm_inputs(P: int = 8, M_r: int = 1024, K: int = 4096, N: int = 4096, seed: int = 4):
     """(A shards [P, M_r, K], B [N, K]) bf16 ~ N(0, 0.02^2)."""
-    g = _gen(seed)
-    a = (torch.randn((P, M_r, K), generator=g, dtype=torch.float32) * 0.02).to(torch.bfloat16)
-    b = (torch.randn((N, K), generator=g, dtype=torch.float32) * 0.02).to(torch.bfloat16)
-    return a, b
+    a = _fill(P, M_r * K, seed, _normal)
+    a *= np.float32(0.02)
+    b = np.empty((N * K,), dtype=np.float32)
+    np.random.default_rng([seed, P]).standard_normal(out=b, dtype=np.float32)
+    b *= np.float32(0.02)
+    return (torch.from_numpy(a).view(P, M_r, K).to(torch.bfloat16),
+            torch.from_numpy(b).view(N, K).to(torch.bfloat16))
 
 
-def bf16_bits(t: torch.Tensor):
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """numpy uint16 view of a CPU bf16 tensor (the bit pattern, no conversion)."""
-    return t.contiguous().view(torch.int16).numpy().view("uint16")
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -1,0 +1,314 @@
+"""GPU parity of the ring collectives against the oracle (needs a GB300).
+
+Every test calls the CUDA library through its C ABI (the Python binding only
+marshals arguments) and compares with the oracle on the same seeded inputs:
+bit for bit for f32 / bf16 (same ring order and per-hop rounding) and i32.
+Sizes span several slices and a ragged tail; the full-size cases are the
+workloads the benchmark times, checked against the full oracle simulation or,
+where that is too slow, against the oracle's closed form at sampled indices
+plus the property that every rank holds the same bits.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ring_collectives_gb300 as rc
+from ring_collectives_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+NAME = {torch.float32: "f32", torch.bfloat16: "bf16", torch.int32: "i32"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(DEV)
+    rc.ring_set_slices(0)
+    rc.ring_set_timeout_ms(2000)
+    yield
+    torch.cuda.synchronize()
+
+
+def np_of(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def make(P, N, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    if dtype == torch.int32:
+        return torch.randint(-2**31, 2**31 - 1, (P, N), generator=g, dtype=torch.int64).to(torch.int32)
+    x = torch.randn((P, N), generator=g, dtype=torch.float32)
+    return x.to(dtype)
+
+
+def ok_status():
+    st = rc.ring_status()
+    assert st == 0, rc.ring_last_error()
+
+
+# ------------------------------------------------------------------ all-reduce
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
+@pytest.mark.parametrize("P,c", [(2, 1), (2, 64), (3, 5), (4, 256), (4, 1000), (5, 3000), (7, 4099),
+                                 (8, 64 * 40 + 3), (8, 100_000), (16, 777), (32, 129), (64, 64)])
+def test_allreduce_matches_oracle(P, c, dtype):
+    N = P * c
+    x = make(P, N, dtype, seed=P * 1000 + c)
+    bufs = x.to(DEV)
+    rc.ring_allreduce(bufs)
+    ok_status()
+    want = oracle.ring_allreduce(np_of(x).copy(), NAME[dtype])
+    assert np.array_equal(np_of(bufs), want)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_allreduce_unaligned_layouts(dtype):
+    """Slot stride not a multiple of 16 bytes, and a base that is not 16-byte
+    aligned: the element-wise path must give the same bits."""
+    P, c = 4, 301
+    N = P * c
+    x = make(P, N, dtype, seed=5)
+    big = torch.zeros((P, N + 3), dtype=dtype, device=DEV)
+    big[:, :N] = x.to(DEV)
+    rc.ring_allreduce(big, N=N)          # stride (N+3)*e: not 16-byte multiple
+    ok_status()
+    want = oracle.ring_allreduce(np_of(x).copy(), NAME[dtype])
+    assert np.array_equal(np_of(big[:, :N]), want)
+    flat = torch.zeros(P * (N + 8) + 1, dtype=dtype, device=DEV)
+    view = flat[1:1 + P * (N + 8)].view(P, N + 8)   # base offset by one element
+    view[:, :N] = x.to(DEV)
+    rc.ring_allreduce(view, N=N)
+    ok_status()
+    assert np.array_equal(np_of(view[:, :N]), want)
+
+
+@pytest.mark.parametrize("P", [2, 3, 4, 8, 16, 31])
+def test_allreduce_i32_bitmask_and_positional(P):
+    c = 1024 + 7
+    N = P * c
+    x = torch.zeros((P, N), dtype=torch.int32)
+    for r in range(P):
+        x[r] = int(np.uint32(1 << r).astype(np.int32))
+    bufs = x.to(DEV)
+    rc.ring_allreduce(bufs)
+    ok_status()
+    assert np.all(np_of(bufs).view(np.uint32) == np.uint32((1 << P) - 1))
+    i = np.arange(N, dtype=np.int64)
+    pos = ((i[None, :] + (np.arange(P, dtype=np.int64)[:, None] << 16)) & 0xFFFFFFFF).astype(np.uint32)
+    bufs = torch.from_numpy(pos.view(np.int32)).to(DEV)
+    rc.ring_allreduce(bufs)
+    ok_status()
+    want = ((P * np.arange(N, dtype=np.int64) + (1 << 16) * P * (P - 1) // 2) & 0xFFFFFFFF).astype(np.uint32)
+    got = np_of(bufs).view(np.uint32)
+    for r in range(P):
+        assert np.array_equal(got[r], want)
+
+
+def test_allreduce_p1_and_empty_are_no_ops():
+    x = make(1, 100, torch.float32, 1).to(DEV)
+    y = x.clone()
+    rc.ring_allreduce(y)
+    assert torch.equal(x, y)
+    e = torch.zeros((4, 0), dtype=torch.float32, device=DEV)
+    rc.ring_allreduce(e)
+    ok_status()
+
+
+def test_allreduce_repeated_calls_and_mixed_shapes():
+    """Monotonic signal rows across many launches of different P / modes."""
+    for it in range(30):
+        P = [2, 8, 3, 16, 5][it % 5]
+        c = 513 + it
+        x = make(P, P * c, torch.int32, seed=it)
+        bufs = x.to(DEV)
+        rc.ring_allreduce(bufs)
+        if it % 3 == 0:
+            out = torch.empty((P, c), dtype=torch.int32, device=DEV)
+            b2 = x.to(DEV)
+            rc.ring_reduce_scatter(b2, out)
+            want_rs = oracle.reduce_scatter(np_of(x).copy(), "i32")
+            assert np.array_equal(np_of(out), want_rs)
+        want = oracle.ring_allreduce(np_of(x).copy(), "i32")
+        assert np.array_equal(np_of(bufs), want), it
+    ok_status()
+
+
+@pytest.mark.parametrize("S", [1, 3, 19, 64])
+def test_allreduce_slice_counts(S):
+    rc.ring_set_slices(S)
+    try:
+        P, c = 8, 64 * 97 + 13 * 4
+        x = make(P, P * c, torch.float32, seed=S)
+        bufs = x.to(DEV)
+        rc.ring_allreduce(bufs)
+        ok_status()
+        assert np.array_equal(np_of(bufs), oracle.ring_allreduce(np_of(x).copy(), "f32"))
+    finally:
+        rc.ring_set_slices(0)
+
+
+# ------------------------------------------------------------------ reduce-scatter
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
+@pytest.mark.parametrize("P,c", [(1, 100), (2, 7), (4, 256), (5, 1001), (8, 64 * 33 + 5), (16, 4096)])
+def test_reduce_scatter_matches_oracle(P, c, dtype):
+    N = P * c
+    x = make(P, N, dtype, seed=77 + P + c)
+    bufs = x.to(DEV)
+    out = torch.full((P, c), 0, dtype=dtype, device=DEV)
+    rc.ring_reduce_scatter(bufs, out)
+    ok_status()
+    ob = np_of(x).copy()
+    want = oracle.reduce_scatter(ob, NAME[dtype])
+    assert np.array_equal(np_of(out), want)
+    assert np.array_equal(np_of(bufs), ob)   # the clobbered partial sums agree too
+
+
+# ------------------------------------------------------------------ all-gather / ppermute
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
+@pytest.mark.parametrize("P,n", [(1, 10), (2, 3), (4, 1024), (5, 333), (8, 64 * 50 + 1), (32, 100)])
+def test_all_gather_matches_oracle(P, n, dtype):
+    x = make(P, n, dtype, seed=P + n)
+    out = torch.zeros((P, P * n), dtype=dtype, device=DEV)
+    rc.ring_all_gather(x.to(DEV), out)
+    ok_status()
+    assert np.array_equal(np_of(out), oracle.all_gather(np_of(x), NAME[dtype]))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
+@pytest.mark.parametrize("P,n", [(1, 5), (2, 1), (4, 1024), (7, 12345), (8, 1 << 20)])
+def test_ppermute_matches_oracle(P, n, dtype):
+    x = make(P, n, dtype, seed=3 * P + n)
+    dst = torch.zeros((P, n), dtype=dtype, device=DEV)
+    rc.ring_ppermute_right(x.to(DEV), dst)
+    torch.cuda.synchronize()
+    assert np.array_equal(np_of(dst), oracle.ppermute_right(np_of(x), NAME[dtype]))
+
+
+def test_tiny_workload_all_four_collectives_p4_and_p2():
+    """The (8,128) fp32 U[0,1) shards of the Pallas examples, P=4 and P=2."""
+    for P in (4, 2):
+        x = synthetic.workload("tiny", P=P)
+        xn = x.numpy()
+        b = x.to(DEV)
+        rc.ring_allreduce(b)
+        assert np.array_equal(np_of(b), oracle.ring_allreduce(xn.copy(), "f32"))
+        d = torch.empty_like(b)
+        rc.ring_ppermute_right(x.to(DEV), d)
+        assert np.array_equal(np_of(d), oracle.ppermute_right(xn, "f32"))
+        o = torch.empty((P, P * 1024), dtype=torch.float32, device=DEV)
+        rc.ring_all_gather(x.to(DEV), o)
+        assert np.array_equal(np_of(o), oracle.all_gather(xn, "f32"))
+        rs = torch.empty((P, 1024 // P), dtype=torch.float32, device=DEV)
+        rc.ring_reduce_scatter(x.to(DEV), rs)
+        assert np.array_equal(np_of(rs), oracle.reduce_scatter(xn.copy(), "f32"))
+        ok_status()
+
+
+# ------------------------------------------------------------------ failure detection
+def test_bounded_wait_reports_timeout_and_device_stays_usable():
+    """A skipped notify (host-side test hook) makes the right neighbour's
+    bounded wait run out: the kernel returns, ring_status reports
+    RC_ERR_TIMEOUT, and the next call is correct."""
+    rc.ring_set_timeout_ms(100)
+    try:
+        P, c = 4, 4096
+        x = make(P, P * c, torch.float32, seed=9)
+        b = x.to(DEV)
+        rc.ring_debug_skip_notify(1, 2)
+        rc.ring_allreduce(b)
+        st = rc.ring_status()
+        assert st == rc.RC_ERR_TIMEOUT
+        assert "timed out" in rc.ring_last_error()
+        b = x.to(DEV)
+        rc.ring_allreduce(b)
+        ok_status()
+        assert np.array_equal(np_of(b), oracle.ring_allreduce(np_of(x).copy(), "f32"))
+    finally:
+        rc.ring_set_timeout_ms(2000)
+
+
+def test_host_entry_point_matches_oracle():
+    P, c = 8, 10_000
+    x = make(P, P * c, torch.float32, seed=21)
+    h_in = x.pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    d = torch.empty((P, P * c), dtype=torch.float32, device=DEV)
+    rc.ring_allreduce_host(h_in, h_out, d)
+    torch.cuda.synchronize()
+    ok_status()
+    assert np.array_equal(h_out.numpy(), oracle.ring_allreduce(x.numpy().copy(), "f32"))
+
+
+# ------------------------------------------------------------------ full-size workloads
+def test_full_f32_64mib_p8_bit_exact():
+    """P=8, 16M fp32 per rank ~ N(0,1) seed 1: the benchmark's workload."""
+    x = synthetic.workload("f32_64mib")
+    bufs = x.to(DEV)
+    rc.ring_allreduce(bufs)
+    ok_status()
+    want = oracle.ring_allreduce(x.numpy().copy(), "f32")
+    assert np.array_equal(np_of(bufs), want)
+    naive = oracle.naive_sum(x.numpy(), "f32").astype(np.float64)
+    got0 = np_of(bufs[0]).astype(np.float64)
+    absx = np.abs(x.numpy()).astype(np.float64).sum(axis=0)
+    # elementwise bound scaled by sum|x| (a plain relative error explodes where the sum is ~0)
+    assert np.all(np.abs(got0 - naive) <= 1e-5 * 8 * absx)
+    big = np.abs(naive) > 1e-3 * np.sqrt(np.mean(naive ** 2))
+    assert np.max(np.abs(got0 - naive)[big] / np.abs(naive)[big]) <= 1e-5 * 8
+
+
+def test_full_f32_integer_valued_exact():
+    x = synthetic.workload("f32_int")
+    bufs = x.to(DEV)
+    rc.ring_allreduce(bufs)
+    ok_status()
+    exact = x.to(torch.int64).sum(dim=0).to(torch.float32).to(DEV)
+    for r in range(8):
+        assert torch.equal(bufs[r], exact)
+
+
+def test_full_bf16_64mib_allreduce_and_reduce_scatter_bit_exact():
+    x = synthetic.workload("bf16_64mib")
+    xn = np_of(x)
+    bufs = x.to(DEV)
+    rc.ring_allreduce(bufs)
+    ok_status()
+    assert np.array_equal(np_of(bufs), oracle.ring_allreduce(xn.copy(), "bf16"))
+    b2 = x.to(DEV)
+    out = torch.empty((8, xn.shape[1] // 8), dtype=torch.bfloat16, device=DEV)
+    rc.ring_reduce_scatter(b2, out)
+    ok_status()
+    assert np.array_equal(np_of(out), oracle.reduce_scatter(xn.copy(), "bf16"))
+
+
+@pytest.mark.parametrize("P", [2, 4, 8, 16, 32])
+def test_weak_scaling_workload(P):
+    """Chunk 4M fp32 ~ U[-1,1) seed 3: the full oracle for P <= 8; above that
+    the closed form at sampled indices (every chunk, both ends) and all ranks
+    bit-identical."""
+    x = synthetic.workload("weak", P=P)
+    bufs = x.to(DEV)
+    rc.ring_allreduce(bufs)
+    ok_status()
+    N = x.shape[1]
+    if P <= 8:
+        assert np.array_equal(np_of(bufs), oracle.ring_allreduce(x.numpy().copy(), "f32"))
+    else:
+        c = N // P
+        rng = np.random.default_rng(P)
+        idx = np.unique(np.concatenate([np.arange(P) * c, np.arange(1, P + 1) * c - 1,
+                                        rng.integers(0, N, 4096)]))
+        want = oracle.ring_fold_at(x.numpy(), "f32", idx)
+        got = bufs[:, torch.from_numpy(idx).to(DEV)].cpu().numpy()
+        for r in range(P):
+            assert np.array_equal(got[r], want)
+        for r in range(1, P):
+            assert torch.equal(bufs[r], bufs[0])
+    del bufs
+    torch.cuda.empty_cache()
