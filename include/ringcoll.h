@@ -190,6 +190,42 @@ int ring_debug_skip_notify(int rank, int step);
 /* Frees the signal workspaces of all devices.  No call may be in flight. */
 int ring_finalize(void);
 
+/*
+ * ring_allreduce_noalloc -- ring_allreduce for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this entry point exists
+ * only because of how some callers run.
+ *
+ * ring_allreduce creates its signal workspace with cudaMalloc (and a
+ * device-wide synchronisation) on the first call, and again whenever a larger
+ * P needs a bigger one.  Some callers cannot allow that: a process whose
+ * framework allocator already holds nearly all of the GPU's memory (so a
+ * library cudaMalloc fails), code that must never trigger an allocation or an
+ * implicit device synchronisation in its steady state, and runtimes that
+ * forbid libraries from owning device allocations.  This variant keeps its
+ * signal rows in a fixed array compiled into the library instead:
+ * RC_NOALLOC_SCRATCH_BYTES bytes of device memory that every GPU which loads
+ * the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Arguments, layout, validation and result: as ring_allreduce (the same
+ * kernel runs; the result is bit-identical).  Additional limit: the signal
+ * rows of one call, slices*P*2(P-1)*P words plus a 128-byte header, must fit
+ * in the array; the slice count is reduced to fit, and P for which even one
+ * slice does not fit (P > 32) is rejected with RC_ERR_INVALID.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress and clears the array with
+ * cudaMemsetAsync on `stream`; make that first call before any stream
+ * capture.  Every call on a device shares the one array, which keeps the last
+ * call's contents (signal rows hold epoch values, so nothing needs clearing
+ * between calls).  Calls that overlap on the GPU -- on different streams
+ * without ordering, or on different host threads -- race on the array and
+ * give undefined results; issue them in stream order.  Errors raised by a
+ * device wait are reported in the array, not read by ring_status().
+ */
+#define RC_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -212,3 +212,20 @@ def ring_debug_skip_notify(rank: int, step: int) -> None:
 
 def ring_finalize() -> None:
     _check(load().ring_finalize())
+
+
+def ring_allreduce_noalloc(bufs: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
+    """ring_allreduce without any device allocation by the library: the signal
+    rows live in a fixed 256 KiB array compiled into the library (P <= 32).
+    For callers that cannot let a library allocate device memory; see the
+    declaration in include/ringcoll.h for set-up and ordering rules."""
+    L = load()
+    fn = L.ring_allreduce_noalloc
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t, ctypes.c_int,
+                   ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    bp, bs, dt = _slots(bufs, "bufs")
+    N = bufs.size(1) if N is None else N
+    with torch.cuda.device(bufs.device):
+        _check(fn(bp, bs, bufs.size(0), N, dt, _stream(stream, bufs.device)))
+    return bufs

@@ -365,6 +365,81 @@ int ring_status(void *stream)
                 h.err_slice);
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free all-reduce.  Its scratch (workspace header + signal rows)
+// is this file-scope device array instead of a cudaMalloc'd workspace.  In
+// host code the name g_noalloc_scratch is only a host-side stand-in, so the
+// device address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint32_t g_noalloc_scratch[RC_NOALLOC_SCRATCH_BYTES / 4];
+
+namespace {
+struct NoAllocState {
+    void *ptr = nullptr;     // device address of g_noalloc_scratch on this device
+    uint64_t launches = 0;   // launches since the array was last cleared
+};
+NoAllocState g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+} // namespace
+
+int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
+    if (N == 0 || P == 1) return RC_OK;
+    if (!bufs_base) return fail(RC_ERR_INVALID, "null slot base");
+    if (stride < N * es) return fail(RC_ERR_INVALID, "stride %zu below the %zu bytes of a slot", stride, N * es);
+    const size_t rows = 2 * (size_t)(P - 1);
+    const size_t avail_words = (RC_NOALLOC_SCRATCH_BYTES - sizeof(rc::WsHeader)) / 4;
+    const size_t words_per_slice = (size_t)P * rows * (size_t)P;
+    if (words_per_slice > avail_words)
+        return fail(RC_ERR_INVALID, "P=%d needs %zu signal words per slice; the static scratch holds %zu (P <= 32)",
+                    P, words_per_slice, avail_words);
+
+    int dev;
+    DeviceState *st = nullptr;
+    int rc_ = current_device(&dev, &st);
+    if (rc_) return rc_;
+    const size_t c = N / (size_t)P;
+    rc::RingParams p{};
+    rc_ = choose_slices(*st, dtype, P, c, c * es, &p.S);
+    if (rc_) return rc_;
+    if ((size_t)p.S * words_per_slice > avail_words) p.S = (int)(avail_words / words_per_slice);
+
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocState &na = g_noalloc[dev];
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!na.ptr || na.launches >= kEpochResetAt) {
+        if (!na.ptr) {
+            void *ptr = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+            na.ptr = ptr;
+        }
+        // Signal rows and the header's epoch, done counter and status start at zero.
+        cudaError_t e = cudaMemsetAsync(na.ptr, 0, RC_NOALLOC_SCRATCH_BYTES, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch");
+        na.launches = 0;
+    }
+    p.data = (char *)bufs_base;
+    p.data_stride = stride;
+    p.chunk = c;
+    p.P = P;
+    p.rows = (int)rows;
+    p.mode = rc::MODE_ALLREDUCE;
+    p.vec_ok = aligned16(bufs_base) && stride % 16 == 0 && (c * es) % 16 == 0;
+    p.hdr = (rc::WsHeader *)na.ptr;
+    p.sig = (uint32_t *)((char *)na.ptr + sizeof(rc::WsHeader));
+    p.timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
+    p.skip_rank = -1;
+    p.skip_step = -1;
+    cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
+    na.launches++;
+    return RC_OK;
+}
+
 int ring_finalize(void)
 {
     std::lock_guard<std::mutex> lock(g_mu);
