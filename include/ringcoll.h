@@ -19,10 +19,11 @@
  *     stream).  Every call is asynchronous on it: the return value reports
  *     argument validation and launch errors only; errors raised on the device
  *     (a bounded wait that ran out) are read with ring_status().
- *   - Alignment: when the base pointers and strides are 16-byte aligned and
- *     the chunk size keeps chunk starts 16-byte aligned, kernels move data in
- *     16-byte vectors; otherwise they fall back to element-wise access.
- *     Misalignment is never an error.
+ *   - Alignment: slot bases and strides must be multiples of the element
+ *     size (RC_ERR_INVALID otherwise).  Kernels move the body of every range
+ *     in 32-byte vectors when source and destination share their offset
+ *     modulo 32 bytes (always, for 32-byte multiple strides), with element-wise
+ *     heads and tails; other layouts run element-wise.
  *   - Degenerate sizes: n = 0 or N = 0 does nothing and returns RC_OK.
  *   - The library owns one signal workspace per device, created on the first
  *     call on that device (a cudaMalloc and a synchronous zeroing), grown on
@@ -94,8 +95,9 @@ int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_
  *     R[k] = ((x_{k+1} + x_{k+2}) + ... + x_{k+P-1}) + x_k   (indices mod P)
  * with "+" the element type's hop add (f32: IEEE binary32 add; bf16: add in
  * binary32, round the partial sum to bf16 at every hop; i32: wrapping add).
- * bufs slots: [N] elements at bufs_base + r*bufs_stride; CLOBBERED: they are
- *     left holding the partial sums of rounds 0..P-3.
+ * bufs slots: [N] elements at bufs_base + r*bufs_stride; CLOBBERED: their
+ *     contents are undefined after the call (they hold partial sums, and the
+ *     L2 lines of partials that are dead are dropped without write-back).
  * out slots:  [N/P] elements at out_base + r*out_stride (written); out must
  *     not overlap bufs.
  * N must be a multiple of P ("SIZE 必须能被 rank 数量整除", same page);
@@ -186,6 +188,18 @@ int ring_set_slices(int slices);
  * (-1, -1) cancels a pending skip.
  */
 int ring_debug_skip_notify(int rank, int step);
+
+/*
+ * Tracing hook: while dev_buf is set (a device buffer of `bytes` bytes), every
+ * ring launch (ring_all_gather, ring_reduce_scatter, ring_allreduce) has
+ * thread 0 of block b (rank b / slices, slice b % slices) write three
+ * %globaltimer stamps (ns) per global step g at word (b*steps + g)*3: the
+ * start of the wait on the left neighbour, its end, and the end of the step
+ * (after the notify).  steps = 2(P-1) for the all-reduce, P-1 otherwise.
+ * Blocks whose stamps would not fit write none.  NULL turns tracing off.
+ * The caller owns the buffer and must keep it alive while launches use it.
+ */
+int ring_debug_set_trace(void *dev_buf, size_t bytes);
 
 /* Frees the signal workspaces of all devices.  No call may be in flight. */
 int ring_finalize(void);

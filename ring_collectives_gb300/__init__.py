@@ -214,6 +214,18 @@ def ring_finalize() -> None:
     _check(load().ring_finalize())
 
 
+def ring_debug_set_trace(buf) -> None:
+    """Step stamps of later ring launches go to ``buf`` (a CUDA uint64/int64
+    tensor) -- see ring_debug_set_trace in include/ringcoll.h; None: off."""
+    fn = load().ring_debug_set_trace
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    fn.restype = ctypes.c_int
+    if buf is None:
+        _check(fn(None, 0))
+    else:
+        _check(fn(buf.data_ptr(), buf.numel() * buf.element_size()))
+
+
 def ring_allreduce_noalloc(bufs: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
     """ring_allreduce without any device allocation by the library: the signal
     rows live in a fixed 256 KiB array compiled into the library (P <= 32).

@@ -17,6 +17,8 @@ thread_local std::string g_err;
 std::atomic<unsigned> g_timeout_ms{2000};
 std::atomic<int> g_slices{0};
 std::atomic<int> g_skip_rank{-1}, g_skip_step{-1};
+std::atomic<unsigned long long *> g_trace{nullptr};
+std::atomic<size_t> g_trace_words{0};
 std::mutex g_mu;
 
 constexpr int kMaxDevices = 64;
@@ -60,7 +62,11 @@ size_t elem_size(int dtype)
     }
 }
 
-bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+// Element accesses need element-aligned slots: base and stride multiples of the element size.
+bool elem_aligned(const void *base, size_t stride, size_t es)
+{
+    return ((uintptr_t)base % es) == 0 && (stride % es) == 0;
+}
 
 // [lo, hi) byte range spanned by P slots of `bytes` each.
 bool regions_overlap(const void *a, size_t a_stride, size_t a_bytes, const void *b, size_t b_stride,
@@ -150,7 +156,7 @@ int choose_slices(const DeviceState &st, int dtype, int P, size_t chunk_elems, s
     if (user > 0) {
         S = user;
     } else {
-        S = (long)(2 * st.sm_count) / P; // about two blocks per SM in total
+        S = cap; // every co-resident block slot of the GPU holds one (rank, slice)
         const long by_size = (long)(chunk_bytes / kMinSliceBytes);
         if (S > by_size) S = by_size;
     }
@@ -180,6 +186,8 @@ int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda)
     p.timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
     p.skip_rank = g_skip_rank.exchange(-1);
     p.skip_step = g_skip_step.exchange(-1);
+    p.trace = g_trace.load();
+    p.trace_words = g_trace_words.load();
     cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, st_cuda);
     if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
     st->launches++;
@@ -194,9 +202,8 @@ int run_copy(const void *src, size_t src_stride, void *dst, size_t dst_stride, i
     int rc_ = current_device(&dev, &st);
     if (rc_) return rc_;
     const size_t es = elem_size(dtype);
-    const int vec_ok = aligned16(src) && aligned16(dst) && (src_stride % 16 == 0) && (dst_stride % 16 == 0);
     cudaError_t e = rc::launch_ppermute((const char *)src, src_stride, (char *)dst, dst_stride, P, n, (int)es,
-                                        vec_ok, st->sm_count, s);
+                                        st->sm_count, s);
     if (e != cudaSuccess) return cuda_fail(e, "copy kernel launch");
     return RC_OK;
 }
@@ -229,6 +236,14 @@ int ring_debug_skip_notify(int rank, int step)
     return RC_OK;
 }
 
+int ring_debug_set_trace(void *dev_buf, size_t bytes)
+{
+    if (!dev_buf) bytes = 0;
+    g_trace_words.store(bytes / 8);
+    g_trace.store((unsigned long long *)dev_buf);
+    return RC_OK;
+}
+
 int ring_ppermute_right(const void *src_base, size_t src_stride, void *dst_base, size_t dst_stride, int P,
                         size_t n, int dtype, void *stream)
 {
@@ -241,6 +256,8 @@ int ring_ppermute_right(const void *src_base, size_t src_stride, void *dst_base,
         return fail(RC_ERR_INVALID, "stride below the %zu bytes of a slot", n * es);
     if (regions_overlap(src_base, src_stride, n * es, dst_base, dst_stride, n * es, P))
         return fail(RC_ERR_INVALID, "src and dst slots overlap");
+    if (!elem_aligned(src_base, src_stride, es) || !elem_aligned(dst_base, dst_stride, es))
+        return fail(RC_ERR_INVALID, "slot bases and strides must be multiples of the %zu-byte element", es);
     return run_copy(src_base, src_stride, dst_base, dst_stride, P, n, dtype, (cudaStream_t)stream);
 }
 
@@ -256,6 +273,8 @@ int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_
         return fail(RC_ERR_INVALID, "stride below a slot's bytes (in %zu, out %zu)", n * es, (size_t)P * n * es);
     if (regions_overlap(in_base, in_stride, n * es, out_base, out_stride, (size_t)P * n * es, P))
         return fail(RC_ERR_INVALID, "in and out slots overlap");
+    if (!elem_aligned(in_base, in_stride, es) || !elem_aligned(out_base, out_stride, es))
+        return fail(RC_ERR_INVALID, "slot bases and strides must be multiples of the %zu-byte element", es);
     if (P == 1) return run_copy(in_base, in_stride, out_base, out_stride, 1, n, dtype, (cudaStream_t)stream);
     rc::RingParams p{};
     p.data = (char *)out_base;
@@ -266,8 +285,7 @@ int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_
     p.P = P;
     p.rows = P - 1;
     p.mode = rc::MODE_ALL_GATHER;
-    p.vec_ok = aligned16(in_base) && aligned16(out_base) && in_stride % 16 == 0 && out_stride % 16 == 0 &&
-               (n * es) % 16 == 0;
+    p.discard = 0;
     return run_ring(p, dtype, (cudaStream_t)stream);
 }
 
@@ -285,6 +303,8 @@ int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, siz
         return fail(RC_ERR_INVALID, "stride below a slot's bytes (bufs %zu, out %zu)", N * es, c * es);
     if (regions_overlap(bufs_base, bufs_stride, N * es, out_base, out_stride, c * es, P))
         return fail(RC_ERR_INVALID, "bufs and out slots overlap");
+    if (!elem_aligned(bufs_base, bufs_stride, es) || !elem_aligned(out_base, out_stride, es))
+        return fail(RC_ERR_INVALID, "slot bases and strides must be multiples of the %zu-byte element", es);
     if (P == 1) return run_copy(bufs_base, bufs_stride, out_base, out_stride, 1, c, dtype, (cudaStream_t)stream);
     rc::RingParams p{};
     p.data = (char *)bufs_base;
@@ -295,8 +315,7 @@ int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, siz
     p.P = P;
     p.rows = P - 1;
     p.mode = rc::MODE_REDUCE_SCATTER;
-    p.vec_ok = aligned16(bufs_base) && aligned16(out_base) && bufs_stride % 16 == 0 && out_stride % 16 == 0 &&
-               (c * es) % 16 == 0;
+    p.discard = 1;
     return run_ring(p, dtype, (cudaStream_t)stream);
 }
 
@@ -309,6 +328,8 @@ int ring_allreduce(void *bufs_base, size_t stride, int P, size_t N, int dtype, v
     if (N == 0 || P == 1) return RC_OK;
     if (!bufs_base) return fail(RC_ERR_INVALID, "null slot base");
     if (stride < N * es) return fail(RC_ERR_INVALID, "stride %zu below the %zu bytes of a slot", stride, N * es);
+    if (!elem_aligned(bufs_base, stride, es))
+        return fail(RC_ERR_INVALID, "slot base and stride must be multiples of the %zu-byte element", es);
     const size_t c = N / (size_t)P;
     rc::RingParams p{};
     p.data = (char *)bufs_base;
@@ -317,7 +338,7 @@ int ring_allreduce(void *bufs_base, size_t stride, int P, size_t N, int dtype, v
     p.P = P;
     p.rows = 2 * (P - 1);
     p.mode = rc::MODE_ALLREDUCE;
-    p.vec_ok = aligned16(bufs_base) && stride % 16 == 0 && (c * es) % 16 == 0;
+    p.discard = 1;
     return run_ring(p, dtype, (cudaStream_t)stream);
 }
 
@@ -390,6 +411,8 @@ int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int 
     if (N == 0 || P == 1) return RC_OK;
     if (!bufs_base) return fail(RC_ERR_INVALID, "null slot base");
     if (stride < N * es) return fail(RC_ERR_INVALID, "stride %zu below the %zu bytes of a slot", stride, N * es);
+    if (!elem_aligned(bufs_base, stride, es))
+        return fail(RC_ERR_INVALID, "slot base and stride must be multiples of the %zu-byte element", es);
     const size_t rows = 2 * (size_t)(P - 1);
     const size_t avail_words = (RC_NOALLOC_SCRATCH_BYTES - sizeof(rc::WsHeader)) / 4;
     const size_t words_per_slice = (size_t)P * rows * (size_t)P;
@@ -428,7 +451,7 @@ int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int 
     p.P = P;
     p.rows = (int)rows;
     p.mode = rc::MODE_ALLREDUCE;
-    p.vec_ok = aligned16(bufs_base) && stride % 16 == 0 && (c * es) % 16 == 0;
+    p.discard = 1;
     p.hdr = (rc::WsHeader *)na.ptr;
     p.sig = (uint32_t *)((char *)na.ptr + sizeof(rc::WsHeader));
     p.timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;

@@ -92,6 +92,49 @@ __device__ __forceinline__ void st_u16(void *p, uint16_t v)
     asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
 }
 
+// 32-byte vectors (sm_100+ 256-bit global accesses).  Ring loads are the last
+// use of their data on this step, so they carry L1::no_allocate and
+// L2::evict_first: the just-written partials and chunks the neighbours read
+// next keep their L2 lines instead.  Stores use the default policy, except the
+// last all-gather step, whose output no one reads again (evict_first).
+__device__ __forceinline__ void ld8_ef(const void *p, uint4 &a, uint4 &b)
+{
+    asm volatile("ld.global.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p)
+                 : "memory");
+}
+
+// Store policies: kStNormal (output read by a neighbour next step), kStEvictFirst
+// (nothing reads it again in this launch), kStEvictLast (a reduce-scatter
+// partial: it must survive in L2 until the right neighbour reads it, which then
+// drops it without write-back).
+enum { kStNormal = 0, kStEvictFirst = 1, kStEvictLast = 2 };
+
+template <int POL>
+__device__ __forceinline__ void st8(void *p, const uint4 &a, const uint4 &b)
+{
+    if (POL == kStEvictFirst)
+        asm volatile("st.global.L1::no_allocate.L2::evict_first.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+                     "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                     : "memory");
+    else if (POL == kStEvictLast)
+        asm volatile("st.global.L1::no_allocate.L2::evict_last.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+                     "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                     : "memory");
+    else
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+                     "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                     : "memory");
+}
+
+// Drops one 128-byte L2 line without writing it back; the memory behind it is
+// undefined afterwards, so only lines whose data is dead may be discarded.
+__device__ __forceinline__ void discard_l2_line(const void *p)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // ------------------------------------------------------------ hop add
 // Element types: 0 = f32, 1 = bf16, 2 = i32.
 // f32: IEEE binary32 add, round to nearest even, subnormals kept (the library

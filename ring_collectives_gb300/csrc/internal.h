@@ -33,19 +33,31 @@ struct RingParams {
     WsHeader *hdr;
     size_t chunk;        // elements per chunk (all-gather: the shard length n)
     int P, S, rows, mode;
-    int vec_ok;          // 1: every slot/chunk start is 16-byte aligned -> 16-byte vectors
+    int discard;         // 1: drop the L2 lines of reduce-scatter partials once read (their data is dead)
     int skip_rank, skip_step; // test hook: this rank skips its notify after this step (-1: none)
     unsigned long long timeout_ns;
+    unsigned long long *trace; // optional step stamps (see ring_debug_set_trace); null: off
+    size_t trace_words;
 };
 
 // Launch helpers implemented in ring_kernels.cu.  They return a cudaError_t.
 cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_t st);
 cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks);
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P,
-                            size_t n, int esize, int vec_ok, int sm_count, cudaStream_t st);
+                            size_t n, int esize, int sm_count, cudaStream_t st);
 
-// Threads per block of the ring kernel.
-constexpr int kRingThreads = 512;
+// Threads per block of the ring kernel, and the blocks per SM its register
+// budget is sized for (build-time tuning knobs).
+// Small blocks, many per SM: while some blocks wait on their left neighbour
+// or drain a step, the others keep streaming (measured on GB300: 128 x 8 per
+// SM beats 512 x 2 and 1024 x 1 by about 10 %).
+#ifndef RC_RING_THREADS
+#define RC_RING_THREADS 128
+#endif
+#ifndef RC_RING_MIN_BLOCKS
+#define RC_RING_MIN_BLOCKS 8
+#endif
+constexpr int kRingThreads = RC_RING_THREADS;
 // Slices start on multiples of this many elements (keeps 16-byte vectors aligned).
 constexpr size_t kSliceGranule = 64;
 

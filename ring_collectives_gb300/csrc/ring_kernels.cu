@@ -30,8 +30,6 @@
 
 namespace rc {
 
-constexpr int kUnroll = 4; // 16-byte vectors in flight per thread and operand
-
 // First element of slice j of a chunk of c elements (slices are granule-aligned).
 __device__ __forceinline__ size_t slice_begin(size_t c, int j, int S)
 {
@@ -41,54 +39,74 @@ __device__ __forceinline__ size_t slice_begin(size_t c, int j, int S)
 }
 
 // ------------------------------------------------------------ block-wide streams
-// dst[i] = a[i] (+) b[i] over nvec 16-byte vectors, strided over the block.
-// T is the block size (a compile-time constant, so the unrolled offsets are
-// immediates and only the three running pointers stay live).
-template <int DT, int T>
-__device__ __forceinline__ void add_vec(char *dst, const char *a, const char *b, size_t nvec)
+// Bodies move 32-byte vectors strided over the T threads of the block (T is a
+// compile-time constant, so the unrolled offsets are immediates); each thread
+// keeps 2 (add) or 4 (copy) vectors per operand in flight.
+
+// dst[i] = a[i] (+) b[i] over n32 32-byte vectors.  The unrolled loop is
+// warp-uniform (every lane runs the same iterations).  With `discard`, each warp
+// drops the L2 lines of `a` it has just consumed (when `discard` is set): after __syncwarp every lane's
+// loads have returned (its store used them), so lane l discards line l of the
+// warp's two 1 KiB pieces.  Only done when `a` is 128-byte aligned, so every
+// discarded line lies wholly inside this warp's piece of the range.
+template <int DT, int T, int POL>
+__device__ __forceinline__ void add_vec32(char *dst, const char *a, const char *b, size_t n32, bool discard)
 {
-    size_t v = threadIdx.x;
-    const char *pa = a + v * 16, *pb = b + v * 16;
-    char *pd = dst + v * 16;
-    for (; v + (kUnroll - 1) * T < nvec; v += kUnroll * T) {
-        uint4 x[kUnroll], y[kUnroll];
+    constexpr int U = 2;
+    const size_t lane = threadIdx.x & 31u;
+    size_t vw = threadIdx.x - lane; // first vector of this warp
+    const bool dline = discard && (((uintptr_t)a & 127u) == 0);
+    for (; vw + 31 + (U - 1) * T < n32; vw += U * T) {
+        const size_t v = vw + lane;
+        uint4 x0[U], x1[U], y0[U], y1[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            x[u] = ld_cg_v4(pa + u * T * 16);
-            y[u] = ld_cg_v4(pb + u * T * 16);
+        for (int u = 0; u < U; ++u) {
+            ld8_ef(a + (v + u * T) * 32, x0[u], x1[u]);
+            ld8_ef(b + (v + u * T) * 32, y0[u], y1[u]);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) st_v4(pd + u * T * 16, hop_add_v4<DT>(x[u], y[u]));
-        pa += kUnroll * T * 16;
-        pb += kUnroll * T * 16;
-        pd += kUnroll * T * 16;
+        for (int u = 0; u < U; ++u)
+            st8<POL>(dst + (v + u * T) * 32, hop_add_v4<DT>(x0[u], y0[u]), hop_add_v4<DT>(x1[u], y1[u]));
+        if (dline) {
+            __syncwarp();
+            if (lane < 8 * U) discard_l2_line(a + (vw + (lane >> 3) * T) * 32 + (lane & 7) * 128);
+        }
     }
-    for (; v < nvec; v += T, pa += T * 16, pb += T * 16, pd += T * 16)
-        st_v4(pd, hop_add_v4<DT>(ld_cg_v4(pa), ld_cg_v4(pb)));
+    for (size_t v = vw + lane; v < n32; v += T) {
+        uint4 x0, x1, y0, y1;
+        ld8_ef(a + v * 32, x0, x1);
+        ld8_ef(b + v * 32, y0, y1);
+        st8<POL>(dst + v * 32, hop_add_v4<DT>(x0, y0), hop_add_v4<DT>(x1, y1));
+    }
 }
 
-template <int T>
-__device__ __forceinline__ void copy_vec(char *dst, const char *src, size_t nvec)
+template <int T, int POL>
+__device__ __forceinline__ void copy_vec32(char *dst, const char *src, size_t n32)
 {
+    constexpr int U = 4;
     size_t v = threadIdx.x;
-    const char *ps = src + v * 16;
-    char *pd = dst + v * 16;
-    for (; v + (kUnroll - 1) * T < nvec; v += kUnroll * T) {
-        uint4 x[kUnroll];
+    const char *ps = src + v * 32;
+    char *pd = dst + v * 32;
+    for (; v + (U - 1) * T < n32; v += U * T) {
+        uint4 x0[U], x1[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) x[u] = ld_cg_v4(ps + u * T * 16);
+        for (int u = 0; u < U; ++u) ld8_ef(ps + u * T * 32, x0[u], x1[u]);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) st_v4(pd + u * T * 16, x[u]);
-        ps += kUnroll * T * 16;
-        pd += kUnroll * T * 16;
+        for (int u = 0; u < U; ++u) st8<POL>(pd + u * T * 32, x0[u], x1[u]);
+        ps += U * T * 32;
+        pd += U * T * 32;
     }
-    for (; v < nvec; v += T, ps += T * 16, pd += T * 16) st_v4(pd, ld_cg_v4(ps));
+    for (; v < n32; v += T, ps += T * 32, pd += T * 32) {
+        uint4 x0, x1;
+        ld8_ef(ps, x0, x1);
+        st8<POL>(pd, x0, x1);
+    }
 }
 
-template <int DT>
+template <int DT, int T>
 __device__ __forceinline__ void add_scalar(char *dst, const char *a, const char *b, size_t n)
 {
-    for (size_t i = threadIdx.x; i < n; i += blockDim.x) {
+    for (size_t i = threadIdx.x; i < n; i += T) {
         if (DT == 1)
             st_u16(dst + 2 * i, add_bf16_bits(ld_cg_u16(a + 2 * i), ld_cg_u16(b + 2 * i)));
         else if (DT == 0)
@@ -98,10 +116,10 @@ __device__ __forceinline__ void add_scalar(char *dst, const char *a, const char 
     }
 }
 
-template <int ES>
+template <int ES, int T>
 __device__ __forceinline__ void copy_scalar(char *dst, const char *src, size_t n)
 {
-    for (size_t i = threadIdx.x; i < n; i += blockDim.x) {
+    for (size_t i = threadIdx.x; i < n; i += T) {
         if (ES == 2)
             st_u16(dst + 2 * i, ld_cg_u16(src + 2 * i));
         else
@@ -109,30 +127,49 @@ __device__ __forceinline__ void copy_scalar(char *dst, const char *src, size_t n
     }
 }
 
-// n elements; vec: all three pointers are 16-byte aligned.
-template <int DT, int T>
-__device__ __forceinline__ void add_range(char *dst, const char *a, const char *b, size_t n, bool vec)
+// Elements before the first 32-byte boundary of dst (all pointers must share
+// dst's offset modulo 32 for the vector body to apply; otherwise the whole
+// range is element-wise).
+template <int ES>
+__device__ __forceinline__ size_t vec_head(const void *dst, size_t n)
 {
-    constexpr size_t ES = DT == 1 ? 2 : 4;
-    size_t head = 0;
-    if (vec) {
-        const size_t nvec = (n * ES) / 16;
-        add_vec<DT, T>(dst, a, b, nvec);
-        head = nvec * 16 / ES;
-    }
-    add_scalar<DT>(dst + head * ES, a + head * ES, b + head * ES, n - head);
+    const size_t mis = (uintptr_t)dst & 31u;
+    const size_t h = mis ? (32 - mis) / ES : 0;
+    return h < n ? h : n;
 }
 
-template <int ES, int T>
-__device__ __forceinline__ void copy_range(char *dst, const char *src, size_t n, bool vec)
+// dst[i] = a[i] (+) b[i], i < n.  discard: a's data is dead after this read
+// (see add_vec32).
+template <int DT, int T, int POL>
+__device__ __forceinline__ void add_range(char *dst, const char *a, const char *b, size_t n, bool discard)
 {
-    size_t head = 0;
-    if (vec) {
-        const size_t nvec = (n * ES) / 16;
-        copy_vec<T>(dst, src, nvec);
-        head = nvec * 16 / ES;
+    constexpr size_t ES = DT == 1 ? 2 : 4;
+    const bool same = ((((uintptr_t)dst ^ (uintptr_t)a) | ((uintptr_t)dst ^ (uintptr_t)b)) & 31u) == 0;
+    if (!same) {
+        add_scalar<DT, T>(dst, a, b, n);
+        return;
     }
-    copy_scalar<ES>(dst + head * ES, src + head * ES, n - head);
+    const size_t h = vec_head<ES>(dst, n);
+    add_scalar<DT, T>(dst, a, b, h);
+    const size_t n32 = (n - h) * ES / 32;
+    add_vec32<DT, T, POL>(dst + h * ES, a + h * ES, b + h * ES, n32, discard);
+    const size_t done = h + n32 * 32 / ES;
+    add_scalar<DT, T>(dst + done * ES, a + done * ES, b + done * ES, n - done);
+}
+
+template <int ES, int T, int POL>
+__device__ __forceinline__ void copy_range(char *dst, const char *src, size_t n)
+{
+    if ((((uintptr_t)dst ^ (uintptr_t)src) & 31u) != 0) {
+        copy_scalar<ES, T>(dst, src, n);
+        return;
+    }
+    const size_t h = vec_head<ES>(dst, n);
+    copy_scalar<ES, T>(dst, src, h);
+    const size_t n32 = (n - h) * ES / 32;
+    copy_vec32<T, POL>(dst + h * ES, src + h * ES, n32);
+    const size_t done = h + n32 * 32 / ES;
+    copy_scalar<ES, T>(dst + done * ES, src + done * ES, n - done);
 }
 
 // ------------------------------------------------------------ bounded wait
@@ -167,7 +204,7 @@ __device__ bool wait_row(const uint32_t *flag, uint32_t E, const RingParams &p, 
 
 // ------------------------------------------------------------ the step engine
 template <int DT>
-__global__ void __launch_bounds__(kRingThreads, 2) k_ring(const RingParams p)
+__global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const RingParams p)
 {
     constexpr size_t ES = DT == 1 ? 2 : 4;
     const int P = p.P, S = p.S;
@@ -176,46 +213,63 @@ __global__ void __launch_bounds__(kRingThreads, 2) k_ring(const RingParams p)
     // The abort word is the header's pad[0]: a launch that gives up stores its epoch there.
     uint32_t *abort_word = &p.hdr->pad[0];
 
+    // State only thread 0 uses (signal rows, step stamps) lives in shared
+    // memory so it does not hold registers through the streaming loops.
     __shared__ uint32_t s_epoch;
     __shared__ int s_abort;
+    __shared__ const uint32_t *s_my_rows;   // [rows][P] signal words of (rank r, slice j)
+    __shared__ uint32_t *s_right_rows;      // the same for (right, j)
+    __shared__ unsigned long long *s_stamp; // step stamps of this block, or null
     if (threadIdx.x == 0) {
         s_epoch = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
         s_abort = 0;
+        s_my_rows = p.sig + ((size_t)j * P + r) * (size_t)p.rows * P;
+        s_right_rows = p.sig + ((size_t)j * P + right) * (size_t)p.rows * P;
+        const int steps = p.mode == MODE_ALLREDUCE ? 2 * (P - 1) : P - 1;
+        s_stamp = (p.trace && (size_t)(blockIdx.x + 1) * steps * 3 <= p.trace_words)
+                      ? p.trace + (size_t)blockIdx.x * steps * 3
+                      : nullptr;
     }
     __syncthreads();
     const uint32_t E = s_epoch;
 
     const size_t c = p.chunk;
     const size_t lo = slice_begin(c, j, S), n = slice_begin(c, j + 1, S) - lo;
-    const bool vec = p.vec_ok != 0;
-    const uint32_t *my_rows = p.sig + ((size_t)j * P + r) * (size_t)p.rows * P;   // [rows][P]
-    uint32_t *right_rows = p.sig + ((size_t)j * P + right) * (size_t)p.rows * P;
     char *my_slot = p.data + (size_t)r * p.data_stride;
     const char *left_slot = p.data + (size_t)left * p.data_stride;
+    constexpr int T = kRingThreads;
 
     int nsteps;
     if (p.mode == MODE_ALL_GATHER) {
         nsteps = P - 1;
         // Prologue: the own shard goes to chunk r of the own output slot,
         // then row 0 of the right neighbour says it may be read.
-        copy_range<ES, kRingThreads>(my_slot + ((size_t)r * c + lo) * ES, p.in + (size_t)r * p.in_stride + lo * ES, n, vec);
+        copy_range<ES, T, kStNormal>(my_slot + ((size_t)r * c + lo) * ES, p.in + (size_t)r * p.in_stride + lo * ES, n);
         __syncthreads();
-        if (threadIdx.x == 0 && nsteps > 0) st_release_gpu(&right_rows[(size_t)0 * P + r], E);
+        if (threadIdx.x == 0 && nsteps > 0) st_release_gpu(&s_right_rows[(size_t)0 * P + r], E);
     } else {
         nsteps = p.mode == MODE_ALLREDUCE ? 2 * (P - 1) : P - 1;
     }
 
+    // Optional step stamps (%globaltimer, thread 0): per block and step, the
+    // start of the wait, its end, and the end of the step (after the notify).
     for (int g = 0; g < nsteps; ++g) {
+        if (threadIdx.x == 0 && s_stamp) s_stamp[3 * g] = global_timer_ns();
         if (g > 0 || p.mode == MODE_ALL_GATHER) {
-            if (threadIdx.x == 0 && !wait_row(&my_rows[(size_t)g * P + left], E, p, r, g, j, abort_word))
+            if (threadIdx.x == 0 && !wait_row(&s_my_rows[(size_t)g * P + left], E, p, r, g, j, abort_word))
                 s_abort = 1;
             __syncthreads();
             if (s_abort) break;
         }
+        if (threadIdx.x == 0 && s_stamp) s_stamp[3 * g + 1] = global_timer_ns();
+        const bool last = g == nsteps - 1; // nothing reads this step's output again in this launch
         if (p.mode == MODE_ALL_GATHER) {
             const int k = (r - 1 - g + P) % P;
             const size_t off = ((size_t)k * c + lo) * ES;
-            copy_range<ES, kRingThreads>(my_slot + off, left_slot + off, n, vec);
+            if (last)
+                copy_range<ES, T, kStEvictFirst>(my_slot + off, left_slot + off, n);
+            else
+                copy_range<ES, T, kStNormal>(my_slot + off, left_slot + off, n);
         } else if (g < P - 1) {
             const int s = g;
             const int k = (r - s - 2 + P) % P; // recv_add_idx == left_send_idx
@@ -224,18 +278,35 @@ __global__ void __launch_bounds__(kRingThreads, 2) k_ring(const RingParams p)
             char *dst = (p.mode == MODE_REDUCE_SCATTER && s == P - 2)
                             ? p.out + (size_t)r * p.out_stride + lo * ES
                             : own;
-            add_range<DT, kRingThreads>(dst, left_slot + off, own, n, vec);
+            // From round 1 on, the left chunk read here is the partial sum the
+            // left neighbour wrote in round s-1; no one reads it again before
+            // the left neighbour overwrites it (all-gather round s), so its
+            // dirty L2 lines are dropped instead of being written back.  The
+            // drops precede this step's notify, which orders them before that
+            // overwrite (it needs P-1 notifies round the ring, this one last).
+            // Rounds 0..P-3 write partial sums that the right neighbour reads next
+            // round and then drops: keep them in L2 (evict_last).  The last round
+            // writes the reduced chunk (read by the all-gather, or the output).
+            const bool drop = p.discard && s >= 1;
+            if (p.discard && s < P - 2)
+                add_range<DT, T, kStEvictLast>(dst, left_slot + off, own, n, drop);
+            else
+                add_range<DT, T, kStNormal>(dst, left_slot + off, own, n, drop);
         } else {
             const int t = g - (P - 1);
             const int k = (r - 1 - t + P) % P;
             const size_t off = ((size_t)k * c + lo) * ES;
-            copy_range<ES, kRingThreads>(my_slot + off, left_slot + off, n, vec);
+            if (last)
+                copy_range<ES, T, kStEvictFirst>(my_slot + off, left_slot + off, n);
+            else
+                copy_range<ES, T, kStNormal>(my_slot + off, left_slot + off, n);
         }
         if (g + 1 < nsteps) {
-            __syncthreads(); // every thread's stores of this step precede the release below
+            __syncthreads(); // every thread's loads, stores and drops of this step precede the release
             if (threadIdx.x == 0 && !(r == p.skip_rank && g == p.skip_step))
-                st_release_gpu(&right_rows[(size_t)(g + 1) * P + r], E);
+                st_release_gpu(&s_right_rows[(size_t)(g + 1) * P + r], E);
         }
+        if (threadIdx.x == 0 && s_stamp) s_stamp[3 * g + 2] = global_timer_ns();
     }
 
     // Epilogue: the last block to finish publishes the new epoch.
@@ -254,27 +325,18 @@ __global__ void __launch_bounds__(kRingThreads, 2) k_ring(const RingParams p)
 // dst_r = src_{(r-1+P)%P}: blockIdx.y is the destination rank, blocks along x
 // split the slot into contiguous pieces.
 template <int ES>
-__global__ void __launch_bounds__(256) k_ppermute(const char *src, size_t ss, char *dst, size_t ds, int P,
-                                                  size_t n, int vec_ok)
+__global__ void __launch_bounds__(256) k_ppermute(const char *src, size_t ss, char *dst, size_t ds, int P, size_t n)
 {
     const int r = blockIdx.y;
     const int left = (r - 1 + P) % P;
     const char *s = src + (size_t)left * ss;
     char *d = dst + (size_t)r * ds;
-    if (vec_ok) {
-        const size_t nvec = n * ES / 16;
-        const size_t per = (nvec + gridDim.x - 1) / gridDim.x;
-        const size_t b0 = per * blockIdx.x, b1 = min(nvec, b0 + per);
-        if (b0 < b1) copy_vec<256>(d + b0 * 16, s + b0 * 16, b1 - b0);
-        if (blockIdx.x == 0) {
-            const size_t head = nvec * 16 / ES;
-            copy_scalar<ES>(d + head * ES, s + head * ES, n - head);
-        }
-    } else {
-        const size_t per = (n + gridDim.x - 1) / gridDim.x;
-        const size_t b0 = per * blockIdx.x, b1 = min(n, b0 + per);
-        if (b0 < b1) copy_scalar<ES>(d + b0 * ES, s + b0 * ES, b1 - b0);
-    }
+    // contiguous pieces of whole 256-byte runs (64 or 128 elements)
+    constexpr size_t G = 256 / ES;
+    const size_t runs = (n + G - 1) / G;
+    const size_t per = (runs + gridDim.x - 1) / gridDim.x;
+    const size_t b0 = min(n, per * blockIdx.x * G), b1 = min(n, per * (blockIdx.x + 1) * G);
+    if (b0 < b1) copy_range<ES, 256, kStEvictFirst>(d + b0 * ES, s + b0 * ES, b1 - b0);
 }
 
 // ------------------------------------------------------------ host launchers
@@ -307,7 +369,7 @@ cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_
 }
 
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P, size_t n,
-                            int esize, int vec_ok, int sm_count, cudaStream_t st)
+                            int esize, int sm_count, cudaStream_t st)
 {
     // About four blocks per SM in total, at least one per rank.
     const size_t bytes = n * (size_t)esize;
@@ -317,9 +379,9 @@ cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_
     if (bx < 1) bx = 1;
     dim3 grid(bx, (unsigned)P);
     if (esize == 2)
-        k_ppermute<2><<<grid, 256, 0, st>>>(src, src_stride, dst, dst_stride, P, n, vec_ok);
+        k_ppermute<2><<<grid, 256, 0, st>>>(src, src_stride, dst, dst_stride, P, n);
     else
-        k_ppermute<4><<<grid, 256, 0, st>>>(src, src_stride, dst, dst_stride, P, n, vec_ok);
+        k_ppermute<4><<<grid, 256, 0, st>>>(src, src_stride, dst, dst_stride, P, n);
     return cudaGetLastError();
 }
 

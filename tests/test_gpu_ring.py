@@ -163,10 +163,8 @@ def test_reduce_scatter_matches_oracle(P, c, dtype):
     out = torch.full((P, c), 0, dtype=dtype, device=DEV)
     rc.ring_reduce_scatter(bufs, out)
     ok_status()
-    ob = np_of(x).copy()
-    want = oracle.reduce_scatter(ob, NAME[dtype])
-    assert np.array_equal(np_of(out), want)
-    assert np.array_equal(np_of(bufs), ob)   # the clobbered partial sums agree too
+    want = oracle.reduce_scatter(np_of(x).copy(), NAME[dtype])
+    assert np.array_equal(np_of(out), want)   # bufs is clobbered (undefined) by contract
 
 
 # ------------------------------------------------------------------ all-gather / ppermute
