@@ -1,8 +1,609 @@
-// ag_gemm.cu -- all-gather + matmul on tcgen05 tensor cores (in progress).
+// ag_gemm.cu -- all-gather of row shards fused with C = A_g . B^T on the
+// 5th-generation tensor cores (tcgen05, accumulators in TMEM).
+//
+// Sources: "TPU 与分布式通信原语", section "collective matmul" (all-gather the
+// row shards, then the local matmul with a bf16 result); "Triton-distributed
+// 语义", sections "生产者-消费者模型" and "AllGather + GEMM 重叠" (a producer
+// copies tiles and signals each one, a consumer waits per tile and computes
+// at once) and "线程块交织" (pid_m = (pid_m + rank*tiles_per_pe) % total so
+// every rank starts on its own, already local, rows).
+//
+// One persistent cooperative launch, one 256-thread block per SM:
+//   warp 0      TMA producer: A and B tiles (128x64 and 256x64 bf16, 128-byte
+//               swizzle) into a 4-stage shared-memory ring.  Before the first
+//               A tile of an M block that came from another rank it waits
+//               (ld.acquire, bounded) on that block's ready flags.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256,
+//               K=16, bf16 x bf16 -> fp32) into one of two TMEM accumulators
+//               and releases smem stages / accumulators with tcgen05.commit.
+//   warp 2      allocates TMEM (512 columns) and, on one thread, runs the
+//               gather producer: 16-row pieces of the shards are copied into
+//               A_g with bulk copies through two 16 KiB staging buffers, in
+//               the order the consumers need them, and each piece publishes
+//               its ready flag (st.release of the launch epoch).
+//   warps 4-7   epilogue: TMEM -> registers (tcgen05.ld), fp32 -> bf16 (RNE),
+//               stores to C, then free the accumulator for the MMA warp.
+// Rows of the own rank are read straight from its shard (local data, no
+// wait); rows of other ranks come from A_g once their flags are set.
+//
+// Every wait (mbarrier or flag) is bounded by %globaltimer; a wait that runs
+// out records RC_ERR_TIMEOUT in the workspace header and makes every role of
+// the block stop; in-flight copies and MMAs are drained (also bounded) and
+// TMEM is freed before the block exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "dev.cuh"
 #include "internal.h"
 #include "ringcoll.h"
 
-extern "C" int ag_gemm(const void *, size_t, void *, const void *, void *, int, int, int, int, int, void *)
+namespace rc {
+namespace ag {
+
+constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;   // 16 KiB
+constexpr int B_STAGE = BN * BK * 2;   // 32 KiB
+constexpr int STAGING = 16384;         // gather staging buffer (x2)
+constexpr int PIECE_ROWS = 16;         // rows per gather unit (one ready flag each)
+constexpr int THREADS = 256;
+constexpr int TMEM_COLS = 512;         // two 128x256 fp32 accumulators
+constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 2 * STAGING + 1024 /*align*/ + 256 /*barriers*/;
+
+struct Params {
+    const char *a_shards;
+    size_t a_stride;
+    char *a_gathered;
+    char *C;
+    uint32_t *flags;     // one per gather unit
+    WsHeader *hdr;
+    int P, rank, M_r, N, K;
+    int total_m, tiles_per_pe, n_tiles, total_tiles, units;
+    unsigned long long timeout_ns;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
-    return RC_ERR_UNSUPPORTED;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+                 ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] . B[smem desc]^T ; accumulate = 0 overwrites D.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes (64 bf16), 8-row groups 1024 bytes
+// apart (stride byte offset), leading byte offset unused for this layout,
+// descriptor version 1 (bits 46-48), swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);      // start address
+    d |= (uint64_t)(1024u >> 4) << 32;             // stride byte offset
+    d |= (uint64_t)1 << 46;                        // version
+    d |= (uint64_t)2 << 61;                        // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N>>3 at bits
+// 17-22, M>>4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                   "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                   "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+                   "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi_bits)), "f"(__uint_as_float(lo_bits)));
+    return r;
+}
+
+// ------------------------------------------------------------ bounded waits
+struct Abort {
+    int *flag;          // shared: set once any role of the block gives up
+    WsHeader *hdr;
+    unsigned long long timeout_ns;
+};
+
+__device__ void record_timeout(const Abort &ab, int where)
+{
+    if (atomicCAS(&ab.hdr->status, 0u, (unsigned)RC_ERR_TIMEOUT) == 0u) {
+        ab.hdr->err_rank = 0xA6u;              // marks the all-gather + GEMM kernel
+        ab.hdr->err_step = (uint32_t)where;
+        ab.hdr->err_slice = blockIdx.x;
+    }
+    atomicExch(ab.flag, 1);
+}
+
+// Waits for mbarrier phase `parity`; false if the block aborted (unless
+// `drain`: then only the time bound ends it) or time ran out.
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, const Abort &ab, int where, bool drain = false)
+{
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (!drain && *(volatile int *)ab.flag) return false;
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > ab.timeout_ns) {
+                record_timeout(ab, where);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ bool wait_flag(const uint32_t *flag, uint32_t E, const Abort &ab, int where)
+{
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (epoch_reached(ld_acquire_gpu(flag), E)) return true;
+        if ((it & 15u) == 15u) {
+            if (*(volatile int *)ab.flag) return false;
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > ab.timeout_ns) {
+                record_timeout(ab, where);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
+// ------------------------------------------------------------ tile order
+// Tile t of the persistent schedule -> (m block, n block).  Raw M order is
+// swizzled by rank so that the first M blocks are the rank's own rows.
+__device__ __forceinline__ void tile_of(const Params &p, int t, int &m, int &n)
+{
+    const int m_raw = t / p.n_tiles;
+    n = t % p.n_tiles;
+    m = (m_raw + p.rank * p.tiles_per_pe) % p.total_m;
+}
+
+// Gather unit u (in the order the consumers need them: other ranks' M blocks
+// in swizzled order, the own rank's last) -> (M block, piece).
+__device__ __forceinline__ void unit_of(const Params &p, int u, int &mb, int &piece)
+{
+    const int pieces = BM / PIECE_ROWS;
+    const int i = u / pieces;
+    piece = u % pieces;
+    const int others = p.total_m - p.tiles_per_pe;
+    const int order = i < others ? i + p.tiles_per_pe : i - others;
+    mb = (order + p.rank * p.tiles_per_pe) % p.total_m;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k_ag_gemm(const __grid_constant__ CUtensorMap map_ag, const __grid_constant__ CUtensorMap map_sh,
+              const __grid_constant__ CUtensorMap map_b, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // 128-byte swizzle wants 1024-byte aligned tiles
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = sA + STAGES * A_STAGE;
+    const uint32_t sStage = sB + STAGES * B_STAGE;
+    uint8_t *bars_g = gbase + STAGES * (A_STAGE + B_STAGE) + 2 * STAGING;
+    const uint32_t bars = smem_u32(bars_g);
+    const uint32_t full_bar = bars, empty_bar = bars + 8 * STAGES;
+    const uint32_t tfull_bar = bars + 16 * STAGES, tempty_bar = tfull_bar + 16;
+    const uint32_t gat_bar = tempty_bar + 16;
+    uint32_t *tmem_slot = (uint32_t *)(bars_g + 16 * STAGES + 48);
+    int *abort_flag = (int *)(bars_g + 16 * STAGES + 52);
+    uint32_t *epoch_slot = (uint32_t *)(bars_g + 16 * STAGES + 56);
+    const uint32_t drain_bar = bars + 16 * STAGES + 64;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar + 8 * a, 1);
+            mbar_init(tempty_bar + 8 * a, 4);   // one arrive per epilogue warp
+            mbar_init(gat_bar + 8 * a, 1);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        *epoch_slot = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_ag) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_sh) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_b) : "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t E = *epoch_slot;
+    const Abort ab{abort_flag, p.hdr, p.timeout_ns};
+    const int ksteps = p.K / BK;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        uint32_t stage = 0, phase = 0;
+        int issued[STAGES] = {0, 0, 0, 0};
+        for (int t = blockIdx.x; t < p.total_tiles && !*(volatile int *)abort_flag; t += gridDim.x) {
+            int m, n;
+            tile_of(p, t, m, n);
+            const int src_rank = (m * BM) / p.M_r;
+            const bool own = src_rank == p.rank;
+            if (!own) {
+                bool ok = true;
+                for (int q = 0; q < BM / PIECE_ROWS && ok; ++q)
+                    ok = wait_flag(&p.flags[m * (BM / PIECE_ROWS) + q], E, ab, 1);
+                if (!ok) break;
+                fence_proxy_async_global(); // the generic-proxy flag orders the async-proxy reads below
+            }
+            const int row_in_shard = (m * BM) % p.M_r;
+            bool ok = true;
+            for (int kb = 0; kb < ksteps; ++kb) {
+                if (!wait_bar(empty_bar + 8 * stage, phase ^ 1u, ab, 2)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(full_bar + 8 * stage, A_STAGE + B_STAGE);
+                if (own)
+                    tma_load_3d(sA + stage * A_STAGE, &map_sh, kb * BK, row_in_shard, src_rank, full_bar + 8 * stage);
+                else
+                    tma_load_2d(sA + stage * A_STAGE, &map_ag, kb * BK, m * BM, full_bar + 8 * stage);
+                tma_load_2d(sB + stage * B_STAGE, &map_b, kb * BK, n * BN, full_bar + 8 * stage);
+                issued[stage]++;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+        // Drain: every load issued must have landed before the block may exit
+        // (the last load into stage s completes phase (issued[s]-1) of full_bar[s]).
+        if (*(volatile int *)abort_flag) {
+            for (int s = 0; s < STAGES; ++s)
+                if (issued[s] > 0) wait_bar(full_bar + 8 * s, (uint32_t)((issued[s] - 1) & 1), ab, 9, true);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        uint32_t stage = 0, phase = 0;
+        int it = 0;
+        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+            const uint32_t acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            if (!wait_bar(tempty_bar + 8 * acc, acc_phase ^ 1u, ab, 3)) break;
+            tc_fence_after();
+            const uint32_t d = tmem_base + acc * BN;
+            bool ok = true;
+            for (int kb = 0; kb < ksteps; ++kb) {
+                if (!wait_bar(full_bar + 8 * stage, phase, ab, 4)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = smem_desc_sw128(sA + stage * A_STAGE);
+                const uint64_t bd = smem_desc_sw128(sB + stage * B_STAGE);
+#pragma unroll
+                for (int k = 0; k < BK / UK; ++k) {
+                    // K advances 16 bf16 = 32 bytes inside the 128-byte swizzle row: +2 in 16-byte units
+                    tc_mma(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc, (kb | k) != 0);
+                }
+                tc_commit(empty_bar + 8 * stage); // frees the smem stage once these MMAs have read it
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            tc_commit(tfull_bar + 8 * acc);       // accumulator ready once every MMA above completes
+            if (!ok) break;
+        }
+        // Drain: no MMA may still read shared memory or write TMEM when the
+        // block frees them; a commit after the last MMA tracks all of them.
+        tc_commit(drain_bar);
+        wait_bar(drain_bar, 0, ab, 10, true);
+    } else if (warp == 2 && lane == 0) {
+        // ---------------- gather producer
+        const size_t row_bytes = (size_t)p.K * 2;
+        const size_t unit_bytes = (size_t)PIECE_ROWS * row_bytes;
+        uint32_t gphase[2] = {0, 0};
+        uint64_t piece_no = 0;
+        for (int u = blockIdx.x; u < p.units && !*(volatile int *)abort_flag; u += gridDim.x) {
+            int mb, piece;
+            unit_of(p, u, mb, piece);
+            const int row = mb * BM + piece * PIECE_ROWS;     // row of A_g
+            const int src_rank = row / p.M_r;
+            const char *src = p.a_shards + (size_t)src_rank * p.a_stride + (size_t)(row % p.M_r) * row_bytes;
+            char *dst = p.a_gathered + (size_t)row * row_bytes;
+            bool ok = true;
+            for (size_t off = 0; off < unit_bytes; off += STAGING, ++piece_no) {
+                const uint32_t bytes = (uint32_t)((unit_bytes - off) < (size_t)STAGING ? (unit_bytes - off) : STAGING);
+                const int b = (int)(piece_no & 1);
+                if (piece_no >= 2) bulk_wait_read1(); // the store that last used buffer b has read it
+                mbar_expect_tx(gat_bar + 8 * b, bytes);
+                bulk_g2s(sStage + b * STAGING, src + off, bytes, gat_bar + 8 * b);
+                if (!wait_bar(gat_bar + 8 * b, gphase[b], ab, 5)) {
+                    wait_bar(gat_bar + 8 * b, gphase[b], ab, 11, true); // the load must land before exit
+                    ok = false;
+                    break;
+                }
+                gphase[b] ^= 1u;
+                bulk_s2g(dst + off, sStage + b * STAGING, bytes);
+                bulk_commit();
+            }
+            bulk_wait_all();              // this unit's rows are in A_g
+            if (!ok) break;
+            fence_proxy_async_global();   // async-proxy writes before the generic release
+            st_release_gpu(&p.flags[mb * (BM / PIECE_ROWS) + piece], E);
+        }
+        bulk_wait_all();
+    } else if (warp >= 4) {
+        // ---------------- epilogue
+        const int q = warp - 4;            // TMEM lane quadrant of this warp
+        int it = 0;
+        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+            const uint32_t acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            // One lane waits and the warp follows its verdict, so the warp stays
+            // converged for the .sync.aligned TMEM loads below.
+            int ok = lane == 0 ? (int)wait_bar(tfull_bar + 8 * acc, acc_phase, ab, 6) : 0;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            int m, n;
+            tile_of(p, t, m, n);
+            const size_t row = (size_t)m * BM + q * 32 + lane;
+            char *crow = p.C + row * (size_t)p.N * 2 + (size_t)n * BN * 2;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + cc * 32, v);
+                uint4 o[4];
+                o[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                  pack_bf16x2(v[6], v[7]));
+                o[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                                  pack_bf16x2(v[14], v[15]));
+                o[2] = make_uint4(pack_bf16x2(v[16], v[17]), pack_bf16x2(v[18], v[19]),
+                                  pack_bf16x2(v[20], v[21]), pack_bf16x2(v[22], v[23]));
+                o[3] = make_uint4(pack_bf16x2(v[24], v[25]), pack_bf16x2(v[26], v[27]),
+                                  pack_bf16x2(v[28], v[29]), pack_bf16x2(v[30], v[31]));
+#pragma unroll
+                for (int w = 0; w < 4; ++w) st_v4(crow + cc * 64 + w * 16, o[w]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar + 8 * acc);
+        }
+    }
+
+    // ---------------- teardown (every role has drained its own async work)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(&p.hdr->done, 1u);
+        if (prev == gridDim.x - 1) {
+            p.hdr->done = 0;
+            st_relaxed_gpu(&p.hdr->epoch, E);
+        }
+    }
+}
+
+// ------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    });
+    return fn;
+}
+
+// bf16 tensor map over `rank` dims (dims[0] innermost, strides in bytes for dims 1..),
+// box {BK, box_rows, 1...}, 128-byte swizzle.
+static int make_map(CUtensorMap *map, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                    uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return set_error(RC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(RC_ERR_INVALID, "tensor map encoding failed (CUresult %d)", (int)r);
+    return RC_OK;
+}
+
+static bool overlap(const void *a, size_t an, const void *b, size_t bn)
+{
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+} // namespace ag
+} // namespace rc
+
+extern "C" int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P,
+                       int rank, int M_r, int N, int K, void *stream)
+{
+    using namespace rc;
+    using namespace rc::ag;
+    if (P < 1 || P > RC_MAX_P) return set_error(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (rank < 0 || rank >= P) return set_error(RC_ERR_INVALID, "rank %d outside 0..P-1", rank);
+    if (M_r <= 0 || N <= 0 || K <= 0 || M_r % BM || N % BN || K % BK)
+        return set_error(RC_ERR_INVALID, "need M_r %% %d == 0, N %% %d == 0, K %% %d == 0 (got %d, %d, %d)", BM, BN, BK,
+                         M_r, N, K);
+    if (!a_shards || !a_gathered || !B || !C) return set_error(RC_ERR_INVALID, "null pointer");
+    if (((uintptr_t)a_shards | (uintptr_t)a_gathered | (uintptr_t)B | (uintptr_t)C | a_stride) & 15u)
+        return set_error(RC_ERR_INVALID, "pointers and a_stride must be 16-byte aligned");
+    const size_t shard_bytes = (size_t)M_r * K * 2;
+    if (P > 1 && a_stride < shard_bytes) return set_error(RC_ERR_INVALID, "a_stride below a shard's bytes");
+    const size_t M = (size_t)P * M_r;
+    const size_t ag_bytes = M * K * 2, b_bytes = (size_t)N * K * 2, c_bytes = M * N * 2;
+    const size_t sh_span = (size_t)(P - 1) * a_stride + shard_bytes;
+    if (overlap(a_gathered, ag_bytes, C, c_bytes) || overlap(a_gathered, ag_bytes, a_shards, sh_span) ||
+        overlap(a_gathered, ag_bytes, B, b_bytes) || overlap(C, c_bytes, a_shards, sh_span) ||
+        overlap(C, c_bytes, B, b_bytes))
+        return set_error(RC_ERR_INVALID, "outputs overlap each other or an input");
+    if (M > (1u << 31) || (size_t)N > (1u << 31)) return set_error(RC_ERR_INVALID, "dimensions too large");
+
+    Params p{};
+    p.a_shards = (const char *)a_shards;
+    p.a_stride = a_stride;
+    p.a_gathered = (char *)a_gathered;
+    p.C = (char *)C;
+    p.P = P;
+    p.rank = rank;
+    p.M_r = M_r;
+    p.N = N;
+    p.K = K;
+    p.total_m = (int)(M / BM);
+    p.tiles_per_pe = M_r / BM;
+    p.n_tiles = N / BN;
+    p.total_tiles = p.total_m * p.n_tiles;
+    p.units = p.total_m * (BM / PIECE_ROWS);
+    int sm_count = 0;
+    int rc_ = prepare_workspace((size_t)p.units, &p.hdr, &p.flags, &sm_count, &p.timeout_ns);
+    if (rc_) return rc_;
+
+    CUtensorMap map_ag, map_sh, map_b;
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        if ((rc_ = make_map(&map_ag, a_gathered, 2, dims, strides, BM))) return rc_;
+    }
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)M_r, (cuuint64_t)P};
+        cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)(P > 1 ? a_stride : shard_bytes)};
+        if ((rc_ = make_map(&map_sh, a_shards, 3, dims, strides, BM))) return rc_;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        if ((rc_ = make_map(&map_b, B, 2, dims, strides, BN))) return rc_;
+    }
+
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(k_ag_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess)
+        return set_error(RC_ERR_CUDA, "shared-memory attribute: %s", cudaGetErrorString(attr_err));
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ag_gemm, THREADS, SMEM_BYTES);
+    if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+    if (per_sm < 1) return set_error(RC_ERR_UNSUPPORTED, "the GEMM block does not fit on an SM");
+    int grid = sm_count * per_sm;
+    if (grid > p.total_tiles) grid = p.total_tiles;
+    void *args[] = {(void *)&map_ag, (void *)&map_sh, (void *)&map_b, (void *)&p};
+    e = cudaLaunchCooperativeKernel((const void *)k_ag_gemm, dim3((unsigned)grid), dim3(THREADS), args,
+                                    (size_t)SMEM_BYTES, (cudaStream_t)stream);
+    if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "ag_gemm launch: %s", cudaGetErrorString(e));
+    return RC_OK;
 }

@@ -210,6 +210,39 @@ int run_copy(const void *src, size_t src_stride, void *dst, size_t dst_stride, i
 
 } // namespace
 
+namespace rc {
+
+int set_error(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int prepare_workspace(size_t sig_words, WsHeader **hdr, uint32_t **sig, int *sm_count,
+                      unsigned long long *timeout_ns)
+{
+    int dev;
+    DeviceState *st = nullptr;
+    int rc_ = current_device(&dev, &st);
+    if (rc_) return rc_;
+    std::lock_guard<std::mutex> lock(g_mu);
+    rc_ = ensure_workspace(*st, sig_words * 4);
+    if (rc_) return rc_;
+    *hdr = (WsHeader *)st->ws;
+    *sig = (uint32_t *)((char *)st->ws + sizeof(WsHeader));
+    *sm_count = st->sm_count;
+    *timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
+    st->launches++;
+    return RC_OK;
+}
+
+} // namespace rc
+
 extern "C" {
 
 const char *ring_last_error(void) { return g_err.c_str(); }

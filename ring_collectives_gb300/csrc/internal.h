@@ -46,6 +46,16 @@ cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks)
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P,
                             size_t n, int esize, int sm_count, cudaStream_t st);
 
+// Host helpers implemented in api.cu and shared with ag_gemm.cu.
+// set_error: records the calling thread's message; returns `code`.
+int set_error(int code, const char *fmt, ...);
+// prepare_workspace: the current device must be an sm_103 GPU with
+// cooperative launch; grows the device's workspace to at least sig_words
+// signal words and returns its header, words, SM count and wait bound.  The
+// epoch in the header is shared by every launch that uses the workspace.
+int prepare_workspace(size_t sig_words, WsHeader **hdr, uint32_t **sig, int *sm_count,
+                      unsigned long long *timeout_ns);
+
 // Threads per block of the ring kernel, and the blocks per SM its register
 // budget is sized for (build-time tuning knobs).
 // Small blocks, many per SM: while some blocks wait on their left neighbour
