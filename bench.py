@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--P", type=int, default=8)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true", help="add the weak-scaling sweep (P=2..32) to the line")
     ap.add_argument("--n-per-rank", type=int, default=0,
                     help="override N per rank (a smaller case of the same workload, e.g. for profiling)")
     return ap.parse_args()
@@ -267,6 +268,62 @@ def time_reduce_scatter(rc, bufs, out, pristine, N, steps, warmup, stream):
     return [a.elapsed_time(b) for a, b in ts]
 
 
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured burst"
+    except Exception:
+        return 1900.0, "fallback burst"
+
+
+def ag_gemm_secondary(rc, dev, stream, args):
+    """All-gather + GEMM at P=8, shards [1024,4096], B [4096,4096] bf16 (tensor-bound)."""
+    P, M_r, K, N = 8, 1024, 4096, 4096
+    a, b = synthetic.ag_gemm_inputs(P=P, M_r=M_r, K=K, N=N)
+    ad, bd = a.to(dev), b.to(dev)
+    ag = torch.empty((P * M_r, K), dtype=torch.bfloat16, device=dev)
+    C = torch.empty((P * M_r, N), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        rc.ag_gemm(ad, ag, bd, C, 3, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for x, y in ev:
+        x.record(stream)
+        rc.ag_gemm(ad, ag, bd, C, 3, stream=stream)
+        y.record(stream)
+    torch.cuda.synchronize()
+    if rc.ring_status(stream) != 0:
+        raise RuntimeError(rc.ring_last_error())
+    ms = statistics.mean(x.elapsed_time(y) for x, y in ev)
+    flop = 2 * P * M_r * N * K
+    peak, kind = bf16_peak()
+    tf = flop / (ms * 1e-3) / 1e12
+    return {"ag_gemm_p8_8192x4096x4096": {
+        "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peak, 4),
+        "peak": peak, "peak_kind": kind, "flop_per_call": flop,
+        "note": "gather of the 8 shards (64 MiB) + C = A_g.B^T, one tcgen05 launch"}}
+
+
+def weak_sweep(rc, dev, stream, args):
+    """Chunk 4M fp32 per rank-step, P in {2,4,8,16,32}: time per ring step."""
+    out = {}
+    for P in (2, 4, 8, 16, 32):
+        N = (4 << 20) * P
+        x = synthetic.workload("weak", P=P)
+        pr = x.to(dev)
+        del x
+        bf = torch.empty_like(pr)
+        ts = time_allreduce(rc, bf, pr, N, max(3, args.steps // 2), args.warmup, stream)
+        ms = statistics.mean(ts)
+        out[f"P{P}"] = {"ms": round(ms, 4), "us_per_step": round(1e3 * ms / (2 * (P - 1)), 2),
+                        "per_rank_step_bytes": 5 * (4 << 20) * 4 // 2,
+                        "GB/s_ring_bytes": round(ring_bytes(P, N, 4) / (ms * 1e-3) / 1e9, 1)}
+        del pr, bf
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, spec, rank, world, dist):
     import ring_collectives_gb300 as rc
     import __graft_entry__
@@ -351,6 +408,11 @@ def run_ours(args, spec, rank, world, dist):
         }
         del pb, bb, out
 
+    if not args.no_secondary and spec["name"] == "f32_64mib":
+        secondary.update(ag_gemm_secondary(rc, dev, stream, args))
+    if args.sweep:
+        secondary["weak_scaling"] = weak_sweep(rc, dev, stream, args)
+
     if rank != 0:
         return 0
     peak, peak_kind = peaks()
@@ -375,6 +437,7 @@ def run_ours(args, spec, rank, world, dist):
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": P * N * e, "d2h_bytes_per_step": P * N * e,
                 "api": "ring_allreduce_host (pinned host slots in and out)"},
         "gpu_launches": args.steps,
+        "gpu_launches_note": "one k_ring launch per timed step; the e2e leg adds one per step as well",
         "clocks": clocks.summary(),
         "ms_min": round(min(times), 4), "ms_median": round(statistics.median(times), 4),
     }
