@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="f32_64mib", choices=["f32_64mib", "bf16_64mib", "weak"])
+    ap.add_argument("--workload", default="f32_64mib", choices=["f32_64mib", "bf16_64mib", "weak", "ag_gemm"])
     ap.add_argument("--P", type=int, default=8)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -447,10 +447,64 @@ def run_ours(args, spec, rank, world, dist):
     return 0
 
 
+def run_ag_gemm(args, rank, world, dist):
+    """--workload ag_gemm: the all-gather + GEMM (P=8 shards [1024,4096], B
+    [4096,4096], bf16, fp32 accumulate) as its own line, in TFLOP/s."""
+    import ring_collectives_gb300 as rc
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    if dist is not None:
+        dist.barrier()
+    with ClockSampler(dev.index) as clocks:
+        res = ag_gemm_secondary(rc, dev, stream, args)["ag_gemm_p8_8192x4096x4096"]
+    ms = res["ms"]
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if rank != 0:
+        return 0
+    flop = res["flop_per_call"]
+    peak, kind = bf16_peak()
+    tf = flop / (res["ms"] * 1e-3) / 1e12
+    line = {
+        "metric": "ag_gemm TFLOP/s (all-gather of P=8 row shards + C = A_g.B^T), 8192x4096x4096 bf16",
+        "value": round(world * flop / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "ag_gemm_p8_m1024_k4096_n4096", "P": 8, "rank": 3, "replicas": world,
+                   "l2": "operands 96 MiB + outputs 128 MiB, larger than L2"},
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tf / peak, 4), "traffic": None, "peak_kind": kind,
+                     "algorithmic_flop_per_launch": flop, "kernel": "k_ag_gemm"},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.workload == "ag_gemm":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the ag_gemm oracle is a sampled check, not a "
+                              "timed baseline; use the default all-reduce workload"}))
+            return 0
+        dist = None
+        if world > 1:
+            import torch.distributed as dist_mod
+            dist_mod.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
+            dist = dist_mod
+        try:
+            return run_ag_gemm(args, rank, world, dist)
+        finally:
+            if dist is not None:
+                dist.destroy_process_group()
     spec = workload_spec(args.workload, args.P, args.n_per_rank)
     if args.impl == "reference":
         return run_reference(args, spec, rank, world)

@@ -34,6 +34,7 @@ struct RingParams {
     size_t chunk;        // elements per chunk (all-gather: the shard length n)
     int P, S, rows, mode;
     int discard;         // 1: drop the L2 lines of reduce-scatter partials once read (their data is dead)
+    int segments;        // chunk segments run one after another (keeps a step's live data in L2)
     int skip_rank, skip_step; // test hook: this rank skips its notify after this step (-1: none)
     unsigned long long timeout_ns;
     unsigned long long *trace; // optional step stamps (see ring_debug_set_trace); null: off

@@ -173,16 +173,16 @@ __device__ __forceinline__ void copy_range(char *dst, const char *src, size_t n)
 }
 
 // ------------------------------------------------------------ bounded wait
-// Spins (one thread) until *flag reaches epoch E.  Gives up when the launch
+// Spins (one thread) until *flag reaches value V.  Gives up when the launch
 // has already failed elsewhere, or after timeout_ns: the first block to time
 // out records RC_ERR_TIMEOUT with its rank/step/slice in the header.  Never
 // traps; the caller returns cleanly and the host reads the status.
-__device__ bool wait_row(const uint32_t *flag, uint32_t E, const RingParams &p, int r, int g, int j,
+__device__ bool wait_row(const uint32_t *flag, uint32_t V, uint32_t E, const RingParams &p, int r, int g, int j,
                          uint32_t *abort_word)
 {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
-        if (epoch_reached(ld_acquire_gpu(flag), E)) return true;
+        if (epoch_reached(ld_acquire_gpu(flag), V)) return true;
         if ((it & 31u) == 31u) {
             if (ld_relaxed_gpu(abort_word) == E) return false;
             const uint64_t now = global_timer_ns();
@@ -203,6 +203,13 @@ __device__ bool wait_row(const uint32_t *flag, uint32_t E, const RingParams &p, 
 }
 
 // ------------------------------------------------------------ the step engine
+// Segments: when one step's live data (P chunks) would not fit in L2, each
+// slice ring runs all its steps on segment 0 of the chunks, then segment 1,
+// and so on (segment q of chunk k is the same element range in every chunk,
+// so every element keeps its ring order).  Segment q signals with the value
+// E0 + q + 1 on the same rows (E0: the epoch before the launch), so values
+// stay monotonic across segments and launches; the launch advances the epoch
+// by the number of segments.
 template <int DT>
 __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const RingParams p)
 {
@@ -212,101 +219,107 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
     const int left = (r - 1 + P) % P, right = (r + 1) % P;
     // The abort word is the header's pad[0]: a launch that gives up stores its epoch there.
     uint32_t *abort_word = &p.hdr->pad[0];
+    const int nsteps = p.mode == MODE_ALLREDUCE ? 2 * (P - 1) : P - 1;
 
     // State only thread 0 uses (signal rows, step stamps) lives in shared
     // memory so it does not hold registers through the streaming loops.
-    __shared__ uint32_t s_epoch;
+    __shared__ uint32_t s_epoch0;
     __shared__ int s_abort;
     __shared__ const uint32_t *s_my_rows;   // [rows][P] signal words of (rank r, slice j)
     __shared__ uint32_t *s_right_rows;      // the same for (right, j)
     __shared__ unsigned long long *s_stamp; // step stamps of this block, or null
     if (threadIdx.x == 0) {
-        s_epoch = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
+        s_epoch0 = ld_relaxed_gpu(&p.hdr->epoch);
         s_abort = 0;
         s_my_rows = p.sig + ((size_t)j * P + r) * (size_t)p.rows * P;
         s_right_rows = p.sig + ((size_t)j * P + right) * (size_t)p.rows * P;
-        const int steps = p.mode == MODE_ALLREDUCE ? 2 * (P - 1) : P - 1;
-        s_stamp = (p.trace && (size_t)(blockIdx.x + 1) * steps * 3 <= p.trace_words)
-                      ? p.trace + (size_t)blockIdx.x * steps * 3
+        s_stamp = (p.trace && (size_t)(blockIdx.x + 1) * nsteps * 3 <= p.trace_words)
+                      ? p.trace + (size_t)blockIdx.x * nsteps * 3
                       : nullptr;
     }
     __syncthreads();
-    const uint32_t E = s_epoch;
-
+    const uint32_t E0 = s_epoch0;
+    const uint32_t E = E0 + 1u;   // identifies this launch (abort word)
     const size_t c = p.chunk;
-    const size_t lo = slice_begin(c, j, S), n = slice_begin(c, j + 1, S) - lo;
     char *my_slot = p.data + (size_t)r * p.data_stride;
     const char *left_slot = p.data + (size_t)left * p.data_stride;
     constexpr int T = kRingThreads;
 
-    int nsteps;
-    if (p.mode == MODE_ALL_GATHER) {
-        nsteps = P - 1;
-        // Prologue: the own shard goes to chunk r of the own output slot,
-        // then row 0 of the right neighbour says it may be read.
-        copy_range<ES, T, kStNormal>(my_slot + ((size_t)r * c + lo) * ES, p.in + (size_t)r * p.in_stride + lo * ES, n);
-        __syncthreads();
-        if (threadIdx.x == 0 && nsteps > 0) st_release_gpu(&s_right_rows[(size_t)0 * P + r], E);
-    } else {
-        nsteps = p.mode == MODE_ALLREDUCE ? 2 * (P - 1) : P - 1;
-    }
+    for (int q = 0; q < p.segments; ++q) {
+        const size_t seg_lo = slice_begin(c, q, p.segments);
+        const size_t seg_n = slice_begin(c, q + 1, p.segments) - seg_lo;
+        const size_t lo = seg_lo + slice_begin(seg_n, j, S);
+        const size_t n = seg_lo + slice_begin(seg_n, j + 1, S) - lo;
+        const uint32_t V = E0 + 1u + (uint32_t)q; // signal value of this segment
 
-    // Optional step stamps (%globaltimer, thread 0): per block and step, the
-    // start of the wait, its end, and the end of the step (after the notify).
-    for (int g = 0; g < nsteps; ++g) {
-        if (threadIdx.x == 0 && s_stamp) s_stamp[3 * g] = global_timer_ns();
-        if (g > 0 || p.mode == MODE_ALL_GATHER) {
-            if (threadIdx.x == 0 && !wait_row(&s_my_rows[(size_t)g * P + left], E, p, r, g, j, abort_word))
-                s_abort = 1;
-            __syncthreads();
-            if (s_abort) break;
-        }
-        if (threadIdx.x == 0 && s_stamp) s_stamp[3 * g + 1] = global_timer_ns();
-        const bool last = g == nsteps - 1; // nothing reads this step's output again in this launch
         if (p.mode == MODE_ALL_GATHER) {
-            const int k = (r - 1 - g + P) % P;
-            const size_t off = ((size_t)k * c + lo) * ES;
-            if (last)
-                copy_range<ES, T, kStEvictFirst>(my_slot + off, left_slot + off, n);
-            else
-                copy_range<ES, T, kStNormal>(my_slot + off, left_slot + off, n);
-        } else if (g < P - 1) {
-            const int s = g;
-            const int k = (r - s - 2 + P) % P; // recv_add_idx == left_send_idx
-            const size_t off = ((size_t)k * c + lo) * ES;
-            char *own = my_slot + off;
-            char *dst = (p.mode == MODE_REDUCE_SCATTER && s == P - 2)
-                            ? p.out + (size_t)r * p.out_stride + lo * ES
-                            : own;
-            // From round 1 on, the left chunk read here is the partial sum the
-            // left neighbour wrote in round s-1; no one reads it again before
-            // the left neighbour overwrites it (all-gather round s), so its
-            // dirty L2 lines are dropped instead of being written back.  The
-            // drops precede this step's notify, which orders them before that
-            // overwrite (it needs P-1 notifies round the ring, this one last).
-            // Rounds 0..P-3 write partial sums that the right neighbour reads next
-            // round and then drops: keep them in L2 (evict_last).  The last round
-            // writes the reduced chunk (read by the all-gather, or the output).
-            const bool drop = p.discard && s >= 1;
-            if (p.discard && s < P - 2)
-                add_range<DT, T, kStEvictLast>(dst, left_slot + off, own, n, drop);
-            else
-                add_range<DT, T, kStNormal>(dst, left_slot + off, own, n, drop);
-        } else {
-            const int t = g - (P - 1);
-            const int k = (r - 1 - t + P) % P;
-            const size_t off = ((size_t)k * c + lo) * ES;
-            if (last)
-                copy_range<ES, T, kStEvictFirst>(my_slot + off, left_slot + off, n);
-            else
-                copy_range<ES, T, kStNormal>(my_slot + off, left_slot + off, n);
+            // Prologue: the own shard goes to chunk r of the own output slot,
+            // then the right neighbour's first row says it may be read.
+            copy_range<ES, T, kStNormal>(my_slot + ((size_t)r * c + lo) * ES, p.in + (size_t)r * p.in_stride + lo * ES,
+                                         n);
+            __syncthreads();
+            if (threadIdx.x == 0) st_release_gpu(&s_right_rows[r], V);
         }
-        if (g + 1 < nsteps) {
-            __syncthreads(); // every thread's loads, stores and drops of this step precede the release
-            if (threadIdx.x == 0 && !(r == p.skip_rank && g == p.skip_step))
-                st_release_gpu(&s_right_rows[(size_t)(g + 1) * P + r], E);
+
+        // Step stamps (%globaltimer, thread 0, first segment): per block and
+        // step, the start of the wait, its end, and the end of the step.
+        for (int g = 0; g < nsteps; ++g) {
+            if (threadIdx.x == 0 && s_stamp && q == 0) s_stamp[3 * g] = global_timer_ns();
+            if (g > 0 || p.mode == MODE_ALL_GATHER) {
+                if (threadIdx.x == 0 &&
+                    !wait_row(&s_my_rows[(size_t)g * P + left], V, E, p, r, g, j, abort_word))
+                    s_abort = 1;
+                __syncthreads();
+                if (s_abort) break;
+            }
+            if (threadIdx.x == 0 && s_stamp && q == 0) s_stamp[3 * g + 1] = global_timer_ns();
+            const bool last = g == nsteps - 1; // nothing reads this step's output again in this launch
+            if (p.mode == MODE_ALL_GATHER) {
+                const int k = (r - 1 - g + P) % P;
+                const size_t off = ((size_t)k * c + lo) * ES;
+                if (last)
+                    copy_range<ES, T, kStEvictFirst>(my_slot + off, left_slot + off, n);
+                else
+                    copy_range<ES, T, kStNormal>(my_slot + off, left_slot + off, n);
+            } else if (g < P - 1) {
+                const int s = g;
+                const int k = (r - s - 2 + P) % P; // recv_add_idx == left_send_idx
+                const size_t off = ((size_t)k * c + lo) * ES;
+                char *own = my_slot + off;
+                char *dst = (p.mode == MODE_REDUCE_SCATTER && s == P - 2)
+                                ? p.out + (size_t)r * p.out_stride + lo * ES
+                                : own;
+                // From round 1 on, the left chunk read here is the partial sum the
+                // left neighbour wrote in round s-1; no one reads it again before
+                // the left neighbour overwrites it (all-gather round s), so its
+                // dirty L2 lines are dropped instead of being written back.  The
+                // drops precede this step's notify, which orders them before that
+                // overwrite (it needs P-1 notifies round the ring, this one last).
+                // Rounds 0..P-3 write partial sums that the right neighbour reads
+                // next round and then drops: keep them in L2 (evict_last).  The last
+                // round writes the reduced chunk (read by the all-gather, or the output).
+                const bool drop = p.discard && s >= 1;
+                if (p.discard && s < P - 2)
+                    add_range<DT, T, kStEvictLast>(dst, left_slot + off, own, n, drop);
+                else
+                    add_range<DT, T, kStNormal>(dst, left_slot + off, own, n, drop);
+            } else {
+                const int t = g - (P - 1);
+                const int k = (r - 1 - t + P) % P;
+                const size_t off = ((size_t)k * c + lo) * ES;
+                if (last)
+                    copy_range<ES, T, kStEvictFirst>(my_slot + off, left_slot + off, n);
+                else
+                    copy_range<ES, T, kStNormal>(my_slot + off, left_slot + off, n);
+            }
+            if (g + 1 < nsteps) {
+                __syncthreads(); // every thread's loads, stores and drops of this step precede the release
+                if (threadIdx.x == 0 && !(r == p.skip_rank && g == p.skip_step))
+                    st_release_gpu(&s_right_rows[(size_t)(g + 1) * P + r], V);
+            }
+            if (threadIdx.x == 0 && s_stamp && q == 0) s_stamp[3 * g + 2] = global_timer_ns();
         }
-        if (threadIdx.x == 0 && s_stamp) s_stamp[3 * g + 2] = global_timer_ns();
+        if (s_abort) break;
     }
 
     // Epilogue: the last block to finish publishes the new epoch.
@@ -316,7 +329,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
         const uint32_t prev = atomicAdd(&p.hdr->done, 1u);
         if (prev == gridDim.x - 1) {
             p.hdr->done = 0;
-            st_relaxed_gpu(&p.hdr->epoch, E);
+            st_relaxed_gpu(&p.hdr->epoch, E0 + (uint32_t)p.segments);
         }
     }
 }

@@ -316,3 +316,47 @@ def test_weak_scaling_workload(P):
             assert torch.equal(bufs[r], bufs[0])
     del bufs
     torch.cuda.empty_cache()
+
+
+_SEGMENT_CHILD = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import oracle, ring_collectives_gb300 as rc
+torch.cuda.set_device(0)
+for P, c, dt in ((8, 64 * 500 + 8, torch.float32), (5, 64 * 333, torch.bfloat16), (16, 64 * 40, torch.int32)):
+    g = torch.Generator().manual_seed(P * 7 + c)
+    if dt == torch.int32:
+        x = torch.randint(-2**31, 2**31 - 1, (P, P * c), generator=g, dtype=torch.int64).to(dt)
+    else:
+        x = torch.randn((P, P * c), generator=g).to(dt)
+    b = x.cuda()
+    rc.ring_allreduce(b)
+    o = torch.empty((P, c), dtype=dt, device="cuda")
+    rc.ring_reduce_scatter(x.cuda(), o)
+    agi = x[:, :c].contiguous()
+    ago = torch.zeros((P, P * c), dtype=dt, device="cuda")
+    rc.ring_all_gather(agi.cuda(), ago)
+    assert rc.ring_status() == 0, rc.ring_last_error()
+    name = {torch.float32: "f32", torch.bfloat16: "bf16", torch.int32: "i32"}[dt]
+    def npv(t):
+        t = t.cpu()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+    xn = npv(x)
+    assert np.array_equal(npv(b), oracle.ring_allreduce(xn.copy(), name)), ("allreduce", P, c, name)
+    assert np.array_equal(npv(o), oracle.reduce_scatter(xn.copy(), name)), ("reduce_scatter", P, c, name)
+    assert np.array_equal(npv(ago), oracle.all_gather(npv(agi), name)), ("all_gather", P, c, name)
+print("ok")
+"""
+
+
+def test_segments_forced_in_a_child_process():
+    """A tiny L2 budget forces many chunk segments (each with its own signal
+    values): results stay bit-exact."""
+    import os
+    import subprocess
+    import sys
+    from tests.conftest import ROOT
+    env = dict(os.environ, RC_L2_LIVE_BYTES="65536")
+    r = subprocess.run([sys.executable, "-c", _SEGMENT_CHILD, ROOT], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
