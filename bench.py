@@ -305,6 +305,39 @@ def ag_gemm_secondary(rc, dev, stream, args):
         "note": "gather of the 8 shards (64 MiB) + C = A_g.B^T, one tcgen05 launch"}}
 
 
+def fold_secondary(rc, dev, stream, args):
+    """Single-pass all-reduces on the benchmark workload: the fused ring-order
+    fold (same bits as ring_allreduce) and the Pallas psum order; both move
+    the minimum 2*P*N*e bytes (roofline (b))."""
+    x = synthetic.workload("f32_64mib")
+    pr = x.to(dev)
+    del x
+    bf = torch.empty_like(pr)
+    P, N = pr.shape
+    out = {}
+    peak = peaks()[0]
+    for name, fn in (("fused_allreduce_f32_64mib", rc.ring_allreduce_fused), ("psum_f32_64mib", rc.ring_psum)):
+        for _ in range(args.warmup):
+            bf.copy_(pr)
+            fn(bf, stream=stream)
+        torch.cuda.synchronize()
+        ev = []
+        for _ in range(args.steps):
+            bf.copy_(pr)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn(bf, stream=stream)
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        gbs = min_bytes(P, N, 4) / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 4), "GB/s_min_bytes": round(gbs, 1), "frac_b": round(gbs / peak, 4),
+                     "ring_bytes_GB/s": round(ring_bytes(P, N, 4) / (ms * 1e-3) / 1e9, 1)}
+    return out
+
+
 def weak_sweep(rc, dev, stream, args):
     """Chunk 4M fp32 per rank-step, P in {2,4,8,16,32}: time per ring step."""
     out = {}
@@ -409,6 +442,7 @@ def run_ours(args, spec, rank, world, dist):
         del pb, bb, out
 
     if not args.no_secondary and spec["name"] == "f32_64mib":
+        secondary.update(fold_secondary(rc, dev, stream, args))
         secondary.update(ag_gemm_secondary(rc, dev, stream, args))
     if args.sweep:
         secondary["weak_scaling"] = weak_sweep(rc, dev, stream, args)

@@ -125,6 +125,31 @@ int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, siz
 int ring_allreduce(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream);
 
 /*
+ * ring_allreduce_fused -- the ring all-reduce's result in a single pass.
+ * Same arguments, validation and result as ring_allreduce, bit for bit:
+ * every element of chunk k becomes R[k] = ((x_{k+1} + x_{k+2}) + ...) + x_k,
+ * the fold order that the reduce-scatter rounds of "全归约 3：Ring——每步大小恒定"
+ * (section "走读") produce.  Instead of 2(P-1) ring steps over HBM, each
+ * element position of all P slots is read once, folded on chip and written
+ * to all P slots: 2*P*N*e bytes, the minimum for an all-reduce.  Uses no
+ * signal workspace.
+ */
+int ring_allreduce_fused(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream);
+
+/*
+ * ring_psum -- rotate-and-accumulate all-reduce of "Pallas TPU Distributed
+ * Collectives 复习文档", section 3 (psum): every rank starts an accumulator at
+ * zero and, in each of P steps, adds the block that arrives from its left
+ * neighbour, so rank r ends with
+ *     o_r = (((0 + x_{r-1}) + x_{r-2}) + ...) + x_r       (indices mod P)
+ * ("+" the element type's hop add).  Each rank folds in its own order, so
+ * floating-point results may differ between ranks (unlike ring_allreduce).
+ * bufs slots: [n] elements at bufs_base + r*stride, replaced by o_r in place.
+ * n need not be a multiple of P.  P = 1: o_0 = 0 + x_0.
+ */
+int ring_psum(void *bufs_base, size_t stride, int P, size_t n, int dtype, void *stream);
+
+/*
  * ring_allreduce_host -- ring_allreduce on inputs held in HOST memory:
  * copies slot r of h_in (host, [N] elements at h_in + r*h_in_stride) into
  * device slot r of d_bufs, runs the all-reduce there, and copies the result

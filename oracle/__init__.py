@@ -59,10 +59,11 @@ def lib() -> ctypes.CDLL:
         L.orc_ring_fold_at.argtypes = [vp, sz, i, sz, i, i64p, sz, vp]
         L.orc_naive_sum.argtypes = [vp, sz, i, sz, i, vp]
         L.orc_ag_gather.argtypes = [vp, sz, i, i, i, vp]
+        L.orc_psum.argtypes = [vp, sz, vp, sz, i, sz, i, i, vp, vp]
         L.orc_gemm_bf16_at.argtypes = [vp, vp, i, i, i, i64p, sz, i64p, sz, vp, vp, vp]
         for f in ("orc_bf16_from_f32", "orc_f32_from_bf16", "orc_ppermute_right", "orc_all_gather",
                   "orc_all_gather_ring", "orc_ring_allreduce", "orc_reduce_scatter",
-                  "orc_ring_fold_at", "orc_naive_sum", "orc_ag_gather", "orc_gemm_bf16_at"):
+                  "orc_ring_fold_at", "orc_naive_sum", "orc_ag_gather", "orc_gemm_bf16_at", "orc_psum"):
             getattr(L, f).restype = i
         _lib = L
     return _lib
@@ -173,6 +174,31 @@ def naive_sum(x: np.ndarray, dtype: str, N: int | None = None) -> np.ndarray:
     out = np.empty(N, dtype=np.int32 if dtype == "i32" else np.float32)
     _check(lib().orc_naive_sum(_ptr(x), x.strides[0], P, N, _DTYPES[dtype][0], _ptr(out)), "naive_sum")
     return out
+
+
+def psum(x: np.ndarray, dtype: str, nsteps: int = -1, buffers: bool = False):
+    """Rotate-and-accumulate all-reduce of [PALLAS] s3: returns o [P, n]
+    (and the final double buffers H0, H1 [P, n] when buffers=True)."""
+    x = _slots(x, dtype)
+    P, n = x.shape
+    out = np.zeros_like(x)
+    h0 = np.zeros_like(x) if buffers else None
+    h1 = np.zeros_like(x) if buffers else None
+    _check(lib().orc_psum(_ptr(x), x.strides[0], _ptr(out), out.strides[0], P, n, _DTYPES[dtype][0], nsteps,
+                          None if h0 is None else _ptr(h0), None if h1 is None else _ptr(h1)), "psum")
+    return (out, h0, h1) if buffers else out
+
+
+def psum_trace(P: int, nsteps: int = -1):
+    """psum on trace cells (one element per device): (o, H0, H1) as text."""
+    cells = trace_cells(P, 1)
+    w = cells.shape[2]
+    out = np.zeros_like(cells)
+    h0 = np.zeros_like(cells)
+    h1 = np.zeros_like(cells)
+    _check(lib().orc_psum(_ptr(cells), cells.strides[0], _ptr(out), out.strides[0], P, 1, TRACE, nsteps,
+                          _ptr(h0), _ptr(h1)), "psum(trace)")
+    return ([t[0] for t in trace_text(out)], [t[0] for t in trace_text(h0)], [t[0] for t in trace_text(h1)])
 
 
 # ---------------------------------------------------------------- trace cells

@@ -439,6 +439,74 @@ int orc_naive_sum(const void *x, size_t stride, int P, size_t N, int dtype, void
 }
 
 /* ------------------------------------------------------------------------ */
+/* psum: unidirectional rotate-and-accumulate all-reduce ([PALLAS] s3, the
+ * psum kernel and the state table of s3.5).  Every device keeps a
+ * two-slot communication buffer H[2] and an accumulator o (zeroed):
+ *   prologue: device r writes x_r into slot 0 of its right neighbour.
+ *   step t = 0 .. P-1 (working = t % 2, receiving = 1 - working):
+ *     recv = own H[working];  the right neighbour's H[receiving] <- own
+ *     H[working] (forward);  o <- o (+) recv.
+ * After P steps o = (((0 (+) x_{r-1}) (+) x_{r-2}) ...) (+) x_r: every
+ * device sums all inputs, each in its own rotated order, so fp results may
+ * differ between devices (the page's point of contrast with the ring).
+ * Messages of a step are taken from every device's state before the step.
+ * x and out are P slots of n elements; h0/h1 (may be NULL) receive the
+ * final H[0] / H[1] of every device (slots of n), for the state-table pin.
+ * nsteps < 0 runs all P steps; the prologue always runs.  Unwritten H slots
+ * are zero.  Pin: the table of [PALLAS] s3.5 (all buffers, every step),
+ * exact integer sums, the per-device order via ORC_TRACE.                  */
+int orc_psum(const void *x, size_t x_stride, void *out, size_t out_stride, int P, size_t n, int dtype,
+             int nsteps, void *h0, void *h1)
+{
+    if (!layout_ok(x, x_stride, P, n, dtype) || !layout_ok(out, out_stride, P, n, dtype)) return -1;
+    size_t es = elem_size(dtype);
+    size_t bytes = n * es;
+    if (bytes == 0) return 0;
+    if (nsteps < 0 || nsteps > P) nsteps = P;
+    char *H = (char *)calloc((size_t)P * 2, bytes);      /* H[r][slot] */
+    char *o = (char *)calloc((size_t)P, bytes);
+    char *snap = (char *)malloc((size_t)P * 2 * bytes);
+    if (!H || !o || !snap) { free(H); free(o); free(snap); return -1; }
+    if (dtype == ORC_TRACE)
+        for (size_t i = 0; i < (size_t)P * n; ++i) strcpy(o + i * ORC_TRACE_W, "0");
+    /* (an all-zero bit pattern is +0 for f32 / bf16 and 0 for i32) */
+    for (int r = 0; r < P; ++r) {
+        int right = (r + 1) % P;
+        memcpy(H + ((size_t)right * 2 + 0) * bytes, cslot_at(x, x_stride, r), bytes);
+    }
+    for (int t = 0; t < nsteps; ++t) {
+        int working = t % 2, receiving = 1 - working;
+        memcpy(snap, H, (size_t)P * 2 * bytes);
+        for (int r = 0; r < P; ++r) {
+            int right = (r + 1) % P;
+            const char *recv = snap + ((size_t)r * 2 + working) * bytes;
+            memcpy(H + ((size_t)right * 2 + receiving) * bytes, recv, bytes);
+        }
+        for (int r = 0; r < P; ++r) {
+            const char *recv = snap + ((size_t)r * 2 + working) * bytes;
+            /* o <- o (+) recv, written as own <- partial (+) own with the
+             * accumulator as the partial: copy, then add the received block */
+            char *acc = o + (size_t)r * bytes;
+            char *tmp = (char *)malloc(bytes);
+            if (!tmp) { free(H); free(o); free(snap); return -1; }
+            memcpy(tmp, recv, bytes);
+            hop_add(dtype, tmp, acc, n);   /* tmp <- acc (+) recv */
+            memcpy(acc, tmp, bytes);
+            free(tmp);
+        }
+    }
+    for (int r = 0; r < P; ++r) {
+        memcpy(slot_at(out, out_stride, r), o + (size_t)r * bytes, bytes);
+        if (h0) memcpy((char *)h0 + (size_t)r * bytes, H + ((size_t)r * 2 + 0) * bytes, bytes);
+        if (h1) memcpy((char *)h1 + (size_t)r * bytes, H + ((size_t)r * 2 + 1) * bytes, bytes);
+    }
+    free(H);
+    free(o);
+    free(snap);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* All-gather + matmul ([TPUBOOK] "collective matmul": gather the row shards,
  * then multiply by the local weight, bf16 result as its _matmul_bf16 casts).
  *

@@ -24,7 +24,7 @@ import torch
 
 __all__ = [
     "RingError", "ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_allreduce",
-    "ring_allreduce_host", "ag_gemm", "ring_status", "ring_last_error", "ring_set_timeout_ms",
+    "ring_allreduce_host", "ring_allreduce_fused", "ring_psum", "ag_gemm", "ring_status", "ring_last_error", "ring_set_timeout_ms",
     "ring_set_slices", "ring_debug_skip_notify", "ring_finalize", "library_path", "load",
 ]
 
@@ -69,7 +69,7 @@ def load() -> ctypes.CDLL:
         L.ring_debug_skip_notify.argtypes = [i, i]
         L.ring_finalize.argtypes = []
         for name in ("ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_allreduce",
-                     "ring_allreduce_host", "ag_gemm", "ring_status", "ring_set_timeout_ms", "ring_set_slices",
+                     "ring_allreduce_host", "ring_allreduce_fused", "ring_psum", "ag_gemm", "ring_status", "ring_set_timeout_ms", "ring_set_slices",
                      "ring_debug_skip_notify", "ring_finalize"):
             getattr(L, name).restype = i
         _lib = L
@@ -145,6 +145,30 @@ def ring_allreduce(bufs: torch.Tensor, N: int | None = None, stream=None) -> tor
     N = bufs.size(1) if N is None else N
     with torch.cuda.device(bufs.device):
         _check(load().ring_allreduce(bp, bs, bufs.size(0), N, dt, _stream(stream, bufs.device)))
+    return bufs
+
+
+def ring_allreduce_fused(bufs: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
+    """Single-pass all-reduce with the ring's result (bit-identical to ring_allreduce)."""
+    fn = load().ring_allreduce_fused
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    bp, bs, dt = _slots(bufs, "bufs")
+    N = bufs.size(1) if N is None else N
+    with torch.cuda.device(bufs.device):
+        _check(fn(bp, bs, bufs.size(0), N, dt, _stream(stream, bufs.device)))
+    return bufs
+
+
+def ring_psum(bufs: torch.Tensor, n: int | None = None, stream=None) -> torch.Tensor:
+    """Rotate-and-accumulate all-reduce (each rank folds in its own rotated order), in place."""
+    fn = load().ring_psum
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    bp, bs, dt = _slots(bufs, "bufs")
+    n = bufs.size(1) if n is None else n
+    with torch.cuda.device(bufs.device):
+        _check(fn(bp, bs, bufs.size(0), n, dt, _stream(stream, bufs.device)))
     return bufs
 
 

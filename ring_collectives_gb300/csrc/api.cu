@@ -404,6 +404,37 @@ int ring_allreduce(void *bufs_base, size_t stride, int P, size_t N, int dtype, v
     return run_ring(p, dtype, (cudaStream_t)stream);
 }
 
+static int run_fold(void *bufs_base, size_t stride, int P, size_t N, int dtype, int order, void *stream)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (order == 0 && N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
+    if (N == 0 || (P == 1 && order == 0)) return RC_OK;
+    if (!bufs_base) return fail(RC_ERR_INVALID, "null slot base");
+    if (P > 1 && stride < N * es) return fail(RC_ERR_INVALID, "stride %zu below the %zu bytes of a slot", stride, N * es);
+    if (!elem_aligned(bufs_base, stride, es))
+        return fail(RC_ERR_INVALID, "slot base and stride must be multiples of the %zu-byte element", es);
+    int dev;
+    DeviceState *st = nullptr;
+    int rc_ = current_device(&dev, &st);
+    if (rc_) return rc_;
+    cudaError_t e = rc::launch_fold((char *)bufs_base, P > 1 ? stride : N * es, P, N, order == 0 ? N / (size_t)P : 1,
+                                    dtype, order, st->sm_count, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fold kernel launch");
+    return RC_OK;
+}
+
+int ring_allreduce_fused(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream)
+{
+    return run_fold(bufs_base, stride, P, N, dtype, 0, stream);
+}
+
+int ring_psum(void *bufs_base, size_t stride, int P, size_t n, int dtype, void *stream)
+{
+    return run_fold(bufs_base, stride, P, n, dtype, 1, stream);
+}
+
 int ring_allreduce_host(const void *h_in, size_t h_in_stride, void *h_out, size_t h_out_stride, void *d_bufs,
                         size_t d_stride, int P, size_t N, int dtype, void *stream)
 {

@@ -44,6 +44,9 @@ struct RingParams {
 // Launch helpers implemented in ring_kernels.cu.  They return a cudaError_t.
 cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_t st);
 cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks);
+// fold_kernels.cu: order 0 = ring order (fused single-pass all-reduce), 1 = psum order.
+cudaError_t launch_fold(char *data, size_t stride, int P, size_t N, size_t chunk, int dtype, int order, int sm_count,
+                        cudaStream_t st);
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P,
                             size_t n, int esize, int sm_count, cudaStream_t st);
 

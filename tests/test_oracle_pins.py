@@ -334,3 +334,54 @@ def test_gemm_matches_numpy_float64_and_sampling():
     f64s, b16s, _ = oracle.gemm_bf16_at(A, B, rows, cols)
     assert np.array_equal(f64s, f64[np.ix_(rows, cols)])
     assert np.array_equal(b16s, b16[np.ix_(rows, cols)])
+
+
+# ---------------------------------------------------------------- psum (rotate-and-accumulate)
+def _flatten_trace(t):
+    """'((0+3)+2)' -> [3, 2]: the contributors in association order, zero dropped."""
+    toks = t.replace("(", " ").replace(")", " ").replace("+", " ").split()
+    out = [int(x) for x in toks]
+    return out[1:] if out and out[0] == 0 and len(out) > 1 else ([] if out == [0] else out)
+
+
+def test_psum_matches_pallas_state_table_p4():
+    """(H0, H1, o) of every device after the prologue and each step ([PALLAS] s3.5)."""
+    rows = _golden_lines("psum_p4_states.txt")
+    for i, row in enumerate(rows):
+        o, h0, h1 = oracle.psum_trace(4, nsteps=i)   # row 0 = prologue only
+        for r, cell in enumerate(row[1:]):
+            H0, H1, acc = cell.split(",")
+            assert h0[r] == ("" if H0 == "-" else H0[1:]), (row[0], r, "H0")
+            assert h1[r] == ("" if H1 == "-" else H1[1:]), (row[0], r, "H1")
+            got = _flatten_trace(o[r])
+            if acc == "0":
+                assert got == []
+            elif acc == "all":
+                assert got == [(r - 1 - t) % 4 for t in range(4)]
+            else:
+                assert got == [int(term[1:]) for term in acc.split("+")], (row[0], r, o[r])
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 5, 8])
+def test_psum_integer_exact_and_bitmask(P):
+    g = np.random.default_rng(P)
+    xi = g.integers(-1000, 1001, size=(P, 77))
+    out = oracle.psum(xi.astype(np.float32), "f32")
+    assert np.all(out == xi.sum(axis=0).astype(np.float32))
+    x = np.zeros((P, 9), dtype=np.int32)
+    for r in range(P):
+        x[r] = int(np.uint32(1 << r).astype(np.int32))
+    assert np.all(oracle.psum(x, "i32").view(np.uint32) == np.uint32((1 << P) - 1))
+
+
+def test_psum_rank_orders_differ_in_floating_point():
+    """Each device folds in its own rotated order, so some fp results differ
+    between devices, while the ring all-reduce leaves every device identical."""
+    g = np.random.default_rng(3)
+    x = g.standard_normal((8, 4096)).astype(np.float32)
+    out = oracle.psum(x, "f32")
+    assert any(not np.array_equal(out[0], out[r]) for r in range(1, 8))
+    exact = np.array([math.fsum(x[:, i].astype(np.float64)) for i in range(x.shape[1])])
+    assert np.all(np.abs(out.astype(np.float64) - exact) <= 8 * 2.0**-24 * np.abs(x).sum(axis=0))
+    o5, _, _ = oracle.psum_trace(5)
+    assert [_flatten_trace(t) for t in o5] == [[(r - 1 - t) % 5 for t in range(5)] for r in range(5)]
