@@ -250,10 +250,11 @@ def time_allreduce(rc, bufs, pristine, N, steps, warmup, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def time_reduce_scatter(rc, bufs, out, pristine, N, steps, warmup, stream):
+def time_reduce_scatter(rc, bufs, out, pristine, N, steps, warmup, stream, fn=None):
+    fn = rc.ring_reduce_scatter if fn is None else fn
     for _ in range(warmup):
         bufs.copy_(pristine)
-        rc.ring_reduce_scatter(bufs, out, N=N, stream=stream)
+        fn(bufs, out, N=N, stream=stream)
     torch.cuda.synchronize()
     ts = []
     for _ in range(steps):
@@ -261,7 +262,7 @@ def time_reduce_scatter(rc, bufs, out, pristine, N, steps, warmup, stream):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        rc.ring_reduce_scatter(bufs, out, N=N, stream=stream)
+        fn(bufs, out, N=N, stream=stream)
         b.record(stream)
         ts.append((a, b))
     torch.cuda.synchronize()
@@ -429,12 +430,18 @@ def run_ours(args, spec, rank, world, dist):
         tb = time_allreduce(rc, bb, pb, Nb, args.steps, args.warmup, stream)
         out = torch.empty((8, Nb // 8), dtype=torch.bfloat16, device=dev)
         trs = time_reduce_scatter(rc, bb, out, pb, Nb, args.steps, args.warmup, stream)
+        tbi = time_reduce_scatter(rc, bb, out, pb, Nb, args.steps, args.warmup, stream,
+                                  fn=rc.ring_reduce_scatter_bidir)
         if rc.ring_status(stream) != 0:
             raise RuntimeError(rc.ring_last_error())
         mb, mrs = statistics.mean(tb), statistics.mean(trs)
         secondary = {
             "bf16_64mib_allreduce": {"ms": round(mb, 4), "GB/s": round(ring_bytes(8, Nb, 2) / mb / 1e6, 1),
                                      "frac_a": round(ring_bytes(8, Nb, 2) / mb / 1e6 / peaks()[0], 4)},
+            "bf16_64mib_reduce_scatter_bidir": {
+                "ms": round(statistics.mean(tbi), 4),
+                "GB/s": round(3 * 7 * Nb * 2 / statistics.mean(tbi) / 1e6, 1),
+                "note": "Pallas-style bidirectional reduce-scatter: P steps, top halves left, bottoms right"},
             "bf16_64mib_reduce_scatter": {"ms": round(mrs, 4),
                                           "GB/s": round(3 * 7 * Nb * 2 / mrs / 1e6, 1),
                                           "frac_a": round(3 * 7 * Nb * 2 / mrs / 1e6 / peaks()[0], 4)},

@@ -107,6 +107,25 @@ int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, siz
                         int P, size_t N, int dtype, void *stream);
 
 /*
+ * ring_reduce_scatter_bidir -- bidirectional reduce-scatter of "Pallas TPU
+ * Distributed Collectives 复习文档", section 4 (psum_scatter): every chunk k
+ * (a block of c = N/P elements) is split into a top half, elements
+ * [0, c/2), whose partial sums travel LEFT round the ring, and a bottom half,
+ * [c/2, c), whose partial sums travel RIGHT; both start at rank k with its
+ * own contribution and are delivered to rank k after P-1 additions.
+ * Result: out_r = block r summed over ranks, with
+ *     top:    ((x_r + x_{r-1}) + x_{r-2}) + ... + x_{r+1}
+ *     bottom: ((x_r + x_{r+1}) + x_{r+2}) + ... + x_{r-1}   (indices mod P)
+ * ("+" the element type's hop add), the order of the page's state tables.
+ * bufs slots: [N] elements at bufs_base + r*bufs_stride; CLOBBERED (contents
+ *     undefined afterwards, as for ring_reduce_scatter).
+ * out slots:  [N/P] elements at out_base + r*out_stride (written).
+ * N must be a multiple of P (RC_ERR_INVALID otherwise).  P = 1 copies.
+ */
+int ring_reduce_scatter_bidir(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P,
+                              size_t N, int dtype, void *stream);
+
+/*
  * ring_allreduce -- in-place ring all-reduce: reduce-scatter (P-1 rounds)
  * then all-gather (P-1 rounds), 2(P-1) steps of one chunk each.
  * "全归约 3：Ring——每步大小恒定", sections "思路" and "走读":

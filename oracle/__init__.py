@@ -60,10 +60,12 @@ def lib() -> ctypes.CDLL:
         L.orc_naive_sum.argtypes = [vp, sz, i, sz, i, vp]
         L.orc_ag_gather.argtypes = [vp, sz, i, i, i, vp]
         L.orc_psum.argtypes = [vp, sz, vp, sz, i, sz, i, i, vp, vp]
+        L.orc_reduce_scatter_bidir.argtypes = [vp, sz, vp, sz, i, sz, i, i, vp]
         L.orc_gemm_bf16_at.argtypes = [vp, vp, i, i, i, i64p, sz, i64p, sz, vp, vp, vp]
         for f in ("orc_bf16_from_f32", "orc_f32_from_bf16", "orc_ppermute_right", "orc_all_gather",
                   "orc_all_gather_ring", "orc_ring_allreduce", "orc_reduce_scatter",
-                  "orc_ring_fold_at", "orc_naive_sum", "orc_ag_gather", "orc_gemm_bf16_at", "orc_psum"):
+                  "orc_ring_fold_at", "orc_naive_sum", "orc_ag_gather", "orc_gemm_bf16_at", "orc_psum",
+                  "orc_reduce_scatter_bidir"):
             getattr(L, f).restype = i
         _lib = L
     return _lib
@@ -199,6 +201,35 @@ def psum_trace(P: int, nsteps: int = -1):
     _check(lib().orc_psum(_ptr(cells), cells.strides[0], _ptr(out), out.strides[0], P, 1, TRACE, nsteps,
                           _ptr(h0), _ptr(h1)), "psum(trace)")
     return ([t[0] for t in trace_text(out)], [t[0] for t in trace_text(h0)], [t[0] for t in trace_text(h1)])
+
+
+def reduce_scatter_bidir(x: np.ndarray, dtype: str, N: int | None = None) -> np.ndarray:
+    """Bidirectional reduce-scatter of [PALLAS] s4: returns out [P, N/P] (block r on rank r)."""
+    x = _slots(x, dtype)
+    P, L = x.shape
+    N = L if N is None else N
+    out = np.zeros((P, N // P), dtype=x.dtype)
+    _check(lib().orc_reduce_scatter_bidir(_ptr(x), x.strides[0], _ptr(out), out.strides[0], P, N,
+                                          _DTYPES[dtype][0], -1, None), "reduce_scatter_bidir")
+    return out
+
+
+def reduce_scatter_bidir_trace(P: int, iters: int):
+    """State of every device after `iters` iterations, blocks of 2 cells (top,
+    bottom); cell of device d, block b is labelled 'd:b'.  Returns per device
+    [H0.top, H0.bot, H1.top, H1.bot, accum, o.top, o.bot] as text."""
+    w = lib().orc_trace_width()
+    cells = np.zeros((P, 2 * P, w), dtype=np.uint8)
+    for d in range(P):
+        for b in range(P):
+            lab = f"{d}:{b}".encode()
+            for h in range(2):
+                cells[d, 2 * b + h, :len(lab)] = np.frombuffer(lab, dtype=np.uint8)
+    out = np.zeros((P, 2, w), dtype=np.uint8)
+    state = np.zeros((P, 7, w), dtype=np.uint8)
+    _check(lib().orc_reduce_scatter_bidir(_ptr(cells), cells.strides[0], _ptr(out), out.strides[0], P, 2 * P,
+                                          TRACE, iters, _ptr(state)), "reduce_scatter_bidir(trace)")
+    return [[bytes(state[d, k]).split(b"\0", 1)[0].decode() for k in range(7)] for d in range(P)]
 
 
 # ---------------------------------------------------------------- trace cells

@@ -507,6 +507,121 @@ int orc_psum(const void *x, size_t x_stride, void *out, size_t out_stride, int P
 }
 
 /* ------------------------------------------------------------------------ */
+/* Bidirectional reduce-scatter ([PALLAS] s4, the psum_scatter kernel and the
+ * state tables of s4.6).  Every device holds P blocks x_me[b] (block b =
+ * elements [b*c, (b+1)*c), c = N/P); a block is split into a top half
+ * (elements [0, c/2)) that travels LEFT and a bottom half ([c/2, c)) that
+ * travels RIGHT.  Device me keeps a two-slot buffer H[2] (each slot one
+ * block: top + bottom), an accumulator and its output o (block me).
+ * The grid is (step = 0..P-1) x (phase = LEFT, RIGHT); with working =
+ * step % 2, receiving = 1 - working, left_block = (me+step+1) % P,
+ * right_block = (me-step-1) % P, in this order per iteration:
+ *   first iteration (0, LEFT): o = 0; init_left: the LEFT neighbour's
+ *     H[working].top <- x_me[me].top, completed before the local update;
+ *     init_right: the RIGHT neighbour's H[working].bottom <- x_me[me].bottom.
+ *   other LEFT phases:  send_right: RIGHT neighbour's H[working].bottom <-
+ *     own H[receiving].bottom.
+ *   RIGHT phases:       send_left: LEFT neighbour's H[receiving].top <- own
+ *     H[working].top.
+ *   local update of the current half (top in LEFT, bottom in RIGHT):
+ *     accum <- H[working].half; unless last step: accum <- accum (+)
+ *     x_me[left_block or right_block].half; H[working].half <- accum; on the
+ *     last step o.half <- accum.
+ * Transfers started in an iteration land at its end (the page waits on them
+ * before the next iteration); they never touch the half being updated.
+ * Result: o_me.top = ((x_me + x_{me-1}) + ...) + x_{me+1} over block me's
+ * top halves, o_me.bottom = ((x_me + x_{me+1}) + ...) + x_{me-1} over its
+ * bottom halves.
+ * out: P slots of c elements.  iters (< 0: all 2P) limits the iterations run;
+ * state (may be NULL) receives, per device, H0.top H0.bot H1.top H1.bot
+ * accum o.top o.bot as [P][7][hmax] elements, hmax = c - c/2 (top halves
+ * padded); for ORC_TRACE, never-written cells stay empty.
+ * Pin: the eight state tables of [PALLAS] s4.6; block sums in integers.    */
+int orc_reduce_scatter_bidir(const void *x, size_t x_stride, void *out, size_t out_stride, int P, size_t N,
+                             int dtype, int iters, void *state)
+{
+    if (!layout_ok(x, x_stride, P, N, dtype)) return -1;
+    if (N % (size_t)P) return -1;
+    size_t es = elem_size(dtype), c = N / (size_t)P;
+    if (!layout_ok(out, out_stride, P, c, dtype)) return -1;
+    if (c == 0) return 0;
+    size_t half = c / 2, hmax = c - half;     /* top: [0, half), bottom: [half, c) */
+    size_t cb = c * es;
+    char *H = (char *)calloc((size_t)P * 2, cb);    /* H[me][slot] block */
+    char *acc = (char *)calloc((size_t)P, hmax * es);
+    char *o = (char *)calloc((size_t)P, cb);
+    char *tmp = (char *)malloc(hmax * es);
+    if (!H || !acc || !o || !tmp) { free(H); free(acc); free(o); free(tmp); return -1; }
+#define HB(me, slot) (H + ((size_t)(me) * 2 + (slot)) * cb)
+#define XB(me, b) (cslot_at(x, x_stride, (me)) + (size_t)(b) * cb)
+    int total = 2 * P;
+    if (iters < 0 || iters > total) iters = total;
+    for (int it = 0; it < iters; ++it) {
+        int step = it / 2, phase = it % 2;           /* phase 0 = LEFT, 1 = RIGHT */
+        int working = step % 2, receiving = 1 - working;
+        int is_first = (step == 0 && phase == 0), is_last = (step == P - 1);
+        if (is_first)                                /* init_left, completed before the local update */
+            for (int me = 0; me < P; ++me)
+                memcpy(HB((me - 1 + P) % P, working), XB(me, me), half * es);
+        /* transfers started now, landing at the end of the iteration (taken from the current state) */
+        char *pending = (char *)malloc((size_t)P * cb);
+        if (!pending) { free(H); free(acc); free(o); free(tmp); return -1; }
+        for (int me = 0; me < P; ++me) {
+            char *msg = pending + (size_t)me * cb;
+            if (is_first)
+                memcpy(msg, XB(me, me) + half * es, hmax * es);             /* bottom of x_me[me] */
+            else if (phase == 0)
+                memcpy(msg, HB(me, receiving) + half * es, hmax * es);      /* own H[receiving].bottom */
+            else
+                memcpy(msg, HB(me, working), half * es);                     /* own H[working].top */
+        }
+        /* local update of the current half */
+        for (int me = 0; me < P; ++me) {
+            size_t off = phase == 0 ? 0 : half, len = phase == 0 ? half : hmax;
+            int blk = phase == 0 ? (me + step + 1) % P : ((me - step - 1) % P + P) % P;
+            char *a = acc + (size_t)me * hmax * es;
+            memcpy(a, HB(me, working) + off * es, len * es);
+            if (!is_last) {
+                memcpy(tmp, XB(me, blk) + off * es, len * es);
+                hop_add(dtype, tmp, a, len);      /* tmp <- accum (+) x */
+                memcpy(a, tmp, len * es);
+            }
+            memcpy(HB(me, working) + off * es, a, len * es);
+            if (is_last) memcpy(o + (size_t)me * cb + off * es, a, len * es);
+        }
+        /* land the transfers */
+        for (int me = 0; me < P; ++me) {
+            const char *msg = pending + (size_t)me * cb;
+            if (is_first || phase == 0)
+                memcpy(HB((me + 1) % P, working) + half * es, msg, hmax * es);
+            else
+                memcpy(HB((me - 1 + P) % P, receiving), msg, half * es);
+        }
+        free(pending);
+    }
+    for (int me = 0; me < P; ++me) {
+        memcpy(slot_at(out, out_stride, me), o + (size_t)me * cb, cb);
+        if (state) {
+            char *st = (char *)state + (size_t)me * 7 * hmax * es;
+            memcpy(st + 0 * hmax * es, HB(me, 0), half * es);
+            memcpy(st + 1 * hmax * es, HB(me, 0) + half * es, hmax * es);
+            memcpy(st + 2 * hmax * es, HB(me, 1), half * es);
+            memcpy(st + 3 * hmax * es, HB(me, 1) + half * es, hmax * es);
+            memcpy(st + 4 * hmax * es, acc + (size_t)me * hmax * es, hmax * es);
+            memcpy(st + 5 * hmax * es, o + (size_t)me * cb, half * es);
+            memcpy(st + 6 * hmax * es, o + (size_t)me * cb + half * es, hmax * es);
+        }
+    }
+#undef HB
+#undef XB
+    free(H);
+    free(acc);
+    free(o);
+    free(tmp);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* All-gather + matmul ([TPUBOOK] "collective matmul": gather the row shards,
  * then multiply by the local weight, bf16 result as its _matmul_bf16 casts).
  *

@@ -139,6 +139,24 @@ def ring_reduce_scatter(bufs: torch.Tensor, out: torch.Tensor, N: int | None = N
     return out
 
 
+def ring_reduce_scatter_bidir(bufs: torch.Tensor, out: torch.Tensor, N: int | None = None,
+                              stream=None) -> torch.Tensor:
+    """Bidirectional reduce-scatter (top halves travel left, bottom halves right);
+    out[r, :N/P] = block r summed over ranks; ``bufs`` is clobbered."""
+    fn = load().ring_reduce_scatter_bidir
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                   ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    bp, bs, dt = _slots(bufs, "bufs")
+    op, os_, dt2 = _slots(out, "out")
+    if dt != dt2 or bufs.size(0) != out.size(0):
+        raise ValueError("bufs and out differ in dtype or rank count")
+    N = bufs.size(1) if N is None else N
+    with torch.cuda.device(bufs.device):
+        _check(fn(bp, bs, op, os_, bufs.size(0), N, dt, _stream(stream, bufs.device)))
+    return out
+
+
 def ring_allreduce(bufs: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
     """In-place ring all-reduce over the first N elements of every row."""
     bp, bs, dt = _slots(bufs, "bufs")

@@ -195,12 +195,15 @@ int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda)
     int rc_ = current_device(&dev, &st);
     if (rc_) return rc_;
     const size_t es = elem_size(dtype);
-    rc_ = choose_slices(*st, dtype, p.P, p.chunk, p.chunk * es, &p.S);
+    // The bidirectional reduce-scatter runs two rings (top and bottom halves) per slice.
+    const int rings = p.mode == rc::MODE_RS_BIDIR ? 2 : 1;
+    const size_t ring_elems = p.chunk / (size_t)rings;
+    rc_ = choose_slices(*st, dtype, p.P * rings, ring_elems, ring_elems * es, &p.S);
     if (rc_) return rc_;
     {
         const size_t live = (size_t)p.P * p.chunk * es, budget = l2_live_bytes();
         size_t G = budget ? (live + budget - 1) / budget : 1;
-        const size_t max_g = p.chunk / ((size_t)p.S * rc::kSliceGranule); // keep every slice non-empty
+        const size_t max_g = ring_elems / ((size_t)p.S * rc::kSliceGranule); // keep every slice non-empty
         if (G > max_g) G = max_g;
         if (G > 64) G = 64;
         if (G < 1) G = 1;
@@ -377,6 +380,36 @@ int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, siz
     p.P = P;
     p.rows = P - 1;
     p.mode = rc::MODE_REDUCE_SCATTER;
+    p.discard = 1;
+    return run_ring(p, dtype, (cudaStream_t)stream);
+}
+
+int ring_reduce_scatter_bidir(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P,
+                              size_t N, int dtype, void *stream)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
+    if (N == 0) return RC_OK;
+    if (!bufs_base || !out_base) return fail(RC_ERR_INVALID, "null slot base");
+    const size_t c = N / (size_t)P;
+    if (P > 1 && (bufs_stride < N * es || out_stride < c * es))
+        return fail(RC_ERR_INVALID, "stride below a slot's bytes (bufs %zu, out %zu)", N * es, c * es);
+    if (regions_overlap(bufs_base, bufs_stride, N * es, out_base, out_stride, c * es, P))
+        return fail(RC_ERR_INVALID, "bufs and out slots overlap");
+    if (!elem_aligned(bufs_base, bufs_stride, es) || !elem_aligned(out_base, out_stride, es))
+        return fail(RC_ERR_INVALID, "slot bases and strides must be multiples of the %zu-byte element", es);
+    if (P == 1) return run_copy(bufs_base, bufs_stride, out_base, out_stride, 1, c, dtype, (cudaStream_t)stream);
+    rc::RingParams p{};
+    p.data = (char *)bufs_base;
+    p.data_stride = bufs_stride;
+    p.out = (char *)out_base;
+    p.out_stride = out_stride;
+    p.chunk = c;
+    p.P = P;
+    p.rows = 2 * P;   // P steps for each of the two halves
+    p.mode = rc::MODE_RS_BIDIR;
     p.discard = 1;
     return run_ring(p, dtype, (cudaStream_t)stream);
 }

@@ -19,7 +19,7 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 128, "header is one 128-byte line");
 
-enum RingMode { MODE_ALLREDUCE = 0, MODE_REDUCE_SCATTER = 1, MODE_ALL_GATHER = 2 };
+enum RingMode { MODE_ALLREDUCE = 0, MODE_REDUCE_SCATTER = 1, MODE_ALL_GATHER = 2, MODE_RS_BIDIR = 3 };
 
 // Arguments of one launch of the ring step engine.
 struct RingParams {
@@ -27,7 +27,7 @@ struct RingParams {
     size_t data_stride;  // bytes between slots
     const char *in;      // all-gather: input shards
     size_t in_stride;
-    char *out;           // reduce-scatter: output chunks
+    char *out;           // reduce-scatters: output chunks
     size_t out_stride;
     uint32_t *sig;       // signal rows, [S][P][rows][P] words
     WsHeader *hdr;

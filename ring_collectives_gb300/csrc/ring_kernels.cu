@@ -210,29 +210,43 @@ __device__ bool wait_row(const uint32_t *flag, uint32_t V, uint32_t E, const Rin
 // E0 + q + 1 on the same rows (E0: the epoch before the launch), so values
 // stay monotonic across segments and launches; the launch advances the epoch
 // by the number of segments.
-template <int DT>
+//
+// MODE_RS_BIDIR (the bidirectional reduce-scatter of "Pallas TPU Distributed
+// Collectives 复习文档", section 4): block (h, r, j) runs half h of every
+// chunk (h = 0: the top half [0, c/2), which travels left; h = 1: the bottom
+// half [c/2, c), which travels right) as its own ring.  In step s < P-1 rank
+// r adds the partial its upstream neighbour (right for the top, left for the
+// bottom) holds for chunk (r+1+s) resp. (r-1-s) to its own contribution; in
+// step P-1 it copies the finished chunk r from that neighbour to out_r.  Each
+// chunk half is written once, so no buffer is ever overwritten while read.
+template <int DT, int MODE>
 __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const RingParams p)
 {
     constexpr size_t ES = DT == 1 ? 2 : 4;
+    constexpr bool BIDIR = MODE == MODE_RS_BIDIR;
     const int P = p.P, S = p.S;
-    const int r = (int)(blockIdx.x / (unsigned)S), j = (int)(blockIdx.x % (unsigned)S);
+    const int rs = (int)(blockIdx.x / (unsigned)S), j = (int)(blockIdx.x % (unsigned)S);
+    const int h = BIDIR ? rs / P : 0;              // half (bidirectional mode only)
+    const int r = BIDIR ? rs % P : rs;
     const int left = (r - 1 + P) % P, right = (r + 1) % P;
+    const int from = (BIDIR && h == 0) ? right : left; // whose data this block pulls
+    const int to = (BIDIR && h == 0) ? left : right;   // whom this block notifies
     // The abort word is the header's pad[0]: a launch that gives up stores its epoch there.
     uint32_t *abort_word = &p.hdr->pad[0];
-    const int nsteps = p.mode == MODE_ALLREDUCE ? 2 * (P - 1) : P - 1;
+    const int nsteps = MODE == MODE_ALLREDUCE ? 2 * (P - 1) : BIDIR ? P : P - 1;
 
     // State only thread 0 uses (signal rows, step stamps) lives in shared
     // memory so it does not hold registers through the streaming loops.
     __shared__ uint32_t s_epoch0;
     __shared__ int s_abort;
-    __shared__ const uint32_t *s_my_rows;   // [rows][P] signal words of (rank r, slice j)
-    __shared__ uint32_t *s_right_rows;      // the same for (right, j)
+    __shared__ const uint32_t *s_my_rows;   // [steps][P] signal words of (rank r, slice j, half h)
+    __shared__ uint32_t *s_to_rows;         // the same for the block this one notifies
     __shared__ unsigned long long *s_stamp; // step stamps of this block, or null
     if (threadIdx.x == 0) {
         s_epoch0 = ld_relaxed_gpu(&p.hdr->epoch);
         s_abort = 0;
-        s_my_rows = p.sig + ((size_t)j * P + r) * (size_t)p.rows * P;
-        s_right_rows = p.sig + ((size_t)j * P + right) * (size_t)p.rows * P;
+        s_my_rows = p.sig + (((size_t)j * P + r) * (size_t)p.rows + (size_t)h * nsteps) * P;
+        s_to_rows = p.sig + (((size_t)j * P + to) * (size_t)p.rows + (size_t)h * nsteps) * P;
         s_stamp = (p.trace && (size_t)(blockIdx.x + 1) * nsteps * 3 <= p.trace_words)
                       ? p.trace + (size_t)blockIdx.x * nsteps * 3
                       : nullptr;
@@ -241,52 +255,69 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
     const uint32_t E0 = s_epoch0;
     const uint32_t E = E0 + 1u;   // identifies this launch (abort word)
     const size_t c = p.chunk;
+    const size_t half = c / 2;
+    const size_t range_lo = BIDIR ? (h == 0 ? 0 : half) : 0;     // element range of this block's ring
+    const size_t range_n = BIDIR ? (h == 0 ? half : c - half) : c;
     char *my_slot = p.data + (size_t)r * p.data_stride;
-    const char *left_slot = p.data + (size_t)left * p.data_stride;
+    const char *from_slot = p.data + (size_t)from * p.data_stride;
     constexpr int T = kRingThreads;
 
     for (int q = 0; q < p.segments; ++q) {
-        const size_t seg_lo = slice_begin(c, q, p.segments);
-        const size_t seg_n = slice_begin(c, q + 1, p.segments) - seg_lo;
+        const size_t seg_lo = range_lo + slice_begin(range_n, q, p.segments);
+        const size_t seg_n = range_lo + slice_begin(range_n, q + 1, p.segments) - seg_lo;
         const size_t lo = seg_lo + slice_begin(seg_n, j, S);
         const size_t n = seg_lo + slice_begin(seg_n, j + 1, S) - lo;
         const uint32_t V = E0 + 1u + (uint32_t)q; // signal value of this segment
 
-        if (p.mode == MODE_ALL_GATHER) {
+        if (MODE == MODE_ALL_GATHER) {
             // Prologue: the own shard goes to chunk r of the own output slot,
             // then the right neighbour's first row says it may be read.
             copy_range<ES, T, kStNormal>(my_slot + ((size_t)r * c + lo) * ES, p.in + (size_t)r * p.in_stride + lo * ES,
                                          n);
             __syncthreads();
-            if (threadIdx.x == 0) st_release_gpu(&s_right_rows[r], V);
+            if (threadIdx.x == 0) st_release_gpu(&s_to_rows[r], V);
         }
 
         // Step stamps (%globaltimer, thread 0, first segment): per block and
         // step, the start of the wait, its end, and the end of the step.
         for (int g = 0; g < nsteps; ++g) {
             if (threadIdx.x == 0 && s_stamp && q == 0) s_stamp[3 * g] = global_timer_ns();
-            if (g > 0 || p.mode == MODE_ALL_GATHER) {
+            if (g > 0 || MODE == MODE_ALL_GATHER) {
                 if (threadIdx.x == 0 &&
-                    !wait_row(&s_my_rows[(size_t)g * P + left], V, E, p, r, g, j, abort_word))
+                    !wait_row(&s_my_rows[(size_t)g * P + from], V, E, p, r, g, j, abort_word))
                     s_abort = 1;
                 __syncthreads();
                 if (s_abort) break;
             }
             if (threadIdx.x == 0 && s_stamp && q == 0) s_stamp[3 * g + 1] = global_timer_ns();
             const bool last = g == nsteps - 1; // nothing reads this step's output again in this launch
-            if (p.mode == MODE_ALL_GATHER) {
+            if (MODE == MODE_ALL_GATHER) {
                 const int k = (r - 1 - g + P) % P;
                 const size_t off = ((size_t)k * c + lo) * ES;
                 if (last)
-                    copy_range<ES, T, kStEvictFirst>(my_slot + off, left_slot + off, n);
+                    copy_range<ES, T, kStEvictFirst>(my_slot + off, from_slot + off, n);
                 else
-                    copy_range<ES, T, kStNormal>(my_slot + off, left_slot + off, n);
+                    copy_range<ES, T, kStNormal>(my_slot + off, from_slot + off, n);
+            } else if (BIDIR) {
+                if (g < P - 1) {
+                    // partial for chunk k: the upstream neighbour's partial (+) own contribution
+                    const int k = h == 0 ? (r + 1 + g) % P : (r - 1 - g + 2 * P) % P;
+                    const size_t off = ((size_t)k * c + lo) * ES;
+                    // The partial read here is dead afterwards (no one reads or
+                    // rewrites it again): its lines are dropped from round 1 on.
+                    add_range<DT, T, kStEvictLast>(my_slot + off, from_slot + off, my_slot + off, n,
+                                                   p.discard && g >= 1);
+                } else {
+                    // the neighbour's partial for chunk r is complete: deliver it
+                    copy_range<ES, T, kStNormal>(p.out + (size_t)r * p.out_stride + lo * ES,
+                                                 from_slot + ((size_t)r * c + lo) * ES, n);
+                }
             } else if (g < P - 1) {
                 const int s = g;
                 const int k = (r - s - 2 + P) % P; // recv_add_idx == left_send_idx
                 const size_t off = ((size_t)k * c + lo) * ES;
                 char *own = my_slot + off;
-                char *dst = (p.mode == MODE_REDUCE_SCATTER && s == P - 2)
+                char *dst = (MODE == MODE_REDUCE_SCATTER && s == P - 2)
                                 ? p.out + (size_t)r * p.out_stride + lo * ES
                                 : own;
                 // From round 1 on, the left chunk read here is the partial sum the
@@ -300,22 +331,22 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                 // round writes the reduced chunk (read by the all-gather, or the output).
                 const bool drop = p.discard && s >= 1;
                 if (p.discard && s < P - 2)
-                    add_range<DT, T, kStEvictLast>(dst, left_slot + off, own, n, drop);
+                    add_range<DT, T, kStEvictLast>(dst, from_slot + off, own, n, drop);
                 else
-                    add_range<DT, T, kStNormal>(dst, left_slot + off, own, n, drop);
+                    add_range<DT, T, kStNormal>(dst, from_slot + off, own, n, drop);
             } else {
                 const int t = g - (P - 1);
                 const int k = (r - 1 - t + P) % P;
                 const size_t off = ((size_t)k * c + lo) * ES;
                 if (last)
-                    copy_range<ES, T, kStEvictFirst>(my_slot + off, left_slot + off, n);
+                    copy_range<ES, T, kStEvictFirst>(my_slot + off, from_slot + off, n);
                 else
-                    copy_range<ES, T, kStNormal>(my_slot + off, left_slot + off, n);
+                    copy_range<ES, T, kStNormal>(my_slot + off, from_slot + off, n);
             }
             if (g + 1 < nsteps) {
                 __syncthreads(); // every thread's loads, stores and drops of this step precede the release
                 if (threadIdx.x == 0 && !(r == p.skip_rank && g == p.skip_step))
-                    st_release_gpu(&s_right_rows[(size_t)(g + 1) * P + r], V);
+                    st_release_gpu(&s_to_rows[(size_t)(g + 1) * P + r], V);
             }
             if (threadIdx.x == 0 && s_stamp && q == 0) s_stamp[3 * g + 2] = global_timer_ns();
         }
@@ -353,23 +384,39 @@ __global__ void __launch_bounds__(256) k_ppermute(const char *src, size_t ss, ch
 }
 
 // ------------------------------------------------------------ host launchers
-static const void *ring_fn(int dtype)
+template <int DT>
+static const void *ring_fn_mode(int mode)
+{
+    switch (mode) {
+    case MODE_ALLREDUCE: return (const void *)k_ring<DT, MODE_ALLREDUCE>;
+    case MODE_REDUCE_SCATTER: return (const void *)k_ring<DT, MODE_REDUCE_SCATTER>;
+    case MODE_ALL_GATHER: return (const void *)k_ring<DT, MODE_ALL_GATHER>;
+    default: return (const void *)k_ring<DT, MODE_RS_BIDIR>;
+    }
+}
+
+static const void *ring_fn(int dtype, int mode)
 {
     switch (dtype) {
-    case 0: return (const void *)k_ring<0>;
-    case 1: return (const void *)k_ring<1>;
-    default: return (const void *)k_ring<2>;
+    case 0: return ring_fn_mode<0>(mode);
+    case 1: return ring_fn_mode<1>(mode);
+    default: return ring_fn_mode<2>(mode);
     }
 }
 
 cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks)
 {
-    int per_sm = 0, sms = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_fn(dtype), threads, 0);
+    // every mode instantiation has the same register budget (launch bounds); take the minimum
+    int sms = 0, best = 1 << 30;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    if (e != cudaSuccess) return e;
-    *blocks = per_sm * sms;
+    for (int mode = 0; mode < 4; ++mode) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_fn(dtype, mode), threads, 0);
+        if (e != cudaSuccess) return e;
+        if (per_sm < best) best = per_sm;
+    }
+    *blocks = best * sms;
     return cudaSuccess;
 }
 
@@ -377,8 +424,8 @@ cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_
 {
     RingParams copy = p;
     void *args[] = {(void *)&copy};
-    return cudaLaunchCooperativeKernel(ring_fn(dtype), dim3((unsigned)(p.P * p.S)), dim3((unsigned)threads),
-                                       args, 0, st);
+    const unsigned blocks = (unsigned)(p.P * p.S) * (p.mode == MODE_RS_BIDIR ? 2u : 1u);
+    return cudaLaunchCooperativeKernel(ring_fn(dtype, p.mode), dim3(blocks), dim3((unsigned)threads), args, 0, st);
 }
 
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P, size_t n,

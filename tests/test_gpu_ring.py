@@ -360,3 +360,27 @@ def test_segments_forced_in_a_child_process():
     r = subprocess.run([sys.executable, "-c", _SEGMENT_CHILD, ROOT], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+# ------------------------------------------------------------------ bidirectional reduce-scatter
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
+@pytest.mark.parametrize("P,c", [(1, 100), (2, 2), (2, 7), (3, 1), (4, 256), (4, 2048), (5, 1001), (8, 64 * 33 + 6),
+                                 (16, 4096), (32, 130)])
+def test_reduce_scatter_bidir_matches_pallas_state_machine(P, c, dtype):
+    N = P * c
+    x = make(P, N, dtype, seed=91 + P + c)
+    bufs = x.to(DEV)
+    out = torch.zeros((P, c), dtype=dtype, device=DEV)
+    rc.ring_reduce_scatter_bidir(bufs, out)
+    ok_status()
+    assert np.array_equal(np_of(out), oracle.reduce_scatter_bidir(np_of(x).copy(), NAME[dtype]))
+
+
+def test_reduce_scatter_bidir_full_bf16():
+    """P=8, 32M bf16 per rank (the gradient-bucket workload)."""
+    x = synthetic.workload("bf16_64mib")
+    xn = np_of(x)
+    out = torch.empty((8, xn.shape[1] // 8), dtype=torch.bfloat16, device=DEV)
+    rc.ring_reduce_scatter_bidir(x.to(DEV), out)
+    ok_status()
+    assert np.array_equal(np_of(out), oracle.reduce_scatter_bidir(xn.copy(), "bf16"))

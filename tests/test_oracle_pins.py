@@ -385,3 +385,87 @@ def test_psum_rank_orders_differ_in_floating_point():
     assert np.all(np.abs(out.astype(np.float64) - exact) <= 8 * 2.0**-24 * np.abs(x).sum(axis=0))
     o5, _, _ = oracle.psum_trace(5)
     assert [_flatten_trace(t) for t in o5] == [[(r - 1 - t) % 5 for t in range(5)] for r in range(5)]
+
+
+# ---------------------------------------------------------------- bidirectional reduce-scatter
+def _parse_trace_cell(t):
+    """'((2:2+1:2)+0:2)' -> (block 2, [2, 1, 0]); '' -> None."""
+    if not t:
+        return None
+    toks = t.replace("(", " ").replace(")", " ").replace("+", " ").split()
+    pairs = [tuple(int(v) for v in tok.split(":")) for tok in toks]
+    blocks = {b for _, b in pairs}
+    assert len(blocks) == 1, t
+    return blocks.pop(), [d for d, _ in pairs]
+
+
+def _parse_table_cell(cell, P=4):
+    """'T2(2+1+0)' -> ('T', 2, [2, 1, 0]); 'T0(all)' -> ('T', 0, None); '-' -> None."""
+    if cell == "-":
+        return None
+    half, rest = cell[0], cell[1:]
+    blk, inner = rest.split("(", 1)
+    inner = inner.rstrip(")")
+    return half, int(blk), None if inner == "all" else [int(v) for v in inner.split("+")]
+
+
+def test_reduce_scatter_bidir_matches_pallas_state_tables_p4():
+    """Every cell of the eight tables of [PALLAS] s4.6 (buffers, accumulator,
+    output).  A swapped direction, an off-by-one block index or a misplaced
+    half changes some cell."""
+    rows = _golden_lines("reduce_scatter_bidir_p4_states.txt")
+    order = ["(0,LEFT)", "(0,RIGHT)", "(1,LEFT)", "(1,RIGHT)", "(2,LEFT)", "(2,RIGHT)", "(3,LEFT)", "(3,RIGHT)"]
+    cache = {}
+    for row in rows:
+        it = order.index(row[0]) + 1
+        d = int(row[1][1:])
+        if it not in cache:
+            cache[it] = oracle.reduce_scatter_bidir_trace(4, it)
+        st = cache[it][d]
+        h0t, h0b, h1t, h1b, acc, ot, ob = st
+        phase_half = "T" if row[0].endswith("LEFT)") else "B"
+        for cell, got in zip(row[2:6], (h0t, h0b, h1t, h1b)):
+            exp = _parse_table_cell(cell)
+            g = _parse_trace_cell(got)
+            if exp is None:
+                assert g is None, (row, cell, got)
+            else:
+                assert g == (exp[1], exp[2]), (row, cell, got)
+        exp = _parse_table_cell(row[6])
+        assert exp[0] == phase_half and _parse_trace_cell(acc) == (exp[1], exp[2]), (row, acc)
+        o_cell = row[7]
+        if o_cell == "-":
+            assert not ot and not ob
+        else:
+            tgot = _parse_trace_cell(ot)
+            assert tgot[0] == d and sorted(tgot[1]) == [0, 1, 2, 3]
+            assert tgot[1] == [(d - t) % 4 for t in range(4)]          # top travelled left
+            if "B" in o_cell:
+                bgot = _parse_trace_cell(ob)
+                assert bgot[0] == d and bgot[1] == [(d + t) % 4 for t in range(4)]  # bottom travelled right
+            else:
+                assert not ob
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8])
+def test_reduce_scatter_bidir_block_sums_exact(P):
+    """o_b = sum over devices of block b ([PALLAS] s4.1), exact in integers, and the
+    closed form: top folds b, b-1, ..., b+1; bottom folds b, b+1, ..., b-1."""
+    g = np.random.default_rng(40 + P)
+    c = 10
+    xi = g.integers(-1000, 1001, size=(P, P * c))
+    out = oracle.reduce_scatter_bidir(xi.astype(np.float32), "f32")
+    for b in range(P):
+        assert np.array_equal(out[b], xi[:, b * c:(b + 1) * c].sum(axis=0).astype(np.float32))
+    xf = g.standard_normal((P, P * c)).astype(np.float32)
+    outf = oracle.reduce_scatter_bidir(xf, "f32")
+    half = c // 2
+    for b in range(P):
+        blk = xf[:, b * c:(b + 1) * c]
+        top = blk[b, :half].copy()
+        for t in range(1, P):
+            top = (top + blk[(b - t) % P, :half]).astype(np.float32)
+        bot = blk[b, half:].copy()
+        for t in range(1, P):
+            bot = (bot + blk[(b + t) % P, half:]).astype(np.float32)
+        assert np.array_equal(outf[b, :half], top) and np.array_equal(outf[b, half:], bot)
