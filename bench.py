@@ -44,7 +44,7 @@ KERNEL_SOURCES = ["ring_collectives_gb300/csrc/ring_kernels.cu", "ring_collectiv
                   "ring_collectives_gb300/csrc/internal.h", "ring_collectives_gb300/csrc/api.cu"]
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -57,7 +57,11 @@ def parse():
     ap.add_argument("--sweep", action="store_true", help="add the weak-scaling sweep (P=2..32) to the line")
     ap.add_argument("--n-per-rank", type=int, default=0,
                     help="override N per rank (a smaller case of the same workload, e.g. for profiling)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def parse_args_for_tests(argv):
+    return parse(argv)
 
 
 def workload_spec(name, P, n_override=0):
@@ -81,6 +85,22 @@ def ring_bytes(P, N, e):
 def min_bytes(P, N, e):
     """Roofline (b): read every input once, write every output once."""
     return 2 * P * N * e
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The slowest replica's time: all-reduce MAX of one float (NCCL tensors
+    on the GPU, gloo tensors on the CPU); identity with one rank."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replicas_value(world: int, bytes_per_replica: float, ms_max: float) -> float:
+    """Whole-job throughput in GB/s: every replica moves bytes_per_replica in
+    at most ms_max milliseconds."""
+    return world * bytes_per_replica / (ms_max * 1e-3) / 1e9
 
 
 def peaks():
@@ -389,11 +409,7 @@ def run_ours(args, spec, rank, world, dist):
     if rc.ring_status(stream) != 0:
         raise RuntimeError(rc.ring_last_error())
     ms = statistics.mean(times)
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, dev)
 
     # end to end through the host entry point: pinned host in -> device -> pinned host out
     h_in = x.pin_memory()
@@ -411,11 +427,7 @@ def run_ours(args, spec, rank, world, dist):
         rc.ring_allreduce_host(h_in, h_out, bufs, stream=stream)
     b.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, dist, dev)
     if rc.ring_status(stream) != 0:
         raise RuntimeError(rc.ring_last_error())
 
@@ -459,7 +471,7 @@ def run_ours(args, spec, rank, world, dist):
     peak, peak_kind = peaks()
     rb = ring_bytes(P, N, e)
     achieved = rb / (ms * 1e-3) / 1e9
-    value = world * rb / (ms_max * 1e-3) / 1e9
+    value = replicas_value(world, rb, ms_max)
     cpu_gbs, cpu_sample, _ = oracle_time(spec, seconds=args.cpu_seconds, frac=1)
     line = {
         "metric": metric_name(spec), "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -474,7 +486,7 @@ def run_ours(args, spec, rank, world, dist):
                      "algorithmic_bytes_per_launch": rb, "kernel": "k_ring (one launch per all-reduce)"},
         "cpu_baseline": {"value": round(cpu_gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": cpu_sample},
-        "e2e": {"value": round(world * rb / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(replicas_value(world, rb, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": P * N * e, "d2h_bytes_per_step": P * N * e,
                 "api": "ring_allreduce_host (pinned host slots in and out)"},
         "gpu_launches": args.steps,
@@ -501,11 +513,7 @@ def run_ag_gemm(args, rank, world, dist):
         dist.barrier()
     with ClockSampler(dev.index) as clocks:
         res = ag_gemm_secondary(rc, dev, stream, args)["ag_gemm_p8_8192x4096x4096"]
-    ms = res["ms"]
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(res["ms"], dist, dev)
     if rank != 0:
         return 0
     flop = res["flop_per_call"]

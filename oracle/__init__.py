@@ -71,6 +71,49 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+class using_library:
+    """Context manager: route every oracle call to another build of the
+    oracle source (used by the mutation tests, which compile copies of
+    ringoracle.c with a planted mistake and check that the pins catch it)."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self.saved = lib()
+        _lib = None
+        alt = ctypes.CDLL(self.path)
+        # reuse the argument declarations of the real library
+        for name in dir(self.saved):
+            if name.startswith("orc_"):
+                f, g = getattr(self.saved, name), getattr(alt, name)
+                g.argtypes, g.restype = f.argtypes, f.restype
+        alt.orc_trace_width.restype = ctypes.c_int
+        _lib = alt
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def build_variant(source_text: str, out_path: str) -> str:
+    """Compile oracle source text (a mutated copy) into out_path."""
+    src = out_path + ".c"
+    with open(src, "w", encoding="utf-8") as f:
+        f.write(source_text)
+    subprocess.run(["gcc", "-std=c11", "-O1", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off", "-w",
+                    "-o", out_path, src], check=True)
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC, encoding="utf-8") as f:
+        return f.read()
+
+
 def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
 
