@@ -202,6 +202,30 @@ int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, const void 
             int P, int rank, int M_r, int N, int K, void *stream);
 
 /*
+ * gemm_rs -- matmul followed by a ring reduce-scatter over output columns.
+ * "TPU 与分布式通信原语", section "collective matmul" (matmul-reduce-scatter:
+ * each rank's partial product is cast to bf16, laid out chunk-major by output
+ * columns and reduce-scattered round the ring), overlapped as in
+ * "Triton-distributed 语义", section "GEMM + ReduceScatter 重叠": here each
+ * output tile's partial products are folded in the GEMM epilogue, so partial
+ * products never reach memory.
+ * A: bf16 [M][K] row-major per rank, slot r at A + r*a_stride (activations).
+ * B: bf16 [N][K] row-major per rank, slot r at B + r*b_stride (row shard of
+ *    the weight, one output feature per row).
+ * out: bf16 [M][N/P] row-major per rank, slot r at out + r*out_stride
+ *    (written): rank r's column chunk, columns [r*N/P, (r+1)*N/P), of
+ *        R = ((C_{r+1} + C_{r+2}) + ...) + C_r,   C_q = bf16(A_q . B_q^T)
+ *    with C_q accumulated in binary32 and rounded once, and "+" the bf16 hop
+ *    add of ring_reduce_scatter -- the ring reduce-scatter of the chunk-major
+ *    partial products.
+ * Requirements (RC_ERR_INVALID otherwise): M % 128 == 0, K % 64 == 0, N a
+ * multiple of 128*P, pointers and strides 16-byte aligned, out not
+ * overlapping A or B.
+ */
+int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_stride, void *out, size_t out_stride,
+            int P, int M, int N, int K, void *stream);
+
+/*
  * ring_status -- waits for `stream`, then returns and clears the device
  * status of the calling device's workspace: RC_OK, or RC_ERR_TIMEOUT when a
  * bounded wait in a kernel ran out (ring_last_error() then names the rank,

@@ -275,6 +275,37 @@ def reduce_scatter_bidir_trace(P: int, iters: int):
     return [[bytes(state[d, k]).split(b"\0", 1)[0].decode() for k in range(7)] for d in range(P)]
 
 
+def gemm_rs(A: np.ndarray, B: np.ndarray, rows=None):
+    """Matmul then ring reduce-scatter ([TPUBOOK] "collective matmul",
+    matmul_reduce_scatter): per rank C_q = bf16(A_q . B_q^T) (binary64 sum,
+    one rounding), laid out chunk-major by output columns (chunk k = columns
+    [k*N/P, (k+1)*N/P)), then the ring reduce-scatter of those P slots.
+    A: bf16 bits [P, M, K]; B: bf16 bits [P, N, K]; rows: optional row
+    subset (rows are independent).  Returns out [P, len(rows), N/P] (bf16),
+    the exact binary64 sums of all partial products [len(rows), N] and the
+    sum over ranks of |C_q| at full precision [len(rows), N] (for bounds)."""
+    A = np.ascontiguousarray(A, dtype=np.uint16)
+    B = np.ascontiguousarray(B, dtype=np.uint16)
+    P, M, K = A.shape
+    N = B.shape[1]
+    rows = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
+    nc = N // P
+    parts = np.empty((P, rows.size, N), dtype=np.uint16)
+    exact = np.zeros((rows.size, N), dtype=np.float64)
+    absc = np.zeros((rows.size, N), dtype=np.float64)
+    absab = np.zeros((rows.size, N), dtype=np.float64)
+    for q in range(P):
+        f64, b16, ab = gemm_bf16_at(A[q], B[q], rows, None)
+        parts[q] = b16
+        exact += f64
+        absc += np.abs(f64)
+        absab += ab
+    # chunk-major slots: slot q = [chunk 0 | chunk 1 | ...], chunk k = parts[q][:, k*nc:(k+1)*nc]
+    slots = np.ascontiguousarray(parts.reshape(P, rows.size, P, nc).transpose(0, 2, 1, 3).reshape(P, -1))
+    out = reduce_scatter(slots, "bf16")
+    return out.reshape(P, rows.size, nc), exact, absc, absab
+
+
 # ---------------------------------------------------------------- trace cells
 def trace_cells(P: int, N: int) -> np.ndarray:
     """[P, N] trace cells, every cell of slot r labelled with the text 'r'."""

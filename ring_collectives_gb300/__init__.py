@@ -24,7 +24,7 @@ import torch
 
 __all__ = [
     "RingError", "ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_allreduce",
-    "ring_allreduce_host", "ring_allreduce_fused", "ring_psum", "ag_gemm", "ring_status", "ring_last_error", "ring_set_timeout_ms",
+    "ring_allreduce_host", "ring_allreduce_fused", "ring_psum", "ag_gemm", "gemm_rs", "ring_status", "ring_last_error", "ring_set_timeout_ms",
     "ring_set_slices", "ring_debug_skip_notify", "ring_finalize", "library_path", "load",
 ]
 
@@ -69,7 +69,7 @@ def load() -> ctypes.CDLL:
         L.ring_debug_skip_notify.argtypes = [i, i]
         L.ring_finalize.argtypes = []
         for name in ("ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_allreduce",
-                     "ring_allreduce_host", "ring_allreduce_fused", "ring_psum", "ag_gemm", "ring_status", "ring_set_timeout_ms", "ring_set_slices",
+                     "ring_allreduce_host", "ring_allreduce_fused", "ring_psum", "ag_gemm", "gemm_rs", "ring_status", "ring_set_timeout_ms", "ring_set_slices",
                      "ring_debug_skip_notify", "ring_finalize"):
             getattr(L, name).restype = i
         _lib = L
@@ -231,6 +231,26 @@ def ag_gemm(a_shards: torch.Tensor, a_gathered: torch.Tensor, B: torch.Tensor, C
         _check(load().ag_gemm(a_shards.data_ptr(), a_shards.stride(0) * 2, a_gathered.data_ptr(), B.data_ptr(),
                               C.data_ptr(), P, rank, M_r, N, K, _stream(stream, a_shards.device)))
     return C
+
+
+def gemm_rs(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """A [P, M, K], B [P, N, K], out [P, M, N/P], all bf16: out[r] = column chunk r
+    of the ring reduce-scatter of the bf16 partial products A[q] . B[q]^T."""
+    fn = load().gemm_rs
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                   ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    for name, t in (("A", A), ("B", B), ("out", out)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous 3-D bf16 CUDA tensor")
+    P, M, K = A.shape
+    N = B.size(1)
+    if B.size(0) != P or B.size(2) != K or tuple(out.shape) != (P, M, N // P):
+        raise ValueError("shapes must be A [P,M,K], B [P,N,K], out [P,M,N/P]")
+    with torch.cuda.device(A.device):
+        _check(fn(A.data_ptr(), A.stride(0) * 2, B.data_ptr(), B.stride(0) * 2, out.data_ptr(), out.stride(0) * 2,
+                  P, M, N, K, _stream(stream, A.device)))
+    return out
 
 
 def ring_status(stream=None, device=None) -> int:

@@ -35,9 +35,7 @@
 
 #include <mutex>
 
-#include "dev.cuh"
-#include "internal.h"
-#include "ringcoll.h"
+#include "tc.cuh"
 
 namespace rc {
 namespace ag {
@@ -64,182 +62,9 @@ struct Params {
     unsigned long long timeout_ns;
 };
 
-// ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(bar), "r"(parity)
-                 : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-                 ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-                 ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// D[tmem] (+)= A[smem desc] . B[smem desc]^T ; accumulate = 0 overwrites D.
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with the
-// 128-byte swizzle: rows of 128 bytes (64 bf16), 8-row groups 1024 bytes
-// apart (stride byte offset), leading byte offset unused for this layout,
-// descriptor version 1 (bits 46-48), swizzle mode 2 = 128B (bits 61-63).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
-{
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);      // start address
-    d |= (uint64_t)(1024u >> 4) << 32;             // stride byte offset
-    d |= (uint64_t)1 << 46;                        // version
-    d |= (uint64_t)2 << 61;                        // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N>>3 at bits
-// 17-22, M>>4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
-{
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-                   "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-                   "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-                   "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-                 : "r"(taddr)
-                 : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi_bits)), "f"(__uint_as_float(lo_bits)));
-    return r;
-}
-
-// ------------------------------------------------------------ bounded waits
-struct Abort {
-    int *flag;          // shared: set once any role of the block gives up
-    WsHeader *hdr;
-    unsigned long long timeout_ns;
-};
-
-__device__ void record_timeout(const Abort &ab, int where)
-{
-    if (atomicCAS(&ab.hdr->status, 0u, (unsigned)RC_ERR_TIMEOUT) == 0u) {
-        ab.hdr->err_rank = 0xA6u;              // marks the all-gather + GEMM kernel
-        ab.hdr->err_step = (uint32_t)where;
-        ab.hdr->err_slice = blockIdx.x;
-    }
-    atomicExch(ab.flag, 1);
-}
-
-// Waits for mbarrier phase `parity`; false if the block aborted (unless
-// `drain`: then only the time bound ends it) or time ran out.
-__device__ bool wait_bar(uint32_t bar, uint32_t parity, const Abort &ab, int where, bool drain = false)
-{
-    uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u) {
-            if (!drain && *(volatile int *)ab.flag) return false;
-            const uint64_t now = global_timer_ns();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > ab.timeout_ns) {
-                record_timeout(ab, where);
-                return false;
-            }
-        }
-    }
-}
-
-__device__ bool wait_flag(const uint32_t *flag, uint32_t E, const Abort &ab, int where)
-{
-    uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        if (epoch_reached(ld_acquire_gpu(flag), E)) return true;
-        if ((it & 15u) == 15u) {
-            if (*(volatile int *)ab.flag) return false;
-            const uint64_t now = global_timer_ns();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > ab.timeout_ns) {
-                record_timeout(ab, where);
-                return false;
-            }
-        }
-        __nanosleep(64);
-    }
-}
+// ------------------------------------------------------------ PTX wrappers (tc.cuh)
+using namespace tc;
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 
 // ------------------------------------------------------------ tile order
 // Tile t of the persistent schedule -> (m block, n block).  Raw M order is
@@ -315,7 +140,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t E = *epoch_slot;
-    const Abort ab{abort_flag, p.hdr, p.timeout_ns};
+    const Abort ab{abort_flag, p.hdr, p.timeout_ns, 0xA6u};
     const int ksteps = p.K / BK;
 
     if (warp == 0 && lane == 0) {

@@ -1,0 +1,322 @@
+// gemm_rs.cu -- matmul followed by a ring reduce-scatter, fused on the
+// 5th-generation tensor cores.
+//
+// Sources: "TPU 与分布式通信原语", section "collective matmul" (matmul-reduce-
+// scatter: every rank multiplies its activations by its row shard of W2,
+// casts the partial product to bf16, lays it out chunk-major by output
+// columns and reduce-scatters it round the ring); "Triton-distributed 语义",
+// section "GEMM + ReduceScatter 重叠" (the GEMM produces output tiles, the
+// reduce-scatter consumes each tile as soon as it exists).
+//
+// On one GPU every rank's partial product of an output tile can be formed
+// where it is consumed, so the reduce-scatter consumer is the GEMM's own
+// epilogue and partial products never reach HBM.  The output tile (m, n)
+// lies in column chunk k = n / (N/P); its value is the ring reduce-scatter's
+//     R = ((C_{k+1} (+) C_{k+2}) (+) ...) (+) C_k,   C_r = bf16(A_r . B_r^T)
+// with (+) the bf16 hop add (binary32 add, rounded to bf16) -- the order in
+// which the ring of the same section folds chunk k.  The MMA warp computes
+// the P partial tiles in that order into two alternating TMEM accumulators;
+// the epilogue rounds each to bf16 and folds it into a register-resident
+// bf16 tile, then writes the finished tile to out_k.
+//
+// One persistent launch, one 256-thread block per SM: warp 0 TMA producer
+// (6-stage ring of 128x64 A and B tiles, 128-byte swizzle), warp 1 MMA issuer
+// (tcgen05.mma.cta_group::1.kind::f16, M=128, N=128, K=16), warp 2 TMEM
+// allocator (256 columns), warps 4-7 epilogue.  Every wait is bounded.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tc.cuh"
+
+namespace rc {
+namespace grs {
+
+using namespace tc;
+
+constexpr int BM = 128, BN = 128, BK = 64, UK = 16;
+constexpr int STAGES = 6;
+constexpr int A_STAGE = BM * BK * 2;   // 16 KiB
+constexpr int B_STAGE = BN * BK * 2;   // 16 KiB
+constexpr int THREADS = 256;
+constexpr int TMEM_COLS = 256;         // two 128x128 fp32 accumulators
+constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+
+struct Params {
+    char *out;
+    size_t out_stride;
+    WsHeader *hdr;
+    int P, M, N, K;          // K: per-rank inner dimension
+    int n_chunk;             // N / P columns per rank
+    int m_tiles, n_tiles, total_tiles;
+    unsigned long long timeout_ns;
+};
+
+// Tile t -> (m block, n block); n-major within an m block keeps a tile row's
+// A operands hot in L2.
+__device__ __forceinline__ void tile_of(const Params &p, int t, int &m, int &n)
+{
+    m = t / p.n_tiles;
+    n = t % p.n_tiles;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_rs(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = sA + STAGES * A_STAGE;
+    uint8_t *bars_g = gbase + STAGES * (A_STAGE + B_STAGE);
+    const uint32_t bars = smem_u32(bars_g);
+    const uint32_t full_bar = bars, empty_bar = bars + 8 * STAGES;
+    const uint32_t tfull_bar = bars + 16 * STAGES, tempty_bar = tfull_bar + 16;
+    const uint32_t drain_bar = tempty_bar + 16;
+    uint32_t *tmem_slot = (uint32_t *)(bars_g + 16 * STAGES + 40);
+    int *abort_flag = (int *)(bars_g + 16 * STAGES + 44);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar + 8 * a, 1);
+            mbar_init(tempty_bar + 8 * a, 4);   // one arrive per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_a) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_b) : "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const Abort ab{abort_flag, p.hdr, p.timeout_ns, 0xA7u};
+    const int ksteps = p.K / BK;
+    const int P = p.P;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer: for every tile, the P partial products in ring order
+        uint32_t stage = 0, phase = 0;
+        int issued[STAGES] = {0, 0, 0, 0, 0, 0};
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            int m, n;
+            tile_of(p, t, m, n);
+            const int k = (n * BN) / p.n_chunk;
+            for (int jj = 1; jj <= P && ok; ++jj) {
+                const int r = (k + jj) % P;               // jj = P is rank k itself, folded last
+                for (int kb = 0; kb < ksteps; ++kb) {
+                    if (!wait_bar(empty_bar + 8 * stage, phase ^ 1u, ab, 2)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full_bar + 8 * stage, A_STAGE + B_STAGE);
+                    tma_load_3d(sA + stage * A_STAGE, &map_a, kb * BK, m * BM, r, full_bar + 8 * stage);
+                    tma_load_3d(sB + stage * B_STAGE, &map_b, kb * BK, n * BN, r, full_bar + 8 * stage);
+                    issued[stage]++;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        if (*(volatile int *)abort_flag) {
+            for (int s = 0; s < STAGES; ++s)
+                if (issued[s] > 0) wait_bar(full_bar + 8 * s, (uint32_t)((issued[s] - 1) & 1), ab, 9, true);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer: one partial product per accumulator
+        uint32_t stage = 0, phase = 0;
+        int it = 0;     // partial products issued so far
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            for (int jj = 1; jj <= P; ++jj, ++it) {
+                const uint32_t acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!wait_bar(tempty_bar + 8 * acc, acc_phase ^ 1u, ab, 3)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * BN;
+                for (int kb = 0; kb < ksteps; ++kb) {
+                    if (!wait_bar(full_bar + 8 * stage, phase, ab, 4)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_sw128(sA + stage * A_STAGE);
+                    const uint64_t bd = smem_desc_sw128(sB + stage * B_STAGE);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UK; ++kk)
+                        tc_mma(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, (kb | kk) != 0);
+                    tc_commit(empty_bar + 8 * stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                tc_commit(tfull_bar + 8 * acc);
+                if (!ok) break;
+            }
+        }
+        tc_commit(drain_bar);
+        wait_bar(drain_bar, 0, ab, 10, true);
+    } else if (warp >= 4) {
+        // ---------------- epilogue: round each partial to bf16 and fold it
+        const int q = warp - 4;          // TMEM lane quadrant = tile rows q*32 .. q*32+31
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            int m, n;
+            tile_of(p, t, m, n);
+            const int k = (n * BN) / p.n_chunk;
+            uint32_t acc[BN / 2];        // the folded tile row: 128 bf16 as 64 packed pairs
+            for (int jj = 1; jj <= P; ++jj, ++it) {
+                const uint32_t buf = it & 1;
+                const uint32_t buf_phase = (it >> 1) & 1;
+                int got = lane == 0 ? (int)wait_bar(tfull_bar + 8 * buf, buf_phase, ab, 6) : 0;
+                got = __shfl_sync(0xFFFFFFFFu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + cc * 32, v);
+#pragma unroll
+                    for (int w = 0; w < 16; ++w) {
+                        const uint32_t c = pack_bf16x2(v[2 * w], v[2 * w + 1]);   // C_r = bf16(partial)
+                        acc[cc * 16 + w] = jj == 1 ? c : add_bf16x2_bits(acc[cc * 16 + w], c);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar + 8 * buf);
+            }
+            if (!ok) break;
+            const size_t row = (size_t)m * BM + q * 32 + lane;
+            const size_t col = (size_t)n * BN - (size_t)k * p.n_chunk;   // column inside chunk k
+            char *dst = p.out + (size_t)k * p.out_stride + (row * (size_t)p.n_chunk + col) * 2;
+#pragma unroll
+            for (int w = 0; w < BN / 8; ++w)
+                st_v4(dst + w * 16, make_uint4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    });
+    return fn;
+}
+
+static int make_map3(CUtensorMap *map, const void *ptr, size_t K, size_t rows, int P, size_t rank_stride)
+{
+    auto fn = encode_fn();
+    if (!fn) return set_error(RC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)P};
+    cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)rank_stride};
+    cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)BM, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(RC_ERR_INVALID, "tensor map encoding failed (CUresult %d)", (int)r);
+    return RC_OK;
+}
+
+static bool overlap(const void *a, size_t an, const void *b, size_t bn)
+{
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+} // namespace grs
+} // namespace rc
+
+extern "C" int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_stride, void *out, size_t out_stride,
+                       int P, int M, int N, int K, void *stream)
+{
+    using namespace rc;
+    using namespace rc::grs;
+    if (P < 1 || P > RC_MAX_P) return set_error(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (M <= 0 || N <= 0 || K <= 0 || M % BM || K % BK || N % P || (N / P) % BN)
+        return set_error(RC_ERR_INVALID, "need M %% %d == 0, K %% %d == 0 and N/P a multiple of %d (got M=%d N=%d K=%d P=%d)",
+                         BM, BK, BN, M, N, K, P);
+    if (!A || !B || !out) return set_error(RC_ERR_INVALID, "null pointer");
+    if (((uintptr_t)A | (uintptr_t)B | (uintptr_t)out | a_stride | b_stride | out_stride) & 15u)
+        return set_error(RC_ERR_INVALID, "pointers and strides must be 16-byte aligned");
+    const size_t a_bytes = (size_t)M * K * 2, b_bytes = (size_t)N * K * 2;
+    const size_t n_chunk = (size_t)N / P, o_bytes = (size_t)M * n_chunk * 2;
+    if (P > 1 && (a_stride < a_bytes || b_stride < b_bytes || out_stride < o_bytes))
+        return set_error(RC_ERR_INVALID, "a stride is below the bytes of a rank's operand");
+    const size_t a_span = (size_t)(P - 1) * a_stride + a_bytes, b_span = (size_t)(P - 1) * b_stride + b_bytes;
+    const size_t o_span = (size_t)(P - 1) * out_stride + o_bytes;
+    if (overlap(out, o_span, A, a_span) || overlap(out, o_span, B, b_span))
+        return set_error(RC_ERR_INVALID, "out overlaps an input");
+
+    Params p{};
+    p.out = (char *)out;
+    p.out_stride = P > 1 ? out_stride : o_bytes;
+    p.P = P;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.n_chunk = (int)n_chunk;
+    p.m_tiles = M / BM;
+    p.n_tiles = N / BN;
+    p.total_tiles = p.m_tiles * p.n_tiles;
+    int sm_count = 0;
+    uint32_t *unused = nullptr;
+    int rc_ = prepare_workspace(0, &p.hdr, &unused, &sm_count, &p.timeout_ns);
+    if (rc_) return rc_;
+    CUtensorMap map_a, map_b;
+    if ((rc_ = make_map3(&map_a, A, (size_t)K, (size_t)M, P, P > 1 ? a_stride : a_bytes))) return rc_;
+    if ((rc_ = make_map3(&map_b, B, (size_t)K, (size_t)N, P, P > 1 ? b_stride : b_bytes))) return rc_;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(k_gemm_rs, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess)
+        return set_error(RC_ERR_CUDA, "shared-memory attribute: %s", cudaGetErrorString(attr_err));
+    int grid = sm_count;
+    if (grid > p.total_tiles) grid = p.total_tiles;
+    k_gemm_rs<<<grid, THREADS, SMEM_BYTES, (cudaStream_t)stream>>>(map_a, map_b, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "gemm_rs launch: %s", cudaGetErrorString(e));
+    return RC_OK;
+}

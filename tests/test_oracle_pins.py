@@ -469,3 +469,24 @@ def test_reduce_scatter_bidir_block_sums_exact(P):
         for t in range(1, P):
             bot = (bot + blk[(b + t) % P, half:]).astype(np.float32)
         assert np.array_equal(outf[b, :half], top) and np.array_equal(outf[b, half:], bot)
+
+
+# ---------------------------------------------------------------- matmul + reduce-scatter
+def test_gemm_rs_oracle_integer_exact_and_p1():
+    """Small integer operands make every partial product and every hop exact
+    in bf16, so out must equal the brute-force column-chunk sums; P = 1 is
+    the plain bf16 matmul."""
+    g = np.random.default_rng(8)
+    P, M, N, K = 4, 6, 8, 5
+    Ai = g.integers(-2, 3, size=(P, M, K))
+    Bi = g.integers(-2, 3, size=(P, N, K))
+    A = oracle.bf16_from_f32(Ai.astype(np.float32))
+    B = oracle.bf16_from_f32(Bi.astype(np.float32))
+    out, exact, _, _ = oracle.gemm_rs(A, B)
+    full = sum(Ai[q] @ Bi[q].T for q in range(P))
+    nc = N // P
+    for r in range(P):
+        assert np.array_equal(oracle.f32_from_bf16(out[r]), full[:, r * nc:(r + 1) * nc].astype(np.float32))
+    assert np.array_equal(exact, full.astype(np.float64))
+    out1, _, _, _ = oracle.gemm_rs(A[:1], B[:1, :2])
+    assert np.array_equal(oracle.f32_from_bf16(out1[0]), (Ai[0] @ Bi[0, :2].T).astype(np.float32))
