@@ -50,7 +50,8 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="f32_64mib", choices=["f32_64mib", "bf16_64mib", "weak", "ag_gemm"])
+    ap.add_argument("--workload", default="f32_64mib",
+                    choices=["f32_64mib", "bf16_64mib", "weak", "ag_gemm", "gemm_rs"])
     ap.add_argument("--P", type=int, default=8)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -359,6 +360,35 @@ def fold_secondary(rc, dev, stream, args):
     return out
 
 
+def gemm_rs_secondary(rc, dev, stream, args):
+    """Matmul + ring reduce-scatter at P=8, A [8192,512] and B [4096,512] per
+    rank (bf16): the mirror of the all-gather + GEMM workload, 275 GFLOP."""
+    P, M, N, K = 8, 8192, 4096, 512
+    a, _ = synthetic.ag_gemm_inputs(P=P, M_r=M, K=K, N=256, seed=11)
+    b, _ = synthetic.ag_gemm_inputs(P=P, M_r=N, K=K, N=256, seed=12)
+    ad, bd = a.to(dev), b.to(dev)
+    out = torch.empty((P, M, N // P), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        rc.gemm_rs(ad, bd, out, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for x, y in ev:
+        x.record(stream)
+        rc.gemm_rs(ad, bd, out, stream=stream)
+        y.record(stream)
+    torch.cuda.synchronize()
+    if rc.ring_status(stream) != 0:
+        raise RuntimeError(rc.ring_last_error())
+    ms = statistics.mean(x.elapsed_time(y) for x, y in ev)
+    flop = 2 * P * M * N * K
+    peak, kind = bf16_peak()
+    tf = flop / (ms * 1e-3) / 1e12
+    return {"gemm_rs_p8_8192x4096x512": {
+        "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peak, 4), "peak": peak,
+        "peak_kind": kind, "flop_per_call": flop,
+        "note": "8 partial products folded in ring order in the epilogue; output [8,8192,512] bf16"}}
+
+
 def weak_sweep(rc, dev, stream, args):
     """Chunk 4M fp32 per rank-step, P in {2,4,8,16,32}: time per ring step."""
     out = {}
@@ -463,6 +493,7 @@ def run_ours(args, spec, rank, world, dist):
     if not args.no_secondary and spec["name"] == "f32_64mib":
         secondary.update(fold_secondary(rc, dev, stream, args))
         secondary.update(ag_gemm_secondary(rc, dev, stream, args))
+        secondary.update(gemm_rs_secondary(rc, dev, stream, args))
     if args.sweep:
         secondary["weak_scaling"] = weak_sweep(rc, dev, stream, args)
 
@@ -512,23 +543,35 @@ def run_ag_gemm(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     with ClockSampler(dev.index) as clocks:
-        res = ag_gemm_secondary(rc, dev, stream, args)["ag_gemm_p8_8192x4096x4096"]
+        if args.workload == "gemm_rs":
+            key, res = next(iter(gemm_rs_secondary(rc, dev, stream, args).items()))
+        else:
+            key, res = next(iter(ag_gemm_secondary(rc, dev, stream, args).items()))
     ms = max_over_ranks(res["ms"], dist, dev)
     if rank != 0:
         return 0
     flop = res["flop_per_call"]
     peak, kind = bf16_peak()
     tf = flop / (res["ms"] * 1e-3) / 1e12
+    if args.workload == "gemm_rs":
+        metric = "gemm_rs TFLOP/s (P=8 partial products A_q.B_q^T + ring reduce-scatter), 8192x4096x512 per rank, bf16"
+        cfg = {"workload": "gemm_rs_p8_m8192_n4096_k512", "P": 8, "replicas": world,
+               "l2": "operands 96 MiB + output 64 MiB"}
+        kern = "k_gemm_rs"
+    else:
+        metric = "ag_gemm TFLOP/s (all-gather of P=8 row shards + C = A_g.B^T), 8192x4096x4096 bf16"
+        cfg = {"workload": "ag_gemm_p8_m1024_k4096_n4096", "P": 8, "rank": 3, "replicas": world,
+               "l2": "operands 96 MiB + outputs 128 MiB, larger than L2"}
+        kern = "k_ag_gemm"
     line = {
-        "metric": "ag_gemm TFLOP/s (all-gather of P=8 row shards + C = A_g.B^T), 8192x4096x4096 bf16",
+        "metric": metric,
         "value": round(world * flop / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "ag_gemm_p8_m1024_k4096_n4096", "P": 8, "rank": 3, "replicas": world,
-                   "l2": "operands 96 MiB + outputs 128 MiB, larger than L2"},
+        "config": cfg,
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(tf / peak, 4), "traffic": None, "peak_kind": kind,
-                     "algorithmic_flop_per_launch": flop, "kernel": "k_ag_gemm"},
+                     "algorithmic_flop_per_launch": flop, "kernel": kern},
         "gpu_launches": args.steps, "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -539,10 +582,10 @@ def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    if args.workload == "ag_gemm":
+    if args.workload in ("ag_gemm", "gemm_rs"):
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the ag_gemm oracle is a sampled check, not a "
-                              "timed baseline; use the default all-reduce workload"}))
+            print(json.dumps({"impl": "reference", "unavailable": "the GEMM oracles are sampled checks, not "
+                              "timed baselines; use the default all-reduce workload"}))
             return 0
         dist = None
         if world > 1:

@@ -219,7 +219,7 @@ int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, const void 
  *    add of ring_reduce_scatter -- the ring reduce-scatter of the chunk-major
  *    partial products.
  * Requirements (RC_ERR_INVALID otherwise): M % 128 == 0, K % 64 == 0, N a
- * multiple of 128*P, pointers and strides 16-byte aligned, out not
+ * multiple of 256*P, pointers and strides 16-byte aligned, out not
  * overlapping A or B.
  */
 int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_stride, void *out, size_t out_stride,

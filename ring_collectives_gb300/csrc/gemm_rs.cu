@@ -20,9 +20,9 @@
 // bf16 tile, then writes the finished tile to out_k.
 //
 // One persistent launch, one 256-thread block per SM: warp 0 TMA producer
-// (6-stage ring of 128x64 A and B tiles, 128-byte swizzle), warp 1 MMA issuer
-// (tcgen05.mma.cta_group::1.kind::f16, M=128, N=128, K=16), warp 2 TMEM
-// allocator (256 columns), warps 4-7 epilogue.  Every wait is bounded.
+// (4-stage ring of 128x64 A and 256x64 B tiles, 128-byte swizzle), warp 1 MMA
+// issuer (tcgen05.mma.cta_group::1.kind::f16, M=128, N=256, K=16), warp 2
+// TMEM allocator (512 columns), warps 4-7 epilogue.  Every wait is bounded.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -34,12 +34,12 @@ namespace grs {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 128, BK = 64, UK = 16;
-constexpr int STAGES = 6;
+constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
+constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;   // 16 KiB
-constexpr int B_STAGE = BN * BK * 2;   // 16 KiB
+constexpr int B_STAGE = BN * BK * 2;   // 32 KiB
 constexpr int THREADS = 256;
-constexpr int TMEM_COLS = 256;         // two 128x128 fp32 accumulators
+constexpr int TMEM_COLS = 512;         // two 128x256 fp32 accumulators
 constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer: for every tile, the P partial products in ring order
         uint32_t stage = 0, phase = 0;
-        int issued[STAGES] = {0, 0, 0, 0, 0, 0};
+        int issued[STAGES] = {0, 0, 0, 0};
         bool ok = true;
         for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
             int m, n;
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int m, n;
             tile_of(p, t, m, n);
             const int k = (n * BN) / p.n_chunk;
-            uint32_t acc[BN / 2];        // the folded tile row: 128 bf16 as 64 packed pairs
+            uint32_t acc[BN / 2];        // the folded tile row: 256 bf16 as 128 packed pairs
             for (int jj = 1; jj <= P; ++jj, ++it) {
                 const uint32_t buf = it & 1;
                 const uint32_t buf_phase = (it >> 1) & 1;
@@ -243,13 +243,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-static int make_map3(CUtensorMap *map, const void *ptr, size_t K, size_t rows, int P, size_t rank_stride)
+static int make_map3(CUtensorMap *map, const void *ptr, size_t K, size_t rows, int P, size_t rank_stride,
+                     uint32_t box_rows)
 {
     auto fn = encode_fn();
     if (!fn) return set_error(RC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)P};
     cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)rank_stride};
-    cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)BM, 1};
+    cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -304,8 +305,8 @@ extern "C" int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_s
     int rc_ = prepare_workspace(0, &p.hdr, &unused, &sm_count, &p.timeout_ns);
     if (rc_) return rc_;
     CUtensorMap map_a, map_b;
-    if ((rc_ = make_map3(&map_a, A, (size_t)K, (size_t)M, P, P > 1 ? a_stride : a_bytes))) return rc_;
-    if ((rc_ = make_map3(&map_b, B, (size_t)K, (size_t)N, P, P > 1 ? b_stride : b_bytes))) return rc_;
+    if ((rc_ = make_map3(&map_a, A, (size_t)K, (size_t)M, P, P > 1 ? a_stride : a_bytes, BM))) return rc_;
+    if ((rc_ = make_map3(&map_b, B, (size_t)K, (size_t)N, P, P > 1 ? b_stride : b_bytes, BN))) return rc_;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {

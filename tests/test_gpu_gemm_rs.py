@@ -61,8 +61,8 @@ def check(P, M, N, K, seed=7, rows=None, min_exact=0.8):
     assert frac >= min_exact, frac
 
 
-@pytest.mark.parametrize("P,M,N,K", [(1, 128, 128, 64), (2, 128, 256, 128), (4, 256, 512, 192), (3, 128, 384, 256),
-                                     (8, 128, 1024, 512)])
+@pytest.mark.parametrize("P,M,N,K", [(1, 128, 256, 64), (2, 128, 512, 128), (4, 256, 1024, 192), (3, 128, 768, 256),
+                                     (8, 128, 2048, 512)])
 def test_gemm_rs_small(P, M, N, K):
     check(P, M, N, K)
 
@@ -80,3 +80,6 @@ def test_gemm_rs_rejects_bad_shapes():
     b = torch.zeros((2, 200, 64), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(rc.RingError):
         rc.gemm_rs(a, b, torch.zeros((2, 128, 100), dtype=torch.bfloat16, device=DEV))
+    b2 = torch.zeros((2, 256, 64), dtype=torch.bfloat16, device=DEV)   # N/P = 128: not a multiple of 256
+    with pytest.raises(rc.RingError):
+        rc.gemm_rs(a, b2, torch.zeros((2, 128, 128), dtype=torch.bfloat16, device=DEV))
