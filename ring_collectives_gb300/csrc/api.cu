@@ -23,11 +23,14 @@ std::atomic<size_t> g_trace_words{0};
 std::mutex g_mu;
 
 constexpr int kMaxDevices = 64;
-// One ring step touches a chunk of every rank; when those P chunks exceed
-// this many bytes the chunks are split into segments run one after another,
-// so the partial sums of a step stay in L2 until the next step reads them
-// (48 MiB measured best on GB300's 126 MB L2).
+// One ring step touches a chunk of every rank.  When those P chunks exceed
+// kL2NoSplitBytes, the chunks are split into segments of at most
+// kDefaultL2LiveBytes run one after another, so the partial sums of a step
+// stay in L2 until the next step reads them.  Both measured on GB300
+// (126 MB L2): up to 64 MiB of live chunks one pass is fastest (each segment
+// adds 2(P-1) signal steps); above it, 48 MiB segments beat 64 and 100 MiB.
 constexpr size_t kDefaultL2LiveBytes = 48ull << 20;
+constexpr size_t kL2NoSplitBytes = 64ull << 20;
 
 // Tuning knob, read once from the environment: RC_L2_LIVE_BYTES (bytes;
 // unset or malformed = the default above; 0 = never segment).
@@ -202,7 +205,8 @@ int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda)
     if (rc_) return rc_;
     {
         const size_t live = (size_t)p.P * p.chunk * es, budget = l2_live_bytes();
-        size_t G = budget ? (live + budget - 1) / budget : 1;
+        const bool split = budget && (live > kL2NoSplitBytes || budget < kDefaultL2LiveBytes);
+        size_t G = split ? (live + budget - 1) / budget : 1;
         const size_t max_g = ring_elems / ((size_t)p.S * rc::kSliceGranule); // keep every slice non-empty
         if (G > max_g) G = max_g;
         if (G > 64) G = 64;
