@@ -144,6 +144,29 @@ int ring_reduce_scatter_bidir(void *bufs_base, size_t bufs_stride, void *out_bas
 int ring_allreduce(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream);
 
 /*
+ * ring_allreduce_ex -- ring_allreduce with a caller-owned signal workspace,
+ * so that calls on different streams can run concurrently (each with its own
+ * workspace) and no library allocation happens.  Arguments, validation and
+ * result as ring_allreduce, plus:
+ *   workspace: DEVICE memory of ws_bytes bytes, 16-byte aligned, owned by the
+ *     caller, zeroed (e.g. cudaMemset 0) once before its first use and not
+ *     modified otherwise.  Calls sharing a workspace must be stream-ordered;
+ *     each call advances the epoch kept in it, so re-zero it (while no call is
+ *     in flight) before about 2^30 calls.
+ *   ws_bytes: at least ring_allreduce_workspace_bytes(P, N, dtype) for the
+ *     current device (RC_ERR_INVALID otherwise).
+ * Device-side timeouts are recorded in the workspace, not read by ring_status.
+ * (The pages' signals live in per-rank signal buffers; this variant lets the
+ * caller place them.)
+ */
+int ring_allreduce_ex(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *workspace, size_t ws_bytes,
+                      void *stream);
+
+/* Bytes of workspace ring_allreduce_ex needs for (P, N, dtype) on the current
+ * device; 0 for invalid arguments or when no sm_103 device is current. */
+size_t ring_allreduce_workspace_bytes(int P, size_t N, int dtype);
+
+/*
  * ring_allreduce_fused -- the ring all-reduce's result in a single pass.
  * Same arguments, validation and result as ring_allreduce, bit for bit:
  * every element of chunk k becomes R[k] = ((x_{k+1} + x_{k+2}) + ...) + x_k,

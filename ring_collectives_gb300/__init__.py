@@ -166,6 +166,31 @@ def ring_allreduce(bufs: torch.Tensor, N: int | None = None, stream=None) -> tor
     return bufs
 
 
+def ring_allreduce_workspace_bytes(P: int, N: int, dtype=torch.float32) -> int:
+    fn = load().ring_allreduce_workspace_bytes
+    fn.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_int]
+    fn.restype = ctypes.c_size_t
+    return int(fn(P, N, _DTYPE[dtype]))
+
+
+def ring_allreduce_ex(bufs: torch.Tensor, workspace: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
+    """ring_allreduce with a caller-owned workspace (a zeroed CUDA byte tensor of
+    at least ring_allreduce_workspace_bytes bytes); calls with distinct
+    workspaces may run concurrently on different streams."""
+    fn = load().ring_allreduce_ex
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                   ctypes.c_size_t, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    bp, bs, dt = _slots(bufs, "bufs")
+    if not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    N = bufs.size(1) if N is None else N
+    with torch.cuda.device(bufs.device):
+        _check(fn(bp, bs, bufs.size(0), N, dt, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                  _stream(stream, bufs.device)))
+    return bufs
+
+
 def ring_allreduce_fused(bufs: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
     """Single-pass all-reduce with the ring's result (bit-identical to ring_allreduce)."""
     fn = load().ring_allreduce_fused

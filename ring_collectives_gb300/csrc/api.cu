@@ -191,12 +191,10 @@ int choose_slices(const DeviceState &st, int dtype, int P, size_t chunk_elems, s
     return RC_OK;
 }
 
-int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda)
+// Chooses slices and segments of a ring launch (the same for every workspace).
+int plan_ring(rc::RingParams &p, int dtype, DeviceState *st)
 {
-    int dev;
-    DeviceState *st = nullptr;
-    int rc_ = current_device(&dev, &st);
-    if (rc_) return rc_;
+    int rc_ = RC_OK;
     const size_t es = elem_size(dtype);
     // The bidirectional reduce-scatter runs two rings (top and bottom halves) per slice.
     const int rings = p.mode == rc::MODE_RS_BIDIR ? 2 : 1;
@@ -213,12 +211,37 @@ int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda)
         if (G < 1) G = 1;
         p.segments = (int)G;
     }
-    const size_t sig_words = (size_t)p.S * p.P * (size_t)p.rows * p.P;
-    std::lock_guard<std::mutex> lock(g_mu);
-    rc_ = ensure_workspace(*st, sig_words * 4);
+    return rc_;
+}
+
+size_t ring_sig_bytes(const rc::RingParams &p) { return (size_t)p.S * p.P * (size_t)p.rows * p.P * 4; }
+
+// Launches a planned ring collective.  ext_ws == nullptr: the device's own
+// workspace; otherwise the caller's (ext_bytes long, zeroed before first use).
+int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda, void *ext_ws = nullptr, size_t ext_bytes = 0)
+{
+    int dev;
+    DeviceState *st = nullptr;
+    int rc_ = current_device(&dev, &st);
     if (rc_) return rc_;
-    p.hdr = (rc::WsHeader *)st->ws;
-    p.sig = (uint32_t *)((char *)st->ws + sizeof(rc::WsHeader));
+    rc_ = plan_ring(p, dtype, st);
+    if (rc_) return rc_;
+    const size_t sig_bytes = ring_sig_bytes(p);
+    std::unique_lock<std::mutex> lock(g_mu, std::defer_lock);
+    if (ext_ws) {
+        if (ext_bytes < sizeof(rc::WsHeader) + sig_bytes)
+            return fail(RC_ERR_INVALID, "workspace of %zu bytes is below the %zu this call needs", ext_bytes,
+                        sizeof(rc::WsHeader) + sig_bytes);
+        if ((uintptr_t)ext_ws & 15u) return fail(RC_ERR_INVALID, "workspace must be 16-byte aligned");
+        p.hdr = (rc::WsHeader *)ext_ws;
+        p.sig = (uint32_t *)((char *)ext_ws + sizeof(rc::WsHeader));
+    } else {
+        lock.lock();
+        rc_ = ensure_workspace(*st, sig_bytes);
+        if (rc_) return rc_;
+        p.hdr = (rc::WsHeader *)st->ws;
+        p.sig = (uint32_t *)((char *)st->ws + sizeof(rc::WsHeader));
+    }
     p.timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
     p.skip_rank = g_skip_rank.exchange(-1);
     p.skip_step = g_skip_step.exchange(-1);
@@ -226,7 +249,7 @@ int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda)
     p.trace_words = g_trace_words.load();
     cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, st_cuda);
     if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
-    st->launches += (uint64_t)p.segments; // the launch advances the epoch by its segment count
+    if (!ext_ws) st->launches += (uint64_t)p.segments; // the launch advances the epoch by its segment count
     return RC_OK;
 }
 
@@ -470,6 +493,52 @@ int ring_allreduce_fused(void *bufs_base, size_t stride, int P, size_t N, int dt
 int ring_psum(void *bufs_base, size_t stride, int P, size_t n, int dtype, void *stream)
 {
     return run_fold(bufs_base, stride, P, n, dtype, 1, stream);
+}
+
+// Validation and parameters shared by ring_allreduce and ring_allreduce_ex.
+static int allreduce_params(void *bufs_base, size_t stride, int P, size_t N, int dtype, rc::RingParams &p)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
+    if (N == 0 || P == 1) return -1; // nothing to do
+    if (!bufs_base) return fail(RC_ERR_INVALID, "null slot base");
+    if (stride < N * es) return fail(RC_ERR_INVALID, "stride %zu below the %zu bytes of a slot", stride, N * es);
+    if (!elem_aligned(bufs_base, stride, es))
+        return fail(RC_ERR_INVALID, "slot base and stride must be multiples of the %zu-byte element", es);
+    p = rc::RingParams{};
+    p.data = (char *)bufs_base;
+    p.data_stride = stride;
+    p.chunk = N / (size_t)P;
+    p.P = P;
+    p.rows = 2 * (P - 1);
+    p.mode = rc::MODE_ALLREDUCE;
+    p.discard = 1;
+    return RC_OK;
+}
+
+size_t ring_allreduce_workspace_bytes(int P, size_t N, int dtype)
+{
+    rc::RingParams p;
+    int v = allreduce_params((void *)(uintptr_t)4096, N * elem_size(dtype), P, N, dtype, p);
+    if (v < 0) return sizeof(rc::WsHeader);
+    if (v) return 0;
+    int dev;
+    DeviceState *st = nullptr;
+    if (current_device(&dev, &st) || plan_ring(p, dtype, st)) return 0;
+    return sizeof(rc::WsHeader) + ring_sig_bytes(p);
+}
+
+int ring_allreduce_ex(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *workspace, size_t ws_bytes,
+                      void *stream)
+{
+    rc::RingParams p;
+    int v = allreduce_params(bufs_base, stride, P, N, dtype, p);
+    if (v < 0) return RC_OK;
+    if (v) return v;
+    if (!workspace) return fail(RC_ERR_INVALID, "null workspace");
+    return run_ring(p, dtype, (cudaStream_t)stream, workspace, ws_bytes);
 }
 
 int ring_allreduce_host(const void *h_in, size_t h_in_stride, void *h_out, size_t h_out_stride, void *d_bufs,

@@ -384,3 +384,53 @@ def test_reduce_scatter_bidir_full_bf16():
     rc.ring_reduce_scatter_bidir(x.to(DEV), out)
     ok_status()
     assert np.array_equal(np_of(out), oracle.reduce_scatter_bidir(xn.copy(), "bf16"))
+
+
+# ------------------------------------------------------------------ caller workspaces, graphs
+def test_allreduce_ex_concurrent_streams_with_own_workspaces():
+    """Two all-reduces on two streams at once, each with its own zeroed
+    workspace, repeated; both bit-exact."""
+    P, c = 8, 64 * 300
+    xs = [make(P, P * c, torch.float32, seed=500 + i) for i in range(2)]
+    want = [oracle.ring_allreduce(np_of(x).copy(), "f32") for x in xs]
+    nb = rc.ring_allreduce_workspace_bytes(P, P * c)
+    assert nb > 128
+    ws = [torch.zeros(nb, dtype=torch.uint8, device=DEV) for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for it in range(3):
+        bufs = [x.to(DEV) for x in xs]
+        torch.cuda.synchronize()
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                rc.ring_allreduce_ex(bufs[i], ws[i])
+        torch.cuda.synchronize()
+        for i in range(2):
+            assert np.array_equal(np_of(bufs[i]), want[i]), (it, i)
+    small = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    with pytest.raises(rc.RingError):
+        rc.ring_allreduce_ex(xs[0].to(DEV), small)
+
+
+def test_allreduce_replayed_from_a_cuda_graph():
+    """The launch epoch lives in device memory, so a captured all-reduce can
+    be replayed: every replay signals with a fresh epoch and stays bit-exact."""
+    P, c = 8, 64 * 200
+    x = make(P, P * c, torch.float32, seed=77)
+    want = oracle.ring_allreduce(np_of(x).copy(), "f32")
+    pristine = x.to(DEV)
+    b = pristine.clone()
+    rc.ring_allreduce(b)                 # creates the workspace before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    b.copy_(pristine)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        rc.ring_allreduce(b)
+    for _ in range(4):
+        b.copy_(pristine)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(np_of(b), want)
+    ok_status()
