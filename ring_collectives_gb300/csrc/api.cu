@@ -45,6 +45,19 @@ size_t l2_live_bytes()
     }();
     return v;
 }
+// Tuning knob, read once from the environment: RC_AG_BULK (1 = all-gather
+// copies with bulk copies through shared memory, 0 = 32-byte vector loads
+// and stores; unset or malformed = the default).
+int ag_bulk_default()
+{
+    static const int v = [] {
+        const char *e = getenv("RC_AG_BULK");
+        if (e && e[0] == '0' && e[1] == 0) return 0;
+        if (e && e[0] == '1' && e[1] == 0) return 1;
+        return 1;
+    }();
+    return v;
+}
 constexpr size_t kMinSliceBytes = 32 << 10; // a slice below this is not worth its own ring
 constexpr uint64_t kEpochResetAt = 1ull << 30; // re-zero the workspace long before 32-bit wrap
 
@@ -211,6 +224,7 @@ int plan_ring(rc::RingParams &p, int dtype, DeviceState *st)
         if (G < 1) G = 1;
         p.segments = (int)G;
     }
+    p.ag_bulk = ag_bulk_default();
     return rc_;
 }
 

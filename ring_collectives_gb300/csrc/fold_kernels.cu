@@ -15,10 +15,16 @@
 //    cost nothing: the block for step t of rank r is slot (r-1-t) mod P, read
 //    from the tile already on chip.
 //
-// A block stages a tile of TE positions of all P slots in shared memory
-// (16-byte vector loads when the rows allow it, evict_first), then computes
-// each output and stores it with coalesced element stores.  Each position
-// is independent, so the kernel is in place.
+// Register form (P <= 8, slots 32-byte aligned): each thread loads the same
+// 32-byte vector of all P slots into registers (coalesced across the warp,
+// evict-first), folds it with P fixed at compile time so every operand index
+// is static, and stores the P results.  The only memory traffic is the P
+// reads and P writes of each position.  Vectors that straddle a chunk
+// boundary and the ragged tail are folded element by element.
+//
+// Shared-memory form (any P or alignment): a block stages a tile of TE
+// positions of all P slots in shared memory, then computes each output and
+// stores it.  Each position is independent, so both forms are in place.
 #include "dev.cuh"
 #include "internal.h"
 #include "ringcoll.h"
@@ -183,10 +189,166 @@ __global__ void __launch_bounds__(kFoldThreads) k_fold(char *data, size_t stride
     }
 }
 
+// ------------------------------------------------------------ register form
+constexpr int kFoldRegThreads = 256;
+
+struct V32 {
+    uint4 a, b;
+};
+
+template <int DT>
+__device__ __forceinline__ V32 add32(const V32 &x, const V32 &y)
+{
+    return V32{hop_add_v4<DT>(x.a, y.a), hop_add_v4<DT>(x.b, y.b)};
+}
+
+// Ring order for chunk K: ((x_{K+1} + x_{K+2}) + ...) + x_K.
+template <int DT, int PC, int K>
+__device__ __forceinline__ V32 ring_fold(const V32 (&x)[PC])
+{
+    V32 acc = x[(K + 1) % PC];
+#pragma unroll
+    for (int jj = 2; jj <= PC; ++jj) acc = add32<DT>(acc, x[(K + jj) % PC]);
+    return acc;
+}
+
+// Runtime chunk index -> the compile-time fold of that chunk.
+template <int DT, int PC, int K = 0>
+__device__ __forceinline__ V32 ring_fold_k(int k, const V32 (&x)[PC])
+{
+    if constexpr (K + 1 < PC) {
+        if (k == K) return ring_fold<DT, PC, K>(x);
+        return ring_fold_k<DT, PC, K + 1>(k, x);
+    } else {
+        return ring_fold<DT, PC, K>(x);
+    }
+}
+
+// Position e of every slot, element by element (chunk-straddling vectors and
+// the tail).
+template <int DT, int ORDER>
+__device__ void fold_elem(char *data, size_t stride, int P, size_t e, size_t chunk)
+{
+    constexpr int ES = DT == 1 ? 2 : 4;
+    auto ld = [&](int r) -> uint32_t {
+        const char *q = data + (size_t)r * stride + e * ES;
+        return ES == 2 ? (uint32_t)ld_cg_u16(q) : ld_cg_u32(q);
+    };
+    if (ORDER == 0) {
+        const int k = (int)(e / chunk);
+        int src = k + 1 == P ? 0 : k + 1;
+        uint32_t acc = ld(src);
+        for (int jj = 2; jj <= P; ++jj) {
+            src = src + 1 == P ? 0 : src + 1;
+            acc = fold_add<DT>(acc, ld(src));
+        }
+        for (int r = 0; r < P; ++r) st_elem<ES>(data + (size_t)r * stride + e * ES, acc);
+    } else {
+        uint32_t out[8];
+        for (int r = 0; r < P; ++r) {
+            int src = r == 0 ? P - 1 : r - 1;
+            uint32_t acc = 0;
+            for (int t = 0; t < P; ++t) {
+                acc = fold_add<DT>(acc, ld(src));
+                src = src == 0 ? P - 1 : src - 1;
+            }
+            out[r] = acc;
+        }
+        for (int r = 0; r < P; ++r) st_elem<ES>(data + (size_t)r * stride + e * ES, out[r]);
+    }
+}
+
+// ORDER 0 = RING, 1 = PSUM; PC = P.  data and stride are 32-byte aligned.
+// Two blocks per SM (<= 128 registers), except the psum order at P >= 7,
+// whose P live outputs need more registers than that.
+template <int ORDER, int PC>
+constexpr int fold_reg_min_blocks() { return (ORDER == 1 && PC >= 7) ? 1 : 2; }
+
+template <int DT, int ORDER, int PC>
+__global__ void __launch_bounds__(kFoldRegThreads, fold_reg_min_blocks<ORDER, PC>()) k_fold_reg(char *data, size_t stride, size_t N, size_t chunk)
+{
+    constexpr int ES = DT == 1 ? 2 : 4;
+    constexpr int VE = 32 / ES;   // elements per 32-byte vector
+    const size_t nvec = N / VE;
+    const size_t step = (size_t)gridDim.x * kFoldRegThreads;
+    for (size_t v = (size_t)blockIdx.x * kFoldRegThreads + threadIdx.x; v < nvec; v += step) {
+        const size_t i = v * VE;
+        const size_t off = i * ES;
+        if (ORDER == 0) {
+            const size_t k = i / chunk;
+            if (i + VE > (k + 1) * chunk) {   // straddles chunks k and k+1
+                for (int q = 0; q < VE; ++q) fold_elem<DT, 0>(data, stride, PC, i + q, chunk);
+                continue;
+            }
+            V32 x[PC];
+#pragma unroll
+            for (int r = 0; r < PC; ++r) ld8_ef(data + (size_t)r * stride + off, x[r].a, x[r].b);
+            const V32 acc = ring_fold_k<DT, PC>((int)k, x);
+#pragma unroll
+            for (int r = 0; r < PC; ++r) st8<kStEvictFirst>(data + (size_t)r * stride + off, acc.a, acc.b);
+        } else {
+            V32 x[PC];
+#pragma unroll
+            for (int r = 0; r < PC; ++r) ld8_ef(data + (size_t)r * stride + off, x[r].a, x[r].b);
+            // rank r: +0, then x_{r-1}, x_{r-2}, ..., x_r
+#pragma unroll
+            for (int r = 0; r < PC; ++r) {
+                V32 acc{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+#pragma unroll
+                for (int t = 0; t < PC; ++t) acc = add32<DT>(acc, x[(r - 1 - t + 2 * PC) % PC]);
+                st8<kStEvictFirst>(data + (size_t)r * stride + off, acc.a, acc.b);
+            }
+        }
+    }
+    // ragged tail: N % VE positions
+    const size_t tail0 = nvec * VE;
+    for (size_t e = tail0 + (size_t)blockIdx.x * kFoldRegThreads + threadIdx.x; e < N; e += step)
+        fold_elem<DT, ORDER>(data, stride, PC, e, chunk);
+}
+
+template <int DT, int ORDER>
+static const void *fold_reg_fn(int P)
+{
+    switch (P) {
+    case 2: return (const void *)k_fold_reg<DT, ORDER, 2>;
+    case 3: return (const void *)k_fold_reg<DT, ORDER, 3>;
+    case 4: return (const void *)k_fold_reg<DT, ORDER, 4>;
+    case 5: return (const void *)k_fold_reg<DT, ORDER, 5>;
+    case 6: return (const void *)k_fold_reg<DT, ORDER, 6>;
+    case 7: return (const void *)k_fold_reg<DT, ORDER, 7>;
+    case 8: return (const void *)k_fold_reg<DT, ORDER, 8>;
+    default: return nullptr;
+    }
+}
+
+static const void *fold_reg_any(int dtype, int order, int P)
+{
+    if (order == 0) return dtype == 0 ? fold_reg_fn<0, 0>(P) : dtype == 1 ? fold_reg_fn<1, 0>(P) : fold_reg_fn<2, 0>(P);
+    return dtype == 0 ? fold_reg_fn<0, 1>(P) : dtype == 1 ? fold_reg_fn<1, 1>(P) : fold_reg_fn<2, 1>(P);
+}
+
 cudaError_t launch_fold(char *data, size_t stride, int P, size_t N, size_t chunk, int dtype, int order, int sm_count,
                         cudaStream_t st)
 {
     const int es = dtype == 1 ? 2 : 4;
+    const void *rf = ((((uintptr_t)data) | stride) & 31u) == 0 ? fold_reg_any(dtype, order, P) : nullptr;
+    if (rf) {
+        // as many 256-thread blocks as fit on the GPU at once (grid-stride loop)
+        static int per_sm[3][2][9] = {};
+        int &occ = per_sm[dtype][order][P];
+        if (occ == 0) {
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rf, kFoldRegThreads, 0);
+            if (e != cudaSuccess) return e;
+            if (occ < 1) occ = 1;
+        }
+        const size_t vecs = N * es / 32 + 1;
+        size_t grid = (size_t)sm_count * occ;
+        const size_t need = (vecs + kFoldRegThreads - 1) / kFoldRegThreads;
+        if (grid > need) grid = need;
+        if (grid < 1) grid = 1;
+        void *args[] = {(void *)&data, (void *)&stride, (void *)&N, (void *)&chunk};
+        return cudaLaunchKernel(rf, dim3((unsigned)grid), dim3(kFoldRegThreads), args, 0, st);
+    }
     int te = kFoldSmem / (P * es);
     te -= te % 64;
     if (te < 64) te = 64;

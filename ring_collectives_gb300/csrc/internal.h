@@ -35,6 +35,7 @@ struct RingParams {
     int P, S, rows, mode;
     int discard;         // 1: drop the L2 lines of reduce-scatter partials once read (their data is dead)
     int segments;        // chunk segments run one after another (keeps a step's live data in L2)
+    int ag_bulk;         // 1: all-gather copies move through shared memory with bulk (TMA) copies
     int skip_rank, skip_step; // test hook: this rank skips its notify after this step (-1: none)
     unsigned long long timeout_ns;
     unsigned long long *trace; // optional step stamps (see ring_debug_set_trace); null: off
@@ -74,5 +75,19 @@ int prepare_workspace(size_t sig_words, WsHeader **hdr, uint32_t **sig, int *sm_
 constexpr int kRingThreads = RC_RING_THREADS;
 // Slices start on multiples of this many elements (keeps 16-byte vectors aligned).
 constexpr size_t kSliceGranule = 64;
+// Bulk-copy staging of the ring's all-gather copies: stages x bytes of
+// shared memory per block (build-time tuning knobs).  Measured on GB300 at
+// P=8 x 64 MiB: 8 x 2 KiB beats 4 x 4 KiB and 2 x 8 KiB by 1-4 %; 24 KiB
+// per block (3 x 8 KiB, 6 x 4 KiB) leaves room for fewer than 8 blocks per
+// SM and is 20 % slower.
+#ifndef RC_AG_STAGES
+#define RC_AG_STAGES 8
+#endif
+#ifndef RC_AG_STAGE_BYTES
+#define RC_AG_STAGE_BYTES 2048
+#endif
+constexpr int kAgStages = RC_AG_STAGES;
+constexpr int kAgStageBytes = RC_AG_STAGE_BYTES;
+static_assert(kAgStageBytes % 16 == 0 && kAgStages >= 2 && kAgStages <= 32, "bulk staging shape");
 
 } // namespace rc

@@ -19,6 +19,10 @@
 // the workspace) and a wait tests "reached the epoch", so rows never need
 // resetting between calls.
 //
+// Data movement: reduce-scatter steps stream 32-byte vectors through
+// registers (two loads, one hop add, one store per vector); all-gather steps
+// move their slice with bulk (TMA) copies staged in shared memory.
+//
 // Why no extra guard against overwriting data a neighbour still reads: rank
 // r reads its left neighbour's chunk (r-s-2) in round s; the left neighbour
 // rewrites that chunk only in all-gather round s (global step P-1+s), and
@@ -27,6 +31,7 @@
 #include "internal.h"
 #include "dev.cuh"
 #include "ringcoll.h"
+#include "tc.cuh"
 
 namespace rc {
 
@@ -202,6 +207,124 @@ __device__ bool wait_row(const uint32_t *flag, uint32_t V, uint32_t E, const Rin
     }
 }
 
+// ------------------------------------------------------------ bulk all-gather copies
+// An all-gather step copies one slice of a chunk from the left neighbour's
+// slot into the own slot.  With p.ag_bulk, thread 0 moves the 16-byte
+// aligned body of that range with bulk (TMA) copies through kAgStages
+// shared-memory buffers: loads (global -> shared, completing on one mbarrier
+// per stage) run up to kAgStages-1 pieces ahead of the stores (shared ->
+// global, bulk groups), while warp 1 copies the unaligned head and tail
+// element-wise.
+struct BulkCtx {
+    uint32_t buf;    // shared address of stage 0
+    uint32_t bar;    // shared address of the mbarrier of stage 0 (8 bytes per stage)
+    uint32_t phase;  // parity bit per stage (thread 0)
+};
+
+// Waits for a stage's load.  A load that has not landed after timeout_ns
+// records RC_ERR_TIMEOUT (the launch then stops at its next step) and is
+// waited for once more, so no copy still targets shared memory when the
+// block exits; false if it failed.
+__device__ bool bulk_bar_wait(uint32_t bar, uint32_t parity, const RingParams &p, int r, int g, int j)
+{
+    uint64_t t0 = 0;
+    bool late = false;
+    for (uint32_t it = 0;; ++it) {
+        if (tc::mbar_try_wait(bar, parity)) return !late;
+        if ((it & 255u) == 255u) {
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > p.timeout_ns) {
+                if (late) return false;
+                if (atomicCAS(&p.hdr->status, 0u, (unsigned)RC_ERR_TIMEOUT) == 0u) {
+                    p.hdr->err_rank = (uint32_t)r;
+                    p.hdr->err_step = (uint32_t)g;
+                    p.hdr->err_slice = (uint32_t)j;
+                }
+                late = true;
+                t0 = now;
+            }
+        }
+    }
+}
+
+// Thread 0: dst[0, bytes) = src[0, bytes), both 16-byte aligned, bytes a
+// multiple of 16.  Runs after this thread's acquire of the step's signal
+// row: the proxy fence orders that acquire before the async-proxy loads
+// and stores.  On return every store has completed and a second proxy fence
+// orders them before the generic-proxy release of the next notify.
+__device__ bool bulk_copy_body(char *dst, const char *src, size_t bytes, BulkCtx &bc, uint64_t pol_src,
+                               uint64_t pol_dst, const RingParams &p, int r, int g, int j)
+{
+    constexpr size_t SB = kAgStageBytes;
+    const size_t np = (bytes + SB - 1) / SB;
+    tc::fence_proxy_async_global();
+    const size_t pre = np < (size_t)kAgStages ? np : (size_t)kAgStages;
+    for (size_t i = 0; i < pre; ++i) {
+        const uint32_t len = (uint32_t)(bytes - i * SB < SB ? bytes - i * SB : SB);
+        tc::mbar_expect_tx(bc.bar + 8u * (uint32_t)i, len);
+        tc::bulk_g2s_hint(bc.buf + (uint32_t)(i * SB), src + i * SB, len, bc.bar + 8u * (uint32_t)i, pol_src);
+    }
+    bool ok = true;
+    for (size_t i = 0; i < np; ++i) {
+        const uint32_t s = (uint32_t)(i % kAgStages);
+        const bool landed = bulk_bar_wait(bc.bar + 8u * s, (bc.phase >> s) & 1u, p, r, g, j);
+        bc.phase ^= 1u << s;
+        if (!landed) ok = false;
+        if (!ok) continue;   // drain the loads already issued; issue nothing more
+        const size_t off = i * SB;
+        const uint32_t len = (uint32_t)(bytes - off < SB ? bytes - off : SB);
+        tc::bulk_s2g_hint(dst + off, bc.buf + s * (uint32_t)SB, len, pol_dst);
+        tc::bulk_commit();
+        const size_t nx = i - 1 + kAgStages;   // next piece for the stage of piece i-1
+        if (i >= 1 && nx < np) {
+            tc::bulk_wait_read1();              // the store of piece i-1 has read its stage
+            const uint32_t t = (uint32_t)(nx % kAgStages);
+            const uint32_t nlen = (uint32_t)(bytes - nx * SB < SB ? bytes - nx * SB : SB);
+            tc::mbar_expect_tx(bc.bar + 8u * t, nlen);
+            tc::bulk_g2s_hint(bc.buf + t * (uint32_t)SB, src + nx * SB, nlen, bc.bar + 8u * t, pol_src);
+        }
+    }
+    tc::bulk_wait_all();
+    tc::fence_proxy_async_global();
+    return ok;
+}
+
+// All threads: dst[0, n) = src[0, n) for an all-gather step.  Without bulk
+// copies (or when dst and src differ in their offset modulo 16) the block
+// streams it with 32-byte vectors; LAST marks the launch's final write of
+// the range (evict-first).
+template <int ES, bool LAST>
+__device__ __forceinline__ void ag_copy(char *dst, const char *src, size_t n, BulkCtx &bc, const RingParams &p,
+                                        int r, int g, int j, int *abort_flag)
+{
+    if (!p.ag_bulk || (((uintptr_t)dst ^ (uintptr_t)src) & 15u) != 0) {
+        copy_range<ES, kRingThreads, LAST ? kStEvictFirst : kStNormal>(dst, src, n);
+        return;
+    }
+    const size_t mis = (uintptr_t)dst & 15u;   // a multiple of ES (slots are element-aligned)
+    size_t head = mis ? (16 - mis) / ES : 0;
+    if (head > n) head = n;
+    const size_t body = ((n - head) * ES) & ~(size_t)15;
+    const size_t done = head + body / ES;
+    if (threadIdx.x == 0) {
+        if (body && !bulk_copy_body(dst + head * ES, src + head * ES, body, bc, tc::policy_evict_first(),
+                                    LAST ? tc::policy_evict_first() : tc::policy_evict_normal(), p, r, g, j))
+            *abort_flag = 1;
+    } else if (threadIdx.x >= 32 && threadIdx.x < 64) {
+        const size_t lane = threadIdx.x - 32;
+        for (size_t i = lane; i < head; i += 32) {
+            if (ES == 2) st_u16(dst + 2 * i, ld_cg_u16(src + 2 * i));
+            else st_u32(dst + 4 * i, ld_cg_u32(src + 4 * i));
+        }
+        for (size_t i = done + lane; i < n; i += 32) {
+            if (ES == 2) st_u16(dst + 2 * i, ld_cg_u16(src + 2 * i));
+            else st_u32(dst + 4 * i, ld_cg_u32(src + 4 * i));
+        }
+    }
+}
+
 // ------------------------------------------------------------ the step engine
 // Segments: when one step's live data (P chunks) would not fit in L2, each
 // slice ring runs all its steps on segment 0 of the chunks, then segment 1,
@@ -242,7 +365,15 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
     __shared__ const uint32_t *s_my_rows;   // [steps][P] signal words of (rank r, slice j, half h)
     __shared__ uint32_t *s_to_rows;         // the same for the block this one notifies
     __shared__ unsigned long long *s_stamp; // step stamps of this block, or null
+    __shared__ __align__(128) unsigned char s_bulk[kAgStages * kAgStageBytes];
+    __shared__ __align__(8) uint64_t s_bulk_bar[kAgStages];
+    BulkCtx bc{tc::smem_u32(s_bulk), tc::smem_u32(s_bulk_bar), 0u};
     if (threadIdx.x == 0) {
+        if (p.ag_bulk) {
+            for (int s = 0; s < kAgStages; ++s) tc::mbar_init(bc.bar + 8u * (uint32_t)s, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
         s_epoch0 = ld_relaxed_gpu(&p.hdr->epoch);
         s_abort = 0;
         s_my_rows = p.sig + (((size_t)j * P + r) * (size_t)p.rows + (size_t)h * nsteps) * P;
@@ -295,9 +426,9 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                 const int k = (r - 1 - g + P) % P;
                 const size_t off = ((size_t)k * c + lo) * ES;
                 if (last)
-                    copy_range<ES, T, kStEvictFirst>(my_slot + off, from_slot + off, n);
+                    ag_copy<ES, true>(my_slot + off, from_slot + off, n, bc, p, r, g, j, &s_abort);
                 else
-                    copy_range<ES, T, kStNormal>(my_slot + off, from_slot + off, n);
+                    ag_copy<ES, false>(my_slot + off, from_slot + off, n, bc, p, r, g, j, &s_abort);
             } else if (BIDIR) {
                 if (g < P - 1) {
                     // partial for chunk k: the upstream neighbour's partial (+) own contribution
@@ -339,12 +470,13 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                 const int k = (r - 1 - t + P) % P;
                 const size_t off = ((size_t)k * c + lo) * ES;
                 if (last)
-                    copy_range<ES, T, kStEvictFirst>(my_slot + off, from_slot + off, n);
+                    ag_copy<ES, true>(my_slot + off, from_slot + off, n, bc, p, r, g, j, &s_abort);
                 else
-                    copy_range<ES, T, kStNormal>(my_slot + off, from_slot + off, n);
+                    ag_copy<ES, false>(my_slot + off, from_slot + off, n, bc, p, r, g, j, &s_abort);
             }
             if (g + 1 < nsteps) {
                 __syncthreads(); // every thread's loads, stores and drops of this step precede the release
+                if (s_abort) break;
                 if (threadIdx.x == 0 && !(r == p.skip_rank && g == p.skip_step))
                     st_release_gpu(&s_to_rows[(size_t)(g + 1) * P + r], V);
             }

@@ -89,3 +89,46 @@ def test_full_size_fused_and_psum():
     rc.ring_psum(b)
     torch.cuda.synchronize()
     assert np.array_equal(npv(b), oracle.psum(x.numpy().copy(), "f32"))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
+@pytest.mark.parametrize("P", [2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("c", [1, 7, 64, 1000, 4096 + 5])
+def test_fold_register_form(P, c, dtype):
+    """Slots on 32-byte boundaries (the register form of both folds, P <= 8),
+    with chunks that are and are not whole 32-byte vectors, so that vectors
+    straddle chunk boundaries and a ragged tail remains."""
+    es = 2 if dtype == torch.bfloat16 else 4
+    N = P * c
+    L = (N + 32 // es - 1) // (32 // es) * (32 // es) + 32 // es   # stride: a multiple of 32 bytes
+    x = make(P, N, dtype, seed=P * 1009 + c)
+    base = torch.zeros((P, L), dtype=dtype, device=DEV)
+    assert base.data_ptr() % 32 == 0
+    base[:, :N] = x.to(DEV)
+    rc.ring_allreduce_fused(base, N=N)
+    torch.cuda.synchronize()
+    assert np.array_equal(npv(base[:, :N]), oracle.ring_allreduce(npv(x).copy(), NAME[dtype]))
+    assert not npv(base[:, N:]).any(), "wrote past N"
+    base[:, :N] = x.to(DEV)
+    rc.ring_psum(base, n=N)
+    torch.cuda.synchronize()
+    assert np.array_equal(npv(base[:, :N]), oracle.psum(npv(x).copy(), NAME[dtype]))
+    assert not npv(base[:, N:]).any(), "wrote past n"
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_fold_register_form_signed_zeros(dtype):
+    """psum starts from +0 (the accumulator is zeroed), so an all -0 position
+    comes out +0; the ring order starts from x_{k+1}, so it stays -0."""
+    P, N = 8, 8 * 64
+    x = torch.full((P, N), -0.0, dtype=dtype)
+    b = x.to(DEV)
+    rc.ring_psum(b)
+    torch.cuda.synchronize()
+    assert np.array_equal(npv(b), oracle.psum(npv(x).copy(), NAME[dtype]))
+    assert not torch.signbit(b.float()).any()
+    b = x.to(DEV)
+    rc.ring_allreduce_fused(b)
+    torch.cuda.synchronize()
+    assert np.array_equal(npv(b), oracle.ring_allreduce(npv(x).copy(), NAME[dtype]))
+    assert torch.signbit(b.float()).all()
