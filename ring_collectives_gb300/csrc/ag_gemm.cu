@@ -33,6 +33,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "tc.cuh"
@@ -58,7 +59,8 @@ struct Params {
     uint32_t *flags;     // one per gather unit
     WsHeader *hdr;
     int P, rank, M_r, N, K;
-    int total_m, tiles_per_pe, n_tiles, total_tiles, units;
+    int total_m, tiles_per_pe, n_tiles, total_tiles, units;  // tile schedule (tile rows: BM, or PM for pairs)
+    int g_total_m, g_per_pe;   // gather schedule, in 128-row blocks (8 units of 16 rows each)
     unsigned long long timeout_ns;
 };
 
@@ -83,9 +85,9 @@ __device__ __forceinline__ void unit_of(const Params &p, int u, int &mb, int &pi
     const int pieces = BM / PIECE_ROWS;
     const int i = u / pieces;
     piece = u % pieces;
-    const int others = p.total_m - p.tiles_per_pe;
-    const int order = i < others ? i + p.tiles_per_pe : i - others;
-    mb = (order + p.rank * p.tiles_per_pe) % p.total_m;
+    const int others = p.g_total_m - p.g_per_pe;
+    const int order = i < others ? i + p.g_per_pe : i - others;
+    mb = (order + p.rank * p.g_per_pe) % p.g_total_m;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -312,6 +314,268 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------ CTA-pair form
+// 256x256 tiles on 2-CTA clusters (the pair scheme of gemm_rs.cu): CTA c
+// stages rows [128c, 128c+128) of the tile's A block and of its B block in
+// K=128 stages (one 32 KiB box per operand half and stage, under the ~70
+// bytes per clock per SM that tiled TMA loads reach on GB300), the even CTA
+// issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and both CTAs drain
+// their own 128 rows of D.  Each CTA waits only on the ready flags of its own
+// 128 A rows; the gather producer runs in every CTA, as in the one-CTA form.
+constexpr int PM = 256, PN = 256, HM = 128, HN = 128;
+constexpr int BK2 = 128;
+constexpr int STAGES2 = 3;
+constexpr int A2_SUB = HM * 64 * 2, B2_SUB = HN * 64 * 2;   // 16 KiB K sub-tiles
+constexpr int A2_STAGE = 2 * A2_SUB, B2_STAGE = 2 * B2_SUB;  // 32 KiB
+constexpr int SMEM2_BYTES = STAGES2 * (A2_STAGE + B2_STAGE) + 2 * STAGING + 1024 + 256;
+constexpr uint32_t kIdesc2 = idesc_bf16_f32(PM, PN);
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    k_ag_gemm2(const __grid_constant__ CUtensorMap map_ag, const __grid_constant__ CUtensorMap map_sh,
+               const __grid_constant__ CUtensorMap map_b, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = sA + STAGES2 * A2_STAGE;
+    const uint32_t sStage = sB + STAGES2 * B2_STAGE;
+    uint8_t *bars_g = gbase + STAGES2 * (A2_STAGE + B2_STAGE) + 2 * STAGING;
+    const uint32_t bars = smem_u32(bars_g);
+    const uint32_t full_bar = bars, empty_bar = bars + 8 * STAGES2;
+    const uint32_t tfull_bar = bars + 16 * STAGES2, tempty_bar = tfull_bar + 16;
+    const uint32_t gat_bar = tempty_bar + 16;
+    const uint32_t drain_bar = gat_bar + 16;
+    uint32_t *tmem_slot = (uint32_t *)(bars_g + 16 * STAGES2 + 56);
+    int *abort_flag = (int *)(bars_g + 16 * STAGES2 + 60);
+    uint32_t *epoch_slot = (uint32_t *)(bars_g + 16 * STAGES2 + 64);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t cta = cluster_ctarank();
+    const bool even = cta == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES2; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar + 8 * a, 1);
+            mbar_init(tempty_bar + 8 * a, 8);   // four epilogue warps of each CTA
+            mbar_init(gat_bar + 8 * a, 1);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        *epoch_slot = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_ag) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_sh) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_b) : "memory");
+    }
+    // Both CTAs are running and their barriers initialised before the
+    // collective TMEM allocation (one warp of each CTA) and any remote arrival.
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t E = *epoch_slot;
+    const uint32_t full_even = mapa_shared(full_bar, 0);
+    const uint32_t tempty_even = mapa_shared(tempty_bar, 0);
+    const Abort ab{abort_flag, p.hdr, p.timeout_ns, 0xA9u, mapa_shared(smem_u32(abort_flag), cta ^ 1u)};
+    const int ksteps = p.K / BK2;
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer (both CTAs): this CTA's halves of A and B
+        uint32_t stage = 0, phase = 0;
+        int issued[STAGES2] = {0, 0, 0};
+        for (int t = pair; t < p.total_tiles && !*(volatile int *)abort_flag; t += npairs) {
+            int m, n;
+            tile_of(p, t, m, n);
+            const int row0 = m * PM + (int)cta * HM;          // this CTA's 128 rows of A_g
+            const int src_rank = row0 / p.M_r;
+            const bool own = src_rank == p.rank;
+            if (!own) {
+                const int mb = row0 / BM;
+                bool ok = true;
+                for (int q = 0; q < BM / PIECE_ROWS && ok; ++q)
+                    ok = wait_flag(&p.flags[mb * (BM / PIECE_ROWS) + q], E, ab, 1);
+                if (!ok) break;
+                fence_proxy_async_global();
+            }
+            const int row_in_shard = row0 % p.M_r;
+            bool ok = true;
+            for (int kb = 0; kb < ksteps; ++kb) {
+                if (!wait_bar(empty_bar + 8 * stage, phase ^ 1u, ab, 2)) {
+                    ok = false;
+                    break;
+                }
+                if (even) mbar_expect_tx(full_bar + 8 * stage, 2 * (A2_STAGE + B2_STAGE));
+                if (own)
+                    tma_load_4d_pair(sA + stage * A2_STAGE, &map_sh, 0, row_in_shard, kb * 2, src_rank,
+                                     full_even + 8 * stage);
+                else
+                    tma_load_3d_pair(sA + stage * A2_STAGE, &map_ag, 0, row0, kb * 2, full_even + 8 * stage);
+                tma_load_3d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * 2,
+                                 full_even + 8 * stage);
+                issued[stage]++;
+                if (++stage == STAGES2) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+        // The even CTA's full barriers count both CTAs' bytes.
+        if (even && *(volatile int *)abort_flag) {
+            for (int s = 0; s < STAGES2; ++s)
+                if (issued[s] > 0) wait_bar(full_bar + 8 * s, (uint32_t)((issued[s] - 1) & 1), ab, 9, true);
+        }
+    } else if (warp == 1 && lane == 0 && even) {
+        // ---------------- MMA issuer (even CTA)
+        uint32_t stage = 0, phase = 0;
+        int it = 0;
+        for (int t = pair; t < p.total_tiles; t += npairs, ++it) {
+            const uint32_t acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            if (!wait_bar<true>(tempty_bar + 8 * acc, acc_phase ^ 1u, ab, 3)) break;
+            tc_fence_after();
+            const uint32_t d = tmem_base + acc * PN;
+            bool ok = true;
+            for (int kb = 0; kb < ksteps; ++kb) {
+                if (!wait_bar(full_bar + 8 * stage, phase, ab, 4)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BK2 / UK; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(sA + stage * A2_STAGE + (kk >> 2) * A2_SUB);
+                    const uint64_t bd = smem_desc_sw128(sB + stage * B2_STAGE + (kk >> 2) * B2_SUB);
+                    tc_mma_pair(d, ad + (uint64_t)(2 * (kk & 3)), bd + (uint64_t)(2 * (kk & 3)), kIdesc2,
+                                (kb | kk) != 0);
+                }
+                tc_commit_pair_mc(empty_bar + 8 * stage, 3);
+                if (++stage == STAGES2) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            tc_commit_pair_mc(tfull_bar + 8 * acc, 3);
+            if (!ok) break;
+        }
+        tc_commit_pair_mc(drain_bar, 1);
+        wait_bar(drain_bar, 0, ab, 10, true);
+    } else if (warp == 2 && lane == 0) {
+        // ---------------- gather producer (every CTA; units spread over the whole grid)
+        const size_t row_bytes = (size_t)p.K * 2;
+        const size_t unit_bytes = (size_t)PIECE_ROWS * row_bytes;
+        uint32_t gphase[2] = {0, 0};
+        uint64_t piece_no = 0;
+        for (int u = blockIdx.x; u < p.units && !*(volatile int *)abort_flag; u += gridDim.x) {
+            int mb, piece;
+            unit_of(p, u, mb, piece);
+            const int row = mb * BM + piece * PIECE_ROWS;
+            const int src_rank = row / p.M_r;
+            const char *src = p.a_shards + (size_t)src_rank * p.a_stride + (size_t)(row % p.M_r) * row_bytes;
+            char *dst = p.a_gathered + (size_t)row * row_bytes;
+            bool ok = true;
+            for (size_t off = 0; off < unit_bytes; off += STAGING, ++piece_no) {
+                const uint32_t bytes = (uint32_t)((unit_bytes - off) < (size_t)STAGING ? (unit_bytes - off) : STAGING);
+                const int b = (int)(piece_no & 1);
+                if (piece_no >= 2) bulk_wait_read1();
+                mbar_expect_tx(gat_bar + 8 * b, bytes);
+                bulk_g2s(sStage + b * STAGING, src + off, bytes, gat_bar + 8 * b);
+                if (!wait_bar(gat_bar + 8 * b, gphase[b], ab, 5)) {
+                    wait_bar(gat_bar + 8 * b, gphase[b], ab, 11, true);
+                    ok = false;
+                    break;
+                }
+                gphase[b] ^= 1u;
+                bulk_s2g(dst + off, sStage + b * STAGING, bytes);
+                bulk_commit();
+            }
+            bulk_wait_all();
+            if (!ok) break;
+            fence_proxy_async_global();
+            st_release_gpu(&p.flags[mb * (BM / PIECE_ROWS) + piece], E);
+        }
+        bulk_wait_all();
+    } else if (warp >= 4) {
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair tile
+        const int q = warp - 4;
+        int it = 0;
+        for (int t = pair; t < p.total_tiles; t += npairs, ++it) {
+            const uint32_t acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            int ok = lane == 0 ? (int)wait_bar(tfull_bar + 8 * acc, acc_phase, ab, 6) : 0;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            int m, n;
+            tile_of(p, t, m, n);
+            const size_t row = (size_t)m * PM + cta * HM + q * 32 + lane;
+            char *crow = p.C + row * (size_t)p.N * 2 + (size_t)n * PN * 2;
+            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + acc * PN;
+            uint32_t va[32], vb[32];
+            tmem_ld32_async(trow, va);
+#pragma unroll
+            for (int cc = 0; cc < PN / 32; cc += 2) {
+                tmem_wait_ld32(va);
+                tmem_ld32_async(trow + (cc + 1) * 32, vb);
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    st_v4(crow + cc * 64 + w * 16,
+                          make_uint4(pack_bf16x2(va[8 * w], va[8 * w + 1]), pack_bf16x2(va[8 * w + 2], va[8 * w + 3]),
+                                     pack_bf16x2(va[8 * w + 4], va[8 * w + 5]),
+                                     pack_bf16x2(va[8 * w + 6], va[8 * w + 7])));
+                tmem_wait_ld32(vb);
+                if (cc + 2 < PN / 32) tmem_ld32_async(trow + (cc + 2) * 32, va);
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    st_v4(crow + (cc + 1) * 64 + w * 16,
+                          make_uint4(pack_bf16x2(vb[8 * w], vb[8 * w + 1]), pack_bf16x2(vb[8 * w + 2], vb[8 * w + 3]),
+                                     pack_bf16x2(vb[8 * w + 4], vb[8 * w + 5]),
+                                     pack_bf16x2(vb[8 * w + 6], vb[8 * w + 7])));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (even)
+                    mbar_arrive(tempty_bar + 8 * acc);
+                else
+                    mbar_arrive_remote(tempty_even + 8 * acc);
+            }
+        }
+    }
+
+    // ---------------- teardown: no MMA of the pair in flight and no TMEM
+    // reader left once both CTAs pass the cluster barrier.
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(&p.hdr->done, 1u);
+        if (prev == gridDim.x - 1) {
+            p.hdr->done = 0;
+            st_relaxed_gpu(&p.hdr->epoch, E);
+        }
+    }
+}
+
 // ------------------------------------------------------------ host side
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -342,6 +606,33 @@ static int make_map(CUtensorMap *map, const void *ptr, int rank, const cuuint64_
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(RC_ERR_INVALID, "tensor map encoding failed (CUresult %d)", (int)r);
     return RC_OK;
+}
+
+// The same over [..][K/64][rows][64] (dims {64, rows, K/64, ...}): a box of two
+// 64-column K blocks of box_rows rows is one request (the CTA-pair stages).
+static int make_map_k2(CUtensorMap *map, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                       uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return set_error(RC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint32_t box[4] = {64, box_rows, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(RC_ERR_INVALID, "tensor map encoding failed (CUresult %d)", (int)r);
+    return RC_OK;
+}
+
+// Tuning knob, read once from the environment: RC_GEMM_PAIRS=0 keeps the
+// one-CTA kernel even where the CTA-pair form applies.
+static bool pair_tiles_enabled()
+{
+    static const bool v = [] {
+        const char *e = getenv("RC_GEMM_PAIRS");
+        return !(e && e[0] == '0' && e[1] == 0);
+    }();
+    return v;
 }
 
 static bool overlap(const void *a, size_t an, const void *b, size_t bn)
@@ -387,48 +678,100 @@ extern "C" int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, 
     p.M_r = M_r;
     p.N = N;
     p.K = K;
-    p.total_m = (int)(M / BM);
-    p.tiles_per_pe = M_r / BM;
-    p.n_tiles = N / BN;
-    p.total_tiles = p.total_m * p.n_tiles;
-    p.units = p.total_m * (BM / PIECE_ROWS);
+    p.g_total_m = (int)(M / BM);
+    p.g_per_pe = M_r / BM;
+    p.units = p.g_total_m * (BM / PIECE_ROWS);
     int sm_count = 0;
     int rc_ = prepare_workspace((size_t)p.units, &p.hdr, &p.flags, &sm_count, &p.timeout_ns);
     if (rc_) return rc_;
+    const bool pairs = M_r % PM == 0 && K % BK2 == 0 && sm_count >= 2 && pair_tiles_enabled();
+    const size_t sh_stride = P > 1 ? a_stride : shard_bytes;
 
     CUtensorMap map_ag, map_sh, map_b;
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-        cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        if ((rc_ = make_map(&map_ag, a_gathered, 2, dims, strides, BM))) return rc_;
-    }
-    {
-        cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)M_r, (cuuint64_t)P};
-        cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)(P > 1 ? a_stride : shard_bytes)};
-        if ((rc_ = make_map(&map_sh, a_shards, 3, dims, strides, BM))) return rc_;
-    }
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
-        cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        if ((rc_ = make_map(&map_b, B, 2, dims, strides, BN))) return rc_;
+    if (pairs) {
+        const cuuint64_t dag[3] = {64, (cuuint64_t)M, (cuuint64_t)K / 64};
+        const cuuint64_t sag[2] = {(cuuint64_t)K * 2, 128};
+        if ((rc_ = make_map_k2(&map_ag, a_gathered, 3, dag, sag, HM))) return rc_;
+        const cuuint64_t dsh[4] = {64, (cuuint64_t)M_r, (cuuint64_t)K / 64, (cuuint64_t)P};
+        const cuuint64_t ssh[3] = {(cuuint64_t)K * 2, 128, (cuuint64_t)sh_stride};
+        if ((rc_ = make_map_k2(&map_sh, a_shards, 4, dsh, ssh, HM))) return rc_;
+        const cuuint64_t db[3] = {64, (cuuint64_t)N, (cuuint64_t)K / 64};
+        const cuuint64_t sb[2] = {(cuuint64_t)K * 2, 128};
+        if ((rc_ = make_map_k2(&map_b, B, 3, db, sb, HN))) return rc_;
+    } else {
+        {
+            cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+            cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+            if ((rc_ = make_map(&map_ag, a_gathered, 2, dims, strides, BM))) return rc_;
+        }
+        {
+            cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)M_r, (cuuint64_t)P};
+            cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)sh_stride};
+            if ((rc_ = make_map(&map_sh, a_shards, 3, dims, strides, BM))) return rc_;
+        }
+        {
+            cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+            cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+            if ((rc_ = make_map(&map_b, B, 2, dims, strides, BN))) return rc_;
+        }
     }
 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         attr_err = cudaFuncSetAttribute(k_ag_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(k_ag_gemm2, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
     });
     if (attr_err != cudaSuccess)
         return set_error(RC_ERR_CUDA, "shared-memory attribute: %s", cudaGetErrorString(attr_err));
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ag_gemm, THREADS, SMEM_BYTES);
-    if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
-    if (per_sm < 1) return set_error(RC_ERR_UNSUPPORTED, "the GEMM block does not fit on an SM");
-    int grid = sm_count * per_sm;
-    if (grid > p.total_tiles) grid = p.total_tiles;
-    void *args[] = {(void *)&map_ag, (void *)&map_sh, (void *)&map_b, (void *)&p};
-    e = cudaLaunchCooperativeKernel((const void *)k_ag_gemm, dim3((unsigned)grid), dim3(THREADS), args,
-                                    (size_t)SMEM_BYTES, (cudaStream_t)stream);
+    cudaError_t e;
+    if (pairs) {
+        p.total_m = (int)(M / PM);
+        p.tiles_per_pe = M_r / PM;
+        p.n_tiles = N / PN;
+        p.total_tiles = p.total_m * p.n_tiles;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = SMEM2_BYTES;
+        cfg.stream = (cudaStream_t)stream;
+        cfg.gridDim = dim3(2);
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, (const void *)k_ag_gemm2, &cfg);
+        if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "cluster occupancy query: %s", cudaGetErrorString(e));
+        if (clusters < 1) return set_error(RC_ERR_UNSUPPORTED, "no CTA pair of the GEMM fits on the GPU");
+        if (clusters > p.total_tiles) clusters = p.total_tiles;
+        cfg.gridDim = dim3(2 * (unsigned)clusters);
+        // Every consumer may wait on ready flags that another CTA's gather
+        // producer sets: ask for co-residency (cooperative launch); the grid is
+        // sized to the clusters that fit at once, so a runtime that refuses the
+        // attribute for clusters still gets every CTA resident.
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, k_ag_gemm2, map_ag, map_sh, map_b, p);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            cfg.numAttrs = 0;
+            e = cudaLaunchKernelEx(&cfg, k_ag_gemm2, map_ag, map_sh, map_b, p);
+        }
+    } else {
+        p.total_m = (int)(M / BM);
+        p.tiles_per_pe = M_r / BM;
+        p.n_tiles = N / BN;
+        p.total_tiles = p.total_m * p.n_tiles;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ag_gemm, THREADS, SMEM_BYTES);
+        if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+        if (per_sm < 1) return set_error(RC_ERR_UNSUPPORTED, "the GEMM block does not fit on an SM");
+        int grid = sm_count * per_sm;
+        if (grid > p.total_tiles) grid = p.total_tiles;
+        void *args[] = {(void *)&map_ag, (void *)&map_sh, (void *)&map_b, (void *)&p};
+        e = cudaLaunchCooperativeKernel((const void *)k_ag_gemm, dim3((unsigned)grid), dim3(THREADS), args,
+                                        (size_t)SMEM_BYTES, (cudaStream_t)stream);
+    }
     if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "ag_gemm launch: %s", cudaGetErrorString(e));
     return RC_OK;
 }

@@ -25,6 +25,7 @@
 // TMEM allocator (512 columns), warps 4-7 epilogue.  Every wait is bounded.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "tc.cuh"
@@ -228,6 +229,238 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
 }
 
+// ------------------------------------------------------------ CTA-pair form
+// The same computation on 256x256 output tiles, each run by a 2-CTA cluster:
+// CTA c of the pair loads rows [128c, 128c+128) of the tile's A block and
+// rows [128c, 128c+128) of its B block, and the even CTA issues
+// tcgen05.mma.cta_group::2 (M=256, N=256, K=16), which reads both CTAs'
+// halves and leaves each CTA's 128 rows of D in its own TMEM.
+// Operand staging is sized to the tile loader (TMA): measured on GB300, one
+// SM's tiled loads top out near 70 bytes per clock, and a request of 16 KiB
+// costs as long as one of 32 KiB.  So a stage is K=128 deep and each operand
+// half arrives as one 32 KiB request (a box of two 64-column K blocks of 128
+// rows): 64 KiB per CTA per 1024 MMA clocks, under that ceiling, where the
+// one-CTA 128x256 tile needs 94 bytes per clock.
+//   even CTA: warp 0 producer (arms the stage's full barrier for the bytes of
+//             both CTAs), warp 1 MMA issuer, warps 4-7 epilogue.
+//   odd CTA:  warp 0 producer (its loads complete on the even CTA's full
+//             barrier), warps 4-7 epilogue (arrive on the even CTA's
+//             accumulator-empty barrier).
+// Both CTAs allocate TMEM together (.cta_group::2) and meet at cluster
+// barriers after set-up and before freeing TMEM.
+constexpr int PM = 256;                 // pair tile rows
+constexpr int PN = 256;                 // pair tile columns
+constexpr int HM = 128, HN = 128;       // per-CTA halves of A rows and B rows
+constexpr int BK2 = 128;                // K per stage: two 64-column swizzled sub-tiles
+constexpr int STAGES2 = 3;
+constexpr int A2_SUB = HM * 64 * 2;     // 16 KiB: one K sub-tile of the A half
+constexpr int B2_SUB = HN * 64 * 2;
+constexpr int A2_STAGE = 2 * A2_SUB;    // 32 KiB
+constexpr int B2_STAGE = 2 * B2_SUB;    // 32 KiB
+constexpr int SMEM2_BYTES = STAGES2 * (A2_STAGE + B2_STAGE) + 1024 + 256;
+constexpr uint32_t kIdesc2 = idesc_bf16_f32(PM, PN);
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    k_gemm_rs2(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = sA + STAGES2 * A2_STAGE;
+    uint8_t *bars_g = gbase + STAGES2 * (A2_STAGE + B2_STAGE);
+    const uint32_t bars = smem_u32(bars_g);
+    const uint32_t full_bar = bars, empty_bar = bars + 8 * STAGES2;
+    const uint32_t tfull_bar = bars + 16 * STAGES2, tempty_bar = tfull_bar + 16;
+    const uint32_t drain_bar = tempty_bar + 16;
+    uint32_t *tmem_slot = (uint32_t *)(bars_g + 16 * STAGES2 + 40);
+    int *abort_flag = (int *)(bars_g + 16 * STAGES2 + 44);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t cta = cluster_ctarank();
+    const bool even = cta == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES2; ++s) {
+            mbar_init(full_bar + 8 * s, 1);      // the even CTA's arm (expect_tx) is its one arrival
+            mbar_init(empty_bar + 8 * s, 1);     // one commit of the pair's MMAs
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar + 8 * a, 1);
+            mbar_init(tempty_bar + 8 * a, 8);    // four epilogue warps of each CTA
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_a) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_b) : "memory");
+    }
+    // Both CTAs are running and their barriers initialised before the
+    // collective TMEM allocation (one warp of each CTA) and any remote arrival.
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t full_even = mapa_shared(full_bar, 0);      // the even CTA's barriers
+    const uint32_t tempty_even = mapa_shared(tempty_bar, 0);
+    const Abort ab{abort_flag, p.hdr, p.timeout_ns, 0xA8u, mapa_shared(smem_u32(abort_flag), cta ^ 1u)};
+    const int ksteps = p.K / BK2;
+    const int P = p.P;
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer (both CTAs)
+        uint32_t stage = 0, phase = 0;
+        int issued[STAGES2] = {0, 0, 0};
+        bool ok = true;
+        for (int t = pair; t < p.total_tiles && ok; t += npairs) {
+            const int m = t / p.n_tiles, n = t % p.n_tiles;
+            const int k = (n * PN) / p.n_chunk;
+            for (int jj = 1; jj <= P && ok; ++jj) {
+                const int r = (k + jj) % P;
+                for (int kb = 0; kb < ksteps; ++kb) {
+                    if (!wait_bar(empty_bar + 8 * stage, phase ^ 1u, ab, 2)) {
+                        ok = false;
+                        break;
+                    }
+                    if (even) mbar_expect_tx(full_bar + 8 * stage, 2 * (A2_STAGE + B2_STAGE));
+                    tma_load_4d_pair(sA + stage * A2_STAGE, &map_a, 0, m * PM + (int)cta * HM, kb * 2, r,
+                                     full_even + 8 * stage);
+                    tma_load_4d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * 2, r,
+                                     full_even + 8 * stage);
+                    issued[stage]++;
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        // The even CTA's full barriers count both CTAs' bytes: once the last
+        // phase armed on each has completed, no load of either CTA is in flight.
+        if (even && *(volatile int *)abort_flag) {
+            for (int s = 0; s < STAGES2; ++s)
+                if (issued[s] > 0) wait_bar(full_bar + 8 * s, (uint32_t)((issued[s] - 1) & 1), ab, 9, true);
+        }
+    } else if (warp == 1 && lane == 0 && even) {
+        // ---------------- MMA issuer (even CTA)
+        uint32_t stage = 0, phase = 0;
+        int it = 0;
+        bool ok = true;
+        for (int t = pair; t < p.total_tiles && ok; t += npairs) {
+            for (int jj = 1; jj <= P; ++jj, ++it) {
+                const uint32_t acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!wait_bar<true>(tempty_bar + 8 * acc, acc_phase ^ 1u, ab, 3)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * PN;
+                for (int kb = 0; kb < ksteps; ++kb) {
+                    if (!wait_bar(full_bar + 8 * stage, phase, ab, 4)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BK2 / UK; ++kk) {
+                        // sub-tile kk/4 of the stage, then 32 bytes per K=16 step inside its swizzled rows
+                        const uint64_t ad = smem_desc_sw128(sA + stage * A2_STAGE + (kk >> 2) * A2_SUB);
+                        const uint64_t bd = smem_desc_sw128(sB + stage * B2_STAGE + (kk >> 2) * B2_SUB);
+                        tc_mma_pair(d, ad + (uint64_t)(2 * (kk & 3)), bd + (uint64_t)(2 * (kk & 3)), kIdesc2,
+                                    (kb | kk) != 0);
+                    }
+                    tc_commit_pair_mc(empty_bar + 8 * stage, 3);   // frees the stage in both CTAs
+                    if (++stage == STAGES2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                tc_commit_pair_mc(tfull_bar + 8 * acc, 3);       // both CTAs' halves of D are ready
+                if (!ok) break;
+            }
+        }
+        tc_commit_pair_mc(drain_bar, 1);
+        wait_bar(drain_bar, 0, ab, 10, true);
+    } else if (warp >= 4) {
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair tile
+        const int q = warp - 4;
+        int it = 0;
+        bool ok = true;
+        for (int t = pair; t < p.total_tiles && ok; t += npairs) {
+            const int m = t / p.n_tiles, n = t % p.n_tiles;
+            const int k = (n * PN) / p.n_chunk;
+            uint32_t acc[PN / 2];
+            for (int jj = 1; jj <= P; ++jj, ++it) {
+                const uint32_t buf = it & 1;
+                const uint32_t buf_phase = (it >> 1) & 1;
+                int got = lane == 0 ? (int)wait_bar(tfull_bar + 8 * buf, buf_phase, ab, 6) : 0;
+                got = __shfl_sync(0xFFFFFFFFu, got, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // Two 32-column loads in flight: the next is issued before this one is folded.
+                const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + buf * PN;
+                uint32_t va[32], vb[32];
+                tmem_ld32_async(trow, va);
+#pragma unroll
+                for (int cc = 0; cc < PN / 32; cc += 2) {
+                    tmem_wait_ld32(va);
+                    tmem_ld32_async(trow + (cc + 1) * 32, vb);
+#pragma unroll
+                    for (int w = 0; w < 16; ++w) {
+                        const uint32_t c = pack_bf16x2(va[2 * w], va[2 * w + 1]);
+                        acc[cc * 16 + w] = jj == 1 ? c : add_bf16x2_bits(acc[cc * 16 + w], c);
+                    }
+                    tmem_wait_ld32(vb);
+                    if (cc + 2 < PN / 32) tmem_ld32_async(trow + (cc + 2) * 32, va);
+#pragma unroll
+                    for (int w = 0; w < 16; ++w) {
+                        const uint32_t c = pack_bf16x2(vb[2 * w], vb[2 * w + 1]);
+                        acc[(cc + 1) * 16 + w] = jj == 1 ? c : add_bf16x2_bits(acc[(cc + 1) * 16 + w], c);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (even)
+                        mbar_arrive(tempty_bar + 8 * buf);
+                    else
+                        mbar_arrive_remote(tempty_even + 8 * buf);
+                }
+            }
+            if (!ok) break;
+            const size_t row = (size_t)m * PM + cta * HM + q * 32 + lane;
+            const size_t col = (size_t)n * PN - (size_t)k * p.n_chunk;
+            char *dst = p.out + (size_t)k * p.out_stride + (row * (size_t)p.n_chunk + col) * 2;
+#pragma unroll
+            for (int w = 0; w < PN / 8; ++w)
+                st_v4(dst + w * 16, make_uint4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]));
+        }
+    }
+
+    // Teardown: no MMA of the pair is in flight (the even CTA drained them) and
+    // no epilogue still reads TMEM once both CTAs pass the cluster barrier.
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -253,6 +486,35 @@ static int make_map3(CUtensorMap *map, const void *ptr, size_t K, size_t rows, i
     cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(RC_ERR_INVALID, "tensor map encoding failed (CUresult %d)", (int)r);
+    return RC_OK;
+}
+
+// Tuning knob, read once from the environment: RC_GEMM_PAIRS=0 keeps the
+// one-CTA kernel even where the CTA-pair form applies (M a multiple of 256).
+static bool pair_tiles_enabled()
+{
+    static const bool v = [] {
+        const char *e = getenv("RC_GEMM_PAIRS");
+        return !(e && e[0] == '0' && e[1] == 0);
+    }();
+    return v;
+}
+
+// The same operand as [P][K/64][rows][64]: a box of two 64-column K blocks of
+// box_rows rows is one request (the CTA-pair kernel's 32 KiB stages).
+static int make_map4(CUtensorMap *map, const void *ptr, size_t K, size_t rows, int P, size_t rank_stride,
+                     uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return set_error(RC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)K / 64, (cuuint64_t)P};
+    cuuint64_t strides[3] = {(cuuint64_t)K * 2, 128, (cuuint64_t)rank_stride};
+    cuuint32_t box[4] = {64, box_rows, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(RC_ERR_INVALID, "tensor map encoding failed (CUresult %d)", (int)r);
@@ -297,26 +559,44 @@ extern "C" int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_s
     p.N = N;
     p.K = K;
     p.n_chunk = (int)n_chunk;
-    p.m_tiles = M / BM;
-    p.n_tiles = N / BN;
-    p.total_tiles = p.m_tiles * p.n_tiles;
     int sm_count = 0;
     uint32_t *unused = nullptr;
     int rc_ = prepare_workspace(0, &p.hdr, &unused, &sm_count, &p.timeout_ns);
     if (rc_) return rc_;
+    const bool pairs = M % PM == 0 && K % BK2 == 0 && sm_count >= 2 && pair_tiles_enabled();
     CUtensorMap map_a, map_b;
-    if ((rc_ = make_map3(&map_a, A, (size_t)K, (size_t)M, P, P > 1 ? a_stride : a_bytes, BM))) return rc_;
-    if ((rc_ = make_map3(&map_b, B, (size_t)K, (size_t)N, P, P > 1 ? b_stride : b_bytes, BN))) return rc_;
+    const size_t ars = P > 1 ? a_stride : a_bytes, brs = P > 1 ? b_stride : b_bytes;
+    if (pairs) {
+        if ((rc_ = make_map4(&map_a, A, (size_t)K, (size_t)M, P, ars, HM))) return rc_;
+        if ((rc_ = make_map4(&map_b, B, (size_t)K, (size_t)N, P, brs, HN))) return rc_;
+    } else {
+        if ((rc_ = make_map3(&map_a, A, (size_t)K, (size_t)M, P, ars, BM))) return rc_;
+        if ((rc_ = make_map3(&map_b, B, (size_t)K, (size_t)N, P, brs, BN))) return rc_;
+    }
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         attr_err = cudaFuncSetAttribute(k_gemm_rs, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(k_gemm_rs2, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
     });
     if (attr_err != cudaSuccess)
         return set_error(RC_ERR_CUDA, "shared-memory attribute: %s", cudaGetErrorString(attr_err));
-    int grid = sm_count;
-    if (grid > p.total_tiles) grid = p.total_tiles;
-    k_gemm_rs<<<grid, THREADS, SMEM_BYTES, (cudaStream_t)stream>>>(map_a, map_b, p);
+    if (pairs) {
+        p.m_tiles = M / PM;
+        p.n_tiles = N / PN;
+        p.total_tiles = p.m_tiles * p.n_tiles;
+        int clusters = sm_count / 2;
+        if (clusters > p.total_tiles) clusters = p.total_tiles;
+        k_gemm_rs2<<<2 * clusters, THREADS, SMEM2_BYTES, (cudaStream_t)stream>>>(map_a, map_b, p);
+    } else {
+        p.m_tiles = M / BM;
+        p.n_tiles = N / BN;
+        p.total_tiles = p.m_tiles * p.n_tiles;
+        int grid = sm_count;
+        if (grid > p.total_tiles) grid = p.total_tiles;
+        k_gemm_rs<<<grid, THREADS, SMEM_BYTES, (cudaStream_t)stream>>>(map_a, map_b, p);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "gemm_rs launch: %s", cudaGetErrorString(e));
     return RC_OK;

@@ -62,9 +62,33 @@ def check(P, M, N, K, seed=7, rows=None, min_exact=0.8):
 
 
 @pytest.mark.parametrize("P,M,N,K", [(1, 128, 256, 64), (2, 128, 512, 128), (4, 256, 1024, 192), (3, 128, 768, 256),
-                                     (8, 128, 2048, 512)])
+                                     (8, 128, 2048, 512), (1, 256, 256, 64), (2, 512, 512, 128), (8, 256, 2048, 512),
+                                     (3, 768, 1536, 384), (3, 768, 1536, 320), (5, 384, 1280, 64), (1, 256, 256, 128),
+                                     (6, 512, 3072, 256)])
 def test_gemm_rs_small(P, M, N, K):
+    """M a multiple of 256 and K of 128 run on CTA pairs (256x256 tiles,
+    K=128 stages); the other shapes on single CTAs (128x256 tiles)."""
     check(P, M, N, K)
+
+
+def test_gemm_rs_pairs_match_single_cta(tmp_path):
+    """The CTA-pair kernel and the one-CTA kernel (RC_GEMM_PAIRS=0, in a child
+    process) agree with the oracle within the same bound on one shape."""
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, %r); import tests.test_gpu_gemm_rs as t, torch; "
+        "import __graft_entry__; __graft_entry__.build(); torch.cuda.set_device(0); "
+        "t.check(4, 512, 2048, 256, seed=21)" % (t_root(),))
+    env = dict(__import__("os").environ, RC_GEMM_PAIRS="0")
+    res = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stdout + res.stderr
+    check(4, 512, 2048, 256, seed=21)
+
+
+def t_root():
+    import os
+    return os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_gemm_rs_full_size_sampled_rows():
