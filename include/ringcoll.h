@@ -198,8 +198,16 @@ int ring_psum(void *bufs_base, size_t stride, int P, size_t n, int dtype, void *
  * of every slot back to h_out (host, may equal h_in).  d_bufs is caller-owned
  * device scratch of P slots (d_stride bytes apart).  Host buffers should be
  * page-locked (cudaHostAlloc / pinned) for the copies to be asynchronous.
- * The copies and the kernel run on `stream`; h_out is valid after the stream
- * completes.  Same validation and result as ring_allreduce.
+ * From 128 MiB of slots on, the work runs in segments of about 64 MiB -- segment q is the
+ * same sub-range of every chunk, so each element keeps its chunk and its
+ * fold order and the result is the same bit for bit -- with the
+ * host-to-device copies on one library-owned stream, the ring launches on
+ * `stream` and the device-to-host copies on a second library-owned stream,
+ * ordered by events, so both copy directions and the kernels overlap.  All
+ * of it is ordered after earlier work on `stream`, and `stream` waits for
+ * all of it: h_out is valid once `stream` completes.  Same validation and
+ * result as ring_allreduce (device slot base and stride must be multiples of
+ * the element size).
  */
 int ring_allreduce_host(const void *h_in, size_t h_in_stride, void *h_out, size_t h_out_stride,
                         void *d_bufs, size_t d_stride, int P, size_t N, int dtype, void *stream);

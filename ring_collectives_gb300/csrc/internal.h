@@ -32,6 +32,8 @@ struct RingParams {
     uint32_t *sig;       // signal rows, [S][P][rows][P] words
     WsHeader *hdr;
     size_t chunk;        // elements per chunk (all-gather: the shard length n)
+    size_t chunk_stride; // elements between the starts of consecutive chunks of a slot (0: = chunk);
+                         // larger when the launch runs one segment of every chunk
     int P, S, rows, mode;
     int discard;         // 1: drop the L2 lines of reduce-scatter partials once read (their data is dead)
     int segments;        // chunk segments run one after another (keeps a step's live data in L2)

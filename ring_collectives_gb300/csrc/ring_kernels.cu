@@ -386,6 +386,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
     const uint32_t E0 = s_epoch0;
     const uint32_t E = E0 + 1u;   // identifies this launch (abort word)
     const size_t c = p.chunk;
+    const size_t cs = p.chunk_stride;   // elements from one chunk's start to the next (>= c)
     const size_t half = c / 2;
     const size_t range_lo = BIDIR ? (h == 0 ? 0 : half) : 0;     // element range of this block's ring
     const size_t range_n = BIDIR ? (h == 0 ? half : c - half) : c;
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
         if (MODE == MODE_ALL_GATHER) {
             // Prologue: the own shard goes to chunk r of the own output slot,
             // then the right neighbour's first row says it may be read.
-            copy_range<ES, T, kStNormal>(my_slot + ((size_t)r * c + lo) * ES, p.in + (size_t)r * p.in_stride + lo * ES,
+            copy_range<ES, T, kStNormal>(my_slot + ((size_t)r * cs + lo) * ES, p.in + (size_t)r * p.in_stride + lo * ES,
                                          n);
             __syncthreads();
             if (threadIdx.x == 0) st_release_gpu(&s_to_rows[r], V);
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
             const bool last = g == nsteps - 1; // nothing reads this step's output again in this launch
             if (MODE == MODE_ALL_GATHER) {
                 const int k = (r - 1 - g + P) % P;
-                const size_t off = ((size_t)k * c + lo) * ES;
+                const size_t off = ((size_t)k * cs + lo) * ES;
                 if (last)
                     ag_copy<ES, true>(my_slot + off, from_slot + off, n, bc, p, r, g, j, &s_abort);
                 else
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                 if (g < P - 1) {
                     // partial for chunk k: the upstream neighbour's partial (+) own contribution
                     const int k = h == 0 ? (r + 1 + g) % P : (r - 1 - g + 2 * P) % P;
-                    const size_t off = ((size_t)k * c + lo) * ES;
+                    const size_t off = ((size_t)k * cs + lo) * ES;
                     // The partial read here is dead afterwards (no one reads or
                     // rewrites it again): its lines are dropped from round 1 on.
                     add_range<DT, T, kStEvictLast>(my_slot + off, from_slot + off, my_slot + off, n,
@@ -441,12 +442,12 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                 } else {
                     // the neighbour's partial for chunk r is complete: deliver it
                     copy_range<ES, T, kStNormal>(p.out + (size_t)r * p.out_stride + lo * ES,
-                                                 from_slot + ((size_t)r * c + lo) * ES, n);
+                                                 from_slot + ((size_t)r * cs + lo) * ES, n);
                 }
             } else if (g < P - 1) {
                 const int s = g;
                 const int k = (r - s - 2 + P) % P; // recv_add_idx == left_send_idx
-                const size_t off = ((size_t)k * c + lo) * ES;
+                const size_t off = ((size_t)k * cs + lo) * ES;
                 char *own = my_slot + off;
                 char *dst = (MODE == MODE_REDUCE_SCATTER && s == P - 2)
                                 ? p.out + (size_t)r * p.out_stride + lo * ES
@@ -468,7 +469,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
             } else {
                 const int t = g - (P - 1);
                 const int k = (r - 1 - t + P) % P;
-                const size_t off = ((size_t)k * c + lo) * ES;
+                const size_t off = ((size_t)k * cs + lo) * ES;
                 if (last)
                     ag_copy<ES, true>(my_slot + off, from_slot + off, n, bc, p, r, g, j, &s_abort);
                 else

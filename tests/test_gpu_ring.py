@@ -243,6 +243,41 @@ def test_host_entry_point_matches_oracle():
     assert np.array_equal(h_out.numpy(), oracle.ring_allreduce(x.numpy().copy(), "f32"))
 
 
+def test_host_pipelined_segments_in_place_ragged():
+    """From 128 MiB of slots on, the host entry point runs in segments (the same
+    sub-range of every chunk, copies and ring launches overlapped on three
+    streams): in place on padded host slots, a chunk length that is not a
+    multiple of the segment count or the slice granule, bf16."""
+    P, c, pad = 4, 8_400_013, 24
+    N = P * c
+    x = make(P, N, torch.bfloat16, seed=23)
+    h = torch.zeros((P, N + pad), dtype=torch.bfloat16).pin_memory()
+    h[:, :N] = x
+    d = torch.empty((P, N + 40), dtype=torch.bfloat16, device=DEV)
+    rc.ring_allreduce_host(h, h, d, N=N)
+    torch.cuda.synchronize()
+    ok_status()
+    want = oracle.ring_allreduce(np_of(x).copy(), "bf16")
+    assert np.array_equal(np_of(h[:, :N]), want)
+    assert not np_of(h[:, N:]).any(), "wrote past N in the host slots"
+
+
+def test_host_pipelined_full_workload():
+    """P=8 x 64 MiB fp32 through pinned host slots (the end-to-end leg of the
+    benchmark): bit-exact with the oracle, twice in a row on one stream."""
+    x = synthetic.workload("f32_64mib")
+    h_in = x.pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    d = torch.empty_like(x, device=DEV)
+    want = oracle.ring_allreduce(x.numpy().copy(), "f32")
+    for _ in range(2):
+        h_out.zero_()
+        rc.ring_allreduce_host(h_in, h_out, d)
+        torch.cuda.synchronize()
+        ok_status()
+        assert np.array_equal(h_out.numpy(), want)
+
+
 # ------------------------------------------------------------------ full-size workloads
 def test_full_f32_64mib_p8_bit_exact():
     """P=8, 16M fp32 per rank ~ N(0,1) seed 1: the benchmark's workload."""
