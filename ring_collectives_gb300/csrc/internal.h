@@ -74,14 +74,23 @@ int prepare_workspace(size_t sig_words, WsHeader **hdr, uint32_t **sig, int *sm_
 #ifndef RC_RING_MIN_BLOCKS
 #define RC_RING_MIN_BLOCKS 8
 #endif
+// 32-byte vector pairs each thread keeps in flight in a reduce-scatter step.
+// Measured on GB300 (P=8 x 64 MiB): 2 pairs at 8 blocks/SM 0.215 ms; 3 pairs
+// 0.220; 4 pairs 0.225; 3-4 pairs at 6 blocks/SM 0.235-0.240; 64-thread
+// blocks at 12-16 per SM 0.235-0.27.
+#ifndef RC_RING_ADD_U
+#define RC_RING_ADD_U 2
+#endif
 constexpr int kRingThreads = RC_RING_THREADS;
 // Slices start on multiples of this many elements (keeps 16-byte vectors aligned).
 constexpr size_t kSliceGranule = 64;
 // Bulk-copy staging of the ring's all-gather copies: stages x bytes of
 // shared memory per block (build-time tuning knobs).  Measured on GB300 at
-// P=8 x 64 MiB: 8 x 2 KiB beats 4 x 4 KiB and 2 x 8 KiB by 1-4 %; 24 KiB
-// per block (3 x 8 KiB, 6 x 4 KiB) leaves room for fewer than 8 blocks per
-// SM and is 20 % slower.
+// P=8 x 64 MiB: 8 x 2 KiB beats 4 x 4 KiB and 2 x 8 KiB by 1-4 % and
+// 4 x 2 KiB by 8 % (the copies are latency-bound on how far loads run
+// ahead); 24 KiB per block (3 x 8 KiB, 6 x 4 KiB) is 20 % slower, and so is
+// any staging depth once the largest shared-memory carveout is requested
+// (0.254 ms): the launch needs the L1 share of the default carveout.
 #ifndef RC_AG_STAGES
 #define RC_AG_STAGES 8
 #endif

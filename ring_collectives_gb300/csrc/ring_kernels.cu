@@ -57,7 +57,7 @@ __device__ __forceinline__ size_t slice_begin(size_t c, int j, int S)
 template <int DT, int T, int POL>
 __device__ __forceinline__ void add_vec32(char *dst, const char *a, const char *b, size_t n32, bool discard)
 {
-    constexpr int U = 2;
+    constexpr int U = RC_RING_ADD_U;
     const size_t lane = threadIdx.x & 31u;
     size_t vw = threadIdx.x - lane; // first vector of this warp
     const bool dline = discard && (((uintptr_t)a & 127u) == 0);
