@@ -1,7 +1,9 @@
 """Benchmark: ring all-reduce on one GB300, P=8 logical ranks, 64 MiB per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload f32_64mib|bf16_64mib|weak] [--P P] [--no-secondary]
+                    [--workload f32_64mib|bf16_64mib|weak|ag_gemm|gemm_rs|fused_f32_64mib|
+                                psum_f32_64mib|reduce_scatter_bf16_64mib|reduce_scatter_bidir_bf16_64mib]
+                    [--P P] [--no-secondary]
 
 One step = one ring all-reduce (reduce-scatter + all-gather, 2(P-1) ring
 steps) over the workload's synthetic inputs, which are resident in HBM when
@@ -42,7 +44,12 @@ from ring_collectives_gb300 import synthetic  # noqa: E402
 
 ES = {"f32": 4, "bf16": 2}
 KERNEL_SOURCES = ["ring_collectives_gb300/csrc/ring_kernels.cu", "ring_collectives_gb300/csrc/dev.cuh",
-                  "ring_collectives_gb300/csrc/internal.h", "ring_collectives_gb300/csrc/api.cu"]
+                  "ring_collectives_gb300/csrc/internal.h", "ring_collectives_gb300/csrc/api.cu",
+                  "ring_collectives_gb300/csrc/tc.cuh"]
+FOLD_SOURCES = ["ring_collectives_gb300/csrc/fold_kernels.cu", "ring_collectives_gb300/csrc/dev.cuh",
+                "ring_collectives_gb300/csrc/internal.h", "ring_collectives_gb300/csrc/api.cu"]
+ROW_WORKLOADS = ("fused_f32_64mib", "psum_f32_64mib", "reduce_scatter_bf16_64mib",
+                 "reduce_scatter_bidir_bf16_64mib")
 
 
 def parse(argv=None):
@@ -52,7 +59,7 @@ def parse(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="f32_64mib",
-                    choices=["f32_64mib", "bf16_64mib", "weak", "ag_gemm", "gemm_rs"])
+                    choices=["f32_64mib", "bf16_64mib", "weak", "ag_gemm", "gemm_rs"] + list(ROW_WORKLOADS))
     ap.add_argument("--P", type=int, default=8)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -115,18 +122,28 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def kernel_hash():
+def _strip_comments(src: str) -> str:
+    """C/C++ source without comments or blank space, so that documentation
+    edits do not count as kernel changes."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
+def kernel_hash(sources=None):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+    for rel in (KERNEL_SOURCES if sources is None else sources):
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per launch of the ring kernel from the committed ncu summary,
-    if it was taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"ring_allreduce_{workload}.md")
+def profiled_traffic(workload, sources=None, prefix="ring_allreduce_"):
+    """DRAM bytes per launch of the timed kernel from the committed ncu
+    summary profiles/<prefix><workload>.md, if it was taken on the current
+    kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{prefix}{workload}.md")
     if not os.path.exists(path):
         return None
     src_hash, traffic = None, None
@@ -139,7 +156,7 @@ def profiled_traffic(workload):
                     traffic = int(ln.split(":", 1)[1].strip())
                 except ValueError:
                     traffic = None
-    return traffic if src_hash == kernel_hash() else None
+    return traffic if src_hash == kernel_hash(sources) else None
 
 
 class ClockSampler:
@@ -591,7 +608,7 @@ def run_ours(args, spec, rank, world, dist):
         "frac_roofline_a": round(achieved / peak, 4),
         "frac_roofline_b": round(min_bytes(P, N, e) / (ms * 1e-3) / 1e9 / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(spec["name"]),
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(spec["name"]) if spec["name"] != "weak" or P == 8 else None,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs, burst copy)",
                      "algorithmic_bytes_per_launch": rb, "kernel": "k_ring (one launch per all-reduce)"},
         "cpu_baseline": {"value": round(cpu_gbs, 3), "unit": "GB/s", "cores": cpu_T, "kind": "oracle",
@@ -637,12 +654,12 @@ def run_ag_gemm(args, rank, world, dist):
         metric = "gemm_rs TFLOP/s (P=8 partial products A_q.B_q^T + ring reduce-scatter), 8192x4096x512 per rank, bf16"
         cfg = {"workload": "gemm_rs_p8_m8192_n4096_k512", "P": 8, "replicas": world,
                "l2": "operands 96 MiB + output 64 MiB"}
-        kern = "k_gemm_rs"
+        kern = "k_gemm_rs2 (CTA pairs)"
     else:
         metric = "ag_gemm TFLOP/s (all-gather of P=8 row shards + C = A_g.B^T), 8192x4096x4096 bf16"
         cfg = {"workload": "ag_gemm_p8_m1024_k4096_n4096", "P": 8, "rank": 3, "replicas": world,
                "l2": "operands 96 MiB + outputs 128 MiB, larger than L2"}
-        kern = "k_ag_gemm"
+        kern = "k_ag_gemm2 (CTA pairs)"
     line = {
         "metric": metric,
         "value": round(world * flop / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "n_gpus": world,
@@ -653,6 +670,100 @@ def run_ag_gemm(args, rank, world, dist):
                      "frac": round(tf / peak, 4), "traffic": None, "peak_kind": kind,
                      "algorithmic_flop_per_launch": flop, "kernel": kern},
         "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_row(args, rank, world, dist):
+    """--workload <row>: one HBM-bound row of the hot path on its own line,
+    timed like the headline (inputs resident, restored by a device copy
+    outside the events), against the row's algorithmic bytes."""
+    import ring_collectives_gb300 as rc
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    name = args.workload
+    if name in ("fused_f32_64mib", "psum_f32_64mib"):
+        x = synthetic.workload("f32_64mib")
+        fn = rc.ring_allreduce_fused if name.startswith("fused") else rc.ring_psum
+        e, dt, out = 4, "f32", None
+    else:
+        x = synthetic.workload("bf16_64mib")
+        fn = rc.ring_reduce_scatter if name == "reduce_scatter_bf16_64mib" else rc.ring_reduce_scatter_bidir
+        e, dt = 2, "bf16"
+    P, N = x.shape
+    pr = x.to(dev)
+    del x
+    bufs = torch.empty_like(pr)
+    if name.startswith("reduce_scatter"):
+        out = torch.empty((P, N // P), dtype=pr.dtype, device=dev)
+        call = lambda: fn(bufs, out, stream=stream)   # noqa: E731
+    else:
+        call = lambda: fn(bufs, stream=stream)        # noqa: E731
+    if name.startswith("fused") or name.startswith("psum"):
+        alg = min_bytes(P, N, e)
+        alg_text = "2*P*N*e (every input read once, every output written once)"
+        kern, sources = "k_fold_reg (register form, P=8)", FOLD_SOURCES
+        metric = (f"{'fused ring-order' if name.startswith('fused') else 'psum'} single-pass all-reduce GB/s "
+                  f"(2*P*N*e / time), P=8, 64 MiB/rank, f32, 1xGB300 per replica")
+    elif name == "reduce_scatter_bf16_64mib":
+        alg = 3 * (P - 1) * N * e
+        alg_text = "3(P-1)*N*e (per rank P-1 steps of 2 chunk reads + 1 chunk write)"
+        kern, sources = "k_ring (reduce-scatter mode)", KERNEL_SOURCES
+        metric = "ring reduce_scatter GB/s (3(P-1)*N*e / time), P=8, 64 MiB/rank, bf16, 1xGB300 per replica"
+    else:
+        alg = (3 * (P - 1) + 2) * N * e
+        alg_text = "(3(P-1)+2)*N*e (P-1 steps of 2 half-chunk reads + 1 write per direction, then a chunk copy)"
+        kern, sources = "k_ring (bidirectional reduce-scatter mode)", KERNEL_SOURCES
+        metric = ("bidirectional reduce_scatter GB/s ((3(P-1)+2)*N*e / time), P=8, 64 MiB/rank, bf16, "
+                  "1xGB300 per replica")
+    for _ in range(args.warmup):
+        bufs.copy_(pr)
+        call()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ev = []
+    with ClockSampler(dev.index) as clocks:
+        for _ in range(args.steps):
+            bufs.copy_(pr)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+    if rc.ring_status(stream) != 0:
+        raise RuntimeError(rc.ring_last_error())
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(times)
+    ms_max = max_over_ranks(ms, dist, dev)
+    if rank != 0:
+        return 0
+    peak, peak_kind = peaks()
+    achieved = alg / (ms * 1e-3) / 1e9
+    # minimum traffic: all-reduces read and write every slot once; reduce-scatters
+    # read every slot once and write one chunk per rank
+    row_min = min_bytes(P, N, e) if name.startswith(("fused", "psum")) else (P + 1) * N * e
+    line = {
+        "metric": metric, "value": round(replicas_value(world, alg, ms_max), 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": name, "P": P, "N_per_rank": N, "bytes_per_rank": N * e, "replicas": world,
+                   "l2": "inputs (P*64 MiB) larger than L2; restored by a device copy before every step, "
+                         "outside the events"},
+        "frac_roofline_b": round(row_min / (ms * 1e-3) / 1e9 / peak, 4),
+        "roofline_b_bytes": row_min,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name, sources, prefix=""),
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs, burst copy)",
+                     "algorithmic_bytes_per_launch": alg, "algorithmic_bytes": alg_text, "kernel": kern},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+        "ms_min": round(min(times), 4), "ms_median": round(statistics.median(times), 4),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -674,6 +785,21 @@ def main():
             dist = dist_mod
         try:
             return run_ag_gemm(args, rank, world, dist)
+        finally:
+            if dist is not None:
+                dist.destroy_process_group()
+    if args.workload in ROW_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the oracle on the "
+                              "default all-reduce workload only"}))
+            return 0
+        dist = None
+        if world > 1:
+            import torch.distributed as dist_mod
+            dist_mod.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))))
+            dist = dist_mod
+        try:
+            return run_row(args, rank, world, dist)
         finally:
             if dist is not None:
                 dist.destroy_process_group()
