@@ -130,6 +130,12 @@ __device__ __forceinline__ void st8(void *p, const uint4 &a, const uint4 &b)
 
 // Drops one 128-byte L2 line without writing it back; the memory behind it is
 // undefined afterwards, so only lines whose data is dead may be discarded.
+// Fetch the 128-byte line at p into L2 (no registers, no completion wait).
+__device__ __forceinline__ void prefetch_l2_line(const void *p)
+{
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void discard_l2_line(const void *p)
 {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");

@@ -81,6 +81,11 @@ int prepare_workspace(size_t sig_words, WsHeader **hdr, uint32_t **sig, int *sm_
 #ifndef RC_RING_ADD_U
 #define RC_RING_ADD_U 2
 #endif
+// Lines of the own input chunk prefetched into L2 while a standalone
+// reduce-scatter round waits for its left neighbour (0: off).
+#ifndef RC_RING_PREFETCH
+#define RC_RING_PREFETCH 32
+#endif
 constexpr int kRingThreads = RC_RING_THREADS;
 // Slices start on multiples of this many elements (keeps 16-byte vectors aligned).
 constexpr size_t kSliceGranule = 64;
