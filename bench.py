@@ -49,7 +49,7 @@ KERNEL_SOURCES = ["ring_collectives_gb300/csrc/ring_kernels.cu", "ring_collectiv
 FOLD_SOURCES = ["ring_collectives_gb300/csrc/fold_kernels.cu", "ring_collectives_gb300/csrc/dev.cuh",
                 "ring_collectives_gb300/csrc/internal.h", "ring_collectives_gb300/csrc/api.cu"]
 ROW_WORKLOADS = ("fused_f32_64mib", "psum_f32_64mib", "reduce_scatter_bf16_64mib",
-                 "reduce_scatter_bidir_bf16_64mib")
+                 "reduce_scatter_bidir_bf16_64mib", "ppermute_f32_64mib", "all_gather_f32_8mib")
 
 
 def parse(argv=None):
@@ -686,42 +686,65 @@ def run_row(args, rank, world, dist):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     name = args.workload
-    if name in ("fused_f32_64mib", "psum_f32_64mib"):
+    restore = True
+    if name in ("fused_f32_64mib", "psum_f32_64mib", "ppermute_f32_64mib"):
         x = synthetic.workload("f32_64mib")
-        fn = rc.ring_allreduce_fused if name.startswith("fused") else rc.ring_psum
-        e, dt, out = 4, "f32", None
+        e, dt = 4, "f32"
+    elif name == "all_gather_f32_8mib":
+        x = synthetic.workload("f32_64mib", N=2 << 20)   # shards of 2M fp32 (8 MiB); outputs 64 MiB per rank
+        e, dt = 4, "f32"
     else:
         x = synthetic.workload("bf16_64mib")
-        fn = rc.ring_reduce_scatter if name == "reduce_scatter_bf16_64mib" else rc.ring_reduce_scatter_bidir
         e, dt = 2, "bf16"
     P, N = x.shape
-    pr = x.to(dev)
+    pr = x.contiguous().to(dev)
     del x
     bufs = torch.empty_like(pr)
-    if name.startswith("reduce_scatter"):
-        out = torch.empty((P, N // P), dtype=pr.dtype, device=dev)
-        call = lambda: fn(bufs, out, stream=stream)   # noqa: E731
-    else:
-        call = lambda: fn(bufs, stream=stream)        # noqa: E731
     if name.startswith("fused") or name.startswith("psum"):
+        fn = rc.ring_allreduce_fused if name.startswith("fused") else rc.ring_psum
+        call = lambda: fn(bufs, stream=stream)        # noqa: E731
         alg = min_bytes(P, N, e)
+        row_min = alg
         alg_text = "2*P*N*e (every input read once, every output written once)"
         kern, sources = "k_fold_reg (register form, P=8)", FOLD_SOURCES
         metric = (f"{'fused ring-order' if name.startswith('fused') else 'psum'} single-pass all-reduce GB/s "
                   f"(2*P*N*e / time), P=8, 64 MiB/rank, f32, 1xGB300 per replica")
-    elif name == "reduce_scatter_bf16_64mib":
-        alg = 3 * (P - 1) * N * e
-        alg_text = "3(P-1)*N*e (per rank P-1 steps of 2 chunk reads + 1 chunk write)"
-        kern, sources = "k_ring (reduce-scatter mode)", KERNEL_SOURCES
-        metric = "ring reduce_scatter GB/s (3(P-1)*N*e / time), P=8, 64 MiB/rank, bf16, 1xGB300 per replica"
+    elif name.startswith("reduce_scatter"):
+        out = torch.empty((P, N // P), dtype=pr.dtype, device=dev)
+        fn = rc.ring_reduce_scatter if name == "reduce_scatter_bf16_64mib" else rc.ring_reduce_scatter_bidir
+        call = lambda: fn(bufs, out, stream=stream)   # noqa: E731
+        row_min = (P + 1) * N * e   # read every slot once, write one chunk per rank
+        if name == "reduce_scatter_bf16_64mib":
+            alg = 3 * (P - 1) * N * e
+            alg_text = "3(P-1)*N*e (per rank P-1 steps of 2 chunk reads + 1 chunk write)"
+            kern = "k_ring (reduce-scatter mode)"
+            metric = "ring reduce_scatter GB/s (3(P-1)*N*e / time), P=8, 64 MiB/rank, bf16, 1xGB300 per replica"
+        else:
+            alg = (3 * (P - 1) + 2) * N * e
+            alg_text = "(3(P-1)+2)*N*e (P-1 steps of 2 half-chunk reads + 1 write per direction, then a chunk copy)"
+            kern = "k_ring (bidirectional reduce-scatter mode)"
+            metric = ("bidirectional reduce_scatter GB/s ((3(P-1)+2)*N*e / time), P=8, 64 MiB/rank, bf16, "
+                      "1xGB300 per replica")
+        sources = KERNEL_SOURCES
+    elif name == "ppermute_f32_64mib":
+        restore = False
+        call = lambda: rc.ring_ppermute_right(pr, bufs, stream=stream)   # noqa: E731
+        alg = row_min = 2 * P * N * e
+        alg_text = "2*P*n*e (every source slot read once, every destination slot written once)"
+        kern, sources = "k_ppermute", KERNEL_SOURCES
+        metric = "ppermute right-shift GB/s (2*P*n*e / time), P=8, 64 MiB/rank, f32, 1xGB300 per replica"
     else:
-        alg = (3 * (P - 1) + 2) * N * e
-        alg_text = "(3(P-1)+2)*N*e (P-1 steps of 2 half-chunk reads + 1 write per direction, then a chunk copy)"
-        kern, sources = "k_ring (bidirectional reduce-scatter mode)", KERNEL_SOURCES
-        metric = ("bidirectional reduce_scatter GB/s ((3(P-1)+2)*N*e / time), P=8, 64 MiB/rank, bf16, "
-                  "1xGB300 per replica")
+        restore = False
+        out = torch.empty((P, P * N), dtype=pr.dtype, device=dev)
+        call = lambda: rc.ring_all_gather(pr, out, stream=stream)   # noqa: E731
+        alg = 2 * P * N * e + 2 * (P - 1) * P * N * e
+        row_min = P * N * e + P * P * N * e
+        alg_text = "2*P*n*e (own shard) + 2(P-1)*P*n*e (P-1 ring steps of a read and a write of n)"
+        kern, sources = "k_ring (all-gather mode)", KERNEL_SOURCES
+        metric = "ring all_gather GB/s (2P*n*e*P / time), P=8, 8 MiB shards, f32, 1xGB300 per replica"
     for _ in range(args.warmup):
-        bufs.copy_(pr)
+        if restore:
+            bufs.copy_(pr)
         call()
     torch.cuda.synchronize()
     if dist is not None:
@@ -729,7 +752,8 @@ def run_row(args, rank, world, dist):
     ev = []
     with ClockSampler(dev.index) as clocks:
         for _ in range(args.steps):
-            bufs.copy_(pr)
+            if restore:
+                bufs.copy_(pr)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -746,16 +770,13 @@ def run_row(args, rank, world, dist):
         return 0
     peak, peak_kind = peaks()
     achieved = alg / (ms * 1e-3) / 1e9
-    # minimum traffic: all-reduces read and write every slot once; reduce-scatters
-    # read every slot once and write one chunk per rank
-    row_min = min_bytes(P, N, e) if name.startswith(("fused", "psum")) else (P + 1) * N * e
     line = {
         "metric": metric, "value": round(replicas_value(world, alg, ms_max), 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
         "config": {"workload": name, "P": P, "N_per_rank": N, "bytes_per_rank": N * e, "replicas": world,
-                   "l2": "inputs (P*64 MiB) larger than L2; restored by a device copy before every step, "
-                         "outside the events"},
+                   "l2": ("inputs larger than L2; in-place inputs restored by a device copy before every "
+                          "step, outside the events")},
         "frac_roofline_b": round(row_min / (ms * 1e-3) / 1e9 / peak, 4),
         "roofline_b_bytes": row_min,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
