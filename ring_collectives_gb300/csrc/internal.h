@@ -86,6 +86,12 @@ int prepare_workspace(size_t sig_words, WsHeader **hdr, uint32_t **sig, int *sm_
 #ifndef RC_RING_PREFETCH
 #define RC_RING_PREFETCH 32
 #endif
+// Blocks per SM of the right-shift copy (256 threads each).  Measured on
+// GB300 (P=8 x 64 MiB fp32): 1 -> 0.187 ms, 2 -> 0.178, 4 -> 0.182,
+// 8 -> 0.167-0.169, 16 -> 0.169-0.170.
+#ifndef RC_PPERMUTE_BLOCKS_PER_SM
+#define RC_PPERMUTE_BLOCKS_PER_SM 8
+#endif
 constexpr int kRingThreads = RC_RING_THREADS;
 // Slices start on multiples of this many elements (keeps 16-byte vectors aligned).
 constexpr size_t kSliceGranule = 64;

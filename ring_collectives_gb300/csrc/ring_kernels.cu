@@ -577,9 +577,9 @@ cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P, size_t n,
                             int esize, int sm_count, cudaStream_t st)
 {
-    // About four blocks per SM in total, at least one per rank.
+    // About RC_PPERMUTE_BLOCKS_PER_SM blocks per SM in total, at least one per rank.
     const size_t bytes = n * (size_t)esize;
-    unsigned bx = (unsigned)((4 * (size_t)sm_count + P - 1) / P);
+    unsigned bx = (unsigned)(((size_t)RC_PPERMUTE_BLOCKS_PER_SM * (size_t)sm_count + P - 1) / P);
     const size_t max_bx = (bytes + 16383) / 16384; // no block below ~16 KiB
     if (bx > max_bx) bx = (unsigned)max_bx;
     if (bx < 1) bx = 1;
