@@ -365,7 +365,10 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
     __shared__ const uint32_t *s_my_rows;   // [steps][P] signal words of (rank r, slice j, half h)
     __shared__ uint32_t *s_to_rows;         // the same for the block this one notifies
     __shared__ unsigned long long *s_stamp; // step stamps of this block, or null
-    __shared__ __align__(128) unsigned char s_bulk[kAgStages * kAgStageBytes];
+    // Bulk-copy staging is dynamic shared memory, present only in launches that
+    // run all-gather steps with bulk copies (ring_dyn_smem): the other modes
+    // leave that space to L1.
+    extern __shared__ __align__(128) unsigned char s_bulk[];
     __shared__ __align__(8) uint64_t s_bulk_bar[kAgStages];
     BulkCtx bc{tc::smem_u32(s_bulk), tc::smem_u32(s_bulk_bar), 0u};
     if (threadIdx.x == 0) {
@@ -550,6 +553,13 @@ static const void *ring_fn(int dtype, int mode)
     }
 }
 
+// Dynamic shared memory of a ring launch: the bulk-copy staging, for modes
+// with all-gather steps when bulk copies are on.
+static size_t ring_dyn_smem(int mode, int ag_bulk)
+{
+    return ag_bulk && (mode == MODE_ALLREDUCE || mode == MODE_ALL_GATHER) ? (size_t)kAgStages * kAgStageBytes : 0;
+}
+
 cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks)
 {
     // every mode instantiation has the same register budget (launch bounds); take the minimum
@@ -558,7 +568,8 @@ cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks)
     if (e != cudaSuccess) return e;
     for (int mode = 0; mode < 4; ++mode) {
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_fn(dtype, mode), threads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_fn(dtype, mode), threads,
+                                                          ring_dyn_smem(mode, 1));
         if (e != cudaSuccess) return e;
         if (per_sm < best) best = per_sm;
     }
@@ -571,7 +582,8 @@ cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_
     RingParams copy = p;
     void *args[] = {(void *)&copy};
     const unsigned blocks = (unsigned)(p.P * p.S) * (p.mode == MODE_RS_BIDIR ? 2u : 1u);
-    return cudaLaunchCooperativeKernel(ring_fn(dtype, p.mode), dim3(blocks), dim3((unsigned)threads), args, 0, st);
+    return cudaLaunchCooperativeKernel(ring_fn(dtype, p.mode), dim3(blocks), dim3((unsigned)threads), args,
+                                       ring_dyn_smem(p.mode, p.ag_bulk), st);
 }
 
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P, size_t n,
