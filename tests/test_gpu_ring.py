@@ -397,6 +397,20 @@ def test_segments_forced_in_a_child_process():
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
 
 
+def test_vector_all_gather_copies_child():
+    """RC_AG_BULK=0 (all-gather steps as 32-byte vector copies instead of bulk
+    copies through shared memory): all-reduce, reduce-scatter and all-gather
+    stay bit-exact."""
+    import os
+    import subprocess
+    import sys
+    from tests.conftest import ROOT
+    env = dict(os.environ, RC_AG_BULK="0")
+    r = subprocess.run([sys.executable, "-c", _SEGMENT_CHILD, ROOT], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
 # ------------------------------------------------------------------ bidirectional reduce-scatter
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
 @pytest.mark.parametrize("P,c", [(1, 100), (2, 2), (2, 7), (3, 1), (4, 256), (4, 2048), (5, 1001), (8, 64 * 33 + 6),
