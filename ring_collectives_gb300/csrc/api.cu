@@ -796,6 +796,8 @@ int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int 
     p.skip_rank = -1;
     p.skip_step = -1;
     p.segments = 1;
+    p.chunk_stride = c;
+    p.ag_bulk = ag_bulk_default();
     cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, s);
     if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
     na.launches++;

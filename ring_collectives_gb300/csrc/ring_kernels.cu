@@ -580,10 +580,11 @@ cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks)
 cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_t st)
 {
     RingParams copy = p;
+    if (copy.chunk_stride == 0) copy.chunk_stride = copy.chunk;   // chunks back to back
     void *args[] = {(void *)&copy};
     const unsigned blocks = (unsigned)(p.P * p.S) * (p.mode == MODE_RS_BIDIR ? 2u : 1u);
     return cudaLaunchCooperativeKernel(ring_fn(dtype, p.mode), dim3(blocks), dim3((unsigned)threads), args,
-                                       ring_dyn_smem(p.mode, p.ag_bulk), st);
+                                       ring_dyn_smem(copy.mode, copy.ag_bulk), st);
 }
 
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P, size_t n,
