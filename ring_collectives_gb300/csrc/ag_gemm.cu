@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
             const uint32_t acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
-            // One lane waits and the warp follows its verdict, so the warp stays
+            // One lane waits and the warp follows its result, so the warp stays
             // converged for the .sync.aligned TMEM loads below.
             int ok = lane == 0 ? (int)wait_bar(tfull_bar + 8 * acc, acc_phase, ab, 6) : 0;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);

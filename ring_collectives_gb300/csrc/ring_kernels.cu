@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                     const int k = h == 0 ? (r + 1 + g) % P : (r - 1 - g + 2 * P) % P;
                     const size_t off = ((size_t)k * cs + lo) * ES;
                     // The partial read here is dead afterwards (no one reads or
-                    // rewrites it again): its lines are dropped from round 1 on.
+                    // rewrites it again): its lines are dropped from step s = 1 on.
                     add_range<DT, T, kStEvictLast>(my_slot + off, from_slot + off, my_slot + off, n,
                                                    p.discard && g >= 1);
                 } else {
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                 char *dst = (MODE == MODE_REDUCE_SCATTER && s == P - 2)
                                 ? p.out + (size_t)r * p.out_stride + lo * ES
                                 : own;
-                // From round 1 on, the left chunk read here is the partial sum the
+                // From reduce-scatter step s = 1 on, the left chunk read here is the partial sum the
                 // left neighbour wrote in round s-1; no one reads it again before
                 // the left neighbour overwrites it (all-gather round s), so its
                 // dirty L2 lines are dropped instead of being written back.  The
