@@ -23,9 +23,11 @@ import os
 import torch
 
 __all__ = [
-    "RingError", "ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_allreduce",
-    "ring_allreduce_host", "ring_allreduce_fused", "ring_psum", "ag_gemm", "gemm_rs", "ring_status", "ring_last_error", "ring_set_timeout_ms",
-    "ring_set_slices", "ring_debug_skip_notify", "ring_finalize", "library_path", "load",
+    "RingError", "ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_reduce_scatter_bidir",
+    "ring_allreduce", "ring_allreduce_ex", "ring_allreduce_workspace_bytes", "ring_allreduce_host",
+    "ring_allreduce_fused", "ring_psum", "ring_allreduce_noalloc", "ag_gemm", "gemm_rs", "ring_status",
+    "ring_last_error", "ring_set_timeout_ms", "ring_set_slices", "ring_debug_skip_notify",
+    "ring_debug_set_trace", "ring_finalize", "library_path", "load",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +35,31 @@ _LIB_PATH = os.path.join(_HERE, "libringcoll.so")
 
 RC_OK, RC_ERR_INVALID, RC_ERR_CUDA, RC_ERR_TIMEOUT, RC_ERR_UNSUPPORTED, RC_ERR_NOMEM = range(6)
 _DTYPE = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
+
+_vp, _sz, _i, _u = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint
+# C signatures of include/ringcoll.h: name -> (argument types, result type)
+_SIGNATURES = {
+    "ring_ppermute_right": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp], _i),
+    "ring_all_gather": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp], _i),
+    "ring_reduce_scatter": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp], _i),
+    "ring_reduce_scatter_bidir": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp], _i),
+    "ring_allreduce": ([_vp, _sz, _i, _sz, _i, _vp], _i),
+    "ring_allreduce_ex": ([_vp, _sz, _i, _sz, _i, _vp, _sz, _vp], _i),
+    "ring_allreduce_workspace_bytes": ([_i, _sz, _i], _sz),
+    "ring_allreduce_host": ([_vp, _sz, _vp, _sz, _vp, _sz, _i, _sz, _i, _vp], _i),
+    "ring_allreduce_fused": ([_vp, _sz, _i, _sz, _i, _vp], _i),
+    "ring_psum": ([_vp, _sz, _i, _sz, _i, _vp], _i),
+    "ring_allreduce_noalloc": ([_vp, _sz, _i, _sz, _i, _vp], _i),
+    "ag_gemm": ([_vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp], _i),
+    "gemm_rs": ([_vp, _sz, _vp, _sz, _vp, _sz, _i, _i, _i, _i, _vp], _i),
+    "ring_status": ([_vp], _i),
+    "ring_last_error": ([], ctypes.c_char_p),
+    "ring_set_timeout_ms": ([_u], _i),
+    "ring_set_slices": ([_i], _i),
+    "ring_debug_skip_notify": ([_i, _i], _i),
+    "ring_debug_set_trace": ([_vp, _sz], _i),
+    "ring_finalize": ([], _i),
+}
 
 _lib = None
 
@@ -54,24 +81,9 @@ def load() -> ctypes.CDLL:
         if not os.path.exists(_LIB_PATH):
             raise RuntimeError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build()")
         L = ctypes.CDLL(_LIB_PATH)
-        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
-        L.ring_ppermute_right.argtypes = [vp, sz, vp, sz, i, sz, i, vp]
-        L.ring_all_gather.argtypes = [vp, sz, vp, sz, i, sz, i, vp]
-        L.ring_reduce_scatter.argtypes = [vp, sz, vp, sz, i, sz, i, vp]
-        L.ring_allreduce.argtypes = [vp, sz, i, sz, i, vp]
-        L.ring_allreduce_host.argtypes = [vp, sz, vp, sz, vp, sz, i, sz, i, vp]
-        L.ag_gemm.argtypes = [vp, sz, vp, vp, vp, i, i, i, i, i, vp]
-        L.ring_status.argtypes = [vp]
-        L.ring_last_error.argtypes = []
-        L.ring_last_error.restype = ctypes.c_char_p
-        L.ring_set_timeout_ms.argtypes = [ctypes.c_uint]
-        L.ring_set_slices.argtypes = [i]
-        L.ring_debug_skip_notify.argtypes = [i, i]
-        L.ring_finalize.argtypes = []
-        for name in ("ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_allreduce",
-                     "ring_allreduce_host", "ring_allreduce_fused", "ring_psum", "ag_gemm", "gemm_rs", "ring_status", "ring_set_timeout_ms", "ring_set_slices",
-                     "ring_debug_skip_notify", "ring_finalize"):
-            getattr(L, name).restype = i
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(L, name)   # AttributeError here: the library is older than this module
+            fn.argtypes = args
         _lib = L
     return _lib
 
@@ -144,9 +156,6 @@ def ring_reduce_scatter_bidir(bufs: torch.Tensor, out: torch.Tensor, N: int | No
     """Bidirectional reduce-scatter (top halves travel left, bottom halves right);
     out[r, :N/P] = block r summed over ranks; ``bufs`` is clobbered."""
     fn = load().ring_reduce_scatter_bidir
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
-                   ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
-    fn.restype = ctypes.c_int
     bp, bs, dt = _slots(bufs, "bufs")
     op, os_, dt2 = _slots(out, "out")
     if dt != dt2 or bufs.size(0) != out.size(0):
@@ -168,8 +177,6 @@ def ring_allreduce(bufs: torch.Tensor, N: int | None = None, stream=None) -> tor
 
 def ring_allreduce_workspace_bytes(P: int, N: int, dtype=torch.float32) -> int:
     fn = load().ring_allreduce_workspace_bytes
-    fn.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_int]
-    fn.restype = ctypes.c_size_t
     return int(fn(P, N, _DTYPE[dtype]))
 
 
@@ -178,9 +185,6 @@ def ring_allreduce_ex(bufs: torch.Tensor, workspace: torch.Tensor, N: int | None
     at least ring_allreduce_workspace_bytes bytes); calls with distinct
     workspaces may run concurrently on different streams."""
     fn = load().ring_allreduce_ex
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
-                   ctypes.c_size_t, ctypes.c_void_p]
-    fn.restype = ctypes.c_int
     bp, bs, dt = _slots(bufs, "bufs")
     if not workspace.is_cuda:
         raise TypeError("workspace must be a CUDA tensor")
@@ -194,8 +198,6 @@ def ring_allreduce_ex(bufs: torch.Tensor, workspace: torch.Tensor, N: int | None
 def ring_allreduce_fused(bufs: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
     """Single-pass all-reduce with the ring's result (bit-identical to ring_allreduce)."""
     fn = load().ring_allreduce_fused
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
-    fn.restype = ctypes.c_int
     bp, bs, dt = _slots(bufs, "bufs")
     N = bufs.size(1) if N is None else N
     with torch.cuda.device(bufs.device):
@@ -206,8 +208,6 @@ def ring_allreduce_fused(bufs: torch.Tensor, N: int | None = None, stream=None) 
 def ring_psum(bufs: torch.Tensor, n: int | None = None, stream=None) -> torch.Tensor:
     """Rotate-and-accumulate all-reduce (each rank folds in its own rotated order), in place."""
     fn = load().ring_psum
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
-    fn.restype = ctypes.c_int
     bp, bs, dt = _slots(bufs, "bufs")
     n = bufs.size(1) if n is None else n
     with torch.cuda.device(bufs.device):
@@ -262,9 +262,6 @@ def gemm_rs(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, stream=None) ->
     """A [P, M, K], B [P, N, K], out [P, M, N/P], all bf16: out[r] = column chunk r
     of the ring reduce-scatter of the bf16 partial products A[q] . B[q]^T."""
     fn = load().gemm_rs
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
-                   ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
-    fn.restype = ctypes.c_int
     for name, t in (("A", A), ("B", B), ("out", out)):
         if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
             raise TypeError(f"{name} must be a contiguous 3-D bf16 CUDA tensor")
@@ -305,8 +302,6 @@ def ring_debug_set_trace(buf) -> None:
     """Step stamps of later ring launches go to ``buf`` (a CUDA uint64/int64
     tensor) -- see ring_debug_set_trace in include/ringcoll.h; None: off."""
     fn = load().ring_debug_set_trace
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
-    fn.restype = ctypes.c_int
     if buf is None:
         _check(fn(None, 0))
     else:
@@ -320,9 +315,6 @@ def ring_allreduce_noalloc(bufs: torch.Tensor, N: int | None = None, stream=None
     declaration in include/ringcoll.h for set-up and ordering rules."""
     L = load()
     fn = L.ring_allreduce_noalloc
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_size_t, ctypes.c_int,
-                   ctypes.c_void_p]
-    fn.restype = ctypes.c_int
     bp, bs, dt = _slots(bufs, "bufs")
     N = bufs.size(1) if N is None else N
     with torch.cuda.device(bufs.device):

@@ -131,11 +131,17 @@ def _pin_gemm():
 PINS = [_pin_ring_order, _pin_bitmask_positional, _pin_exact_and_fold, _pin_ppermute_allgather, _pin_bf16,
         _pin_psum, _pin_bidir, _pin_gemm]
 
+# the reduce-scatter round of orc_ring_allreduce around its left send index
+_LEFT_SEND = ("int left_send_idx = {};\n            memcpy(msg + (size_t)my_rank * cbytes,\n"
+              "                   slot_at(bufs, stride, left) + (size_t)left_send_idx * cbytes, cbytes);\n"
+              "        }}\n        for (int my_rank = 0; my_rank < P; ++my_rank) {{\n"
+              "            int recv_add_idx = (my_rank - step - 1 + P) % P;\n            hop_add")
+
 MUTANTS = {
     "recv_add_idx off by one": ("int recv_add_idx = (my_rank - step - 1 + P) % P;\n            hop_add",
                                 "int recv_add_idx = (my_rank - step + P) % P;\n            hop_add"),
-    "left send index off by one": ("int left_send_idx = (left - step + P) % P;\n            memcpy(msg + (size_t)my_rank * cbytes,\n                   slot_at(bufs, stride, left) + (size_t)left_send_idx * cbytes, cbytes);\n        }\n        for (int my_rank = 0; my_rank < P; ++my_rank) {\n            int recv_add_idx = (my_rank - step - 1 + P) % P;\n            hop_add",
-                                   "int left_send_idx = (left - step - 1 + P) % P;\n            memcpy(msg + (size_t)my_rank * cbytes,\n                   slot_at(bufs, stride, left) + (size_t)left_send_idx * cbytes, cbytes);\n        }\n        for (int my_rank = 0; my_rank < P; ++my_rank) {\n            int recv_add_idx = (my_rank - step - 1 + P) % P;\n            hop_add"),
+    "left send index off by one": (_LEFT_SEND.format("(left - step + P) % P"),
+                                   _LEFT_SEND.format("(left - step - 1 + P) % P")),
     "all-gather phase index": ("int recv_idx = (my_rank - 1 - t + P) % P;", "int recv_idx = (my_rank - t + P) % P;"),
     "reduction sign": ("for (i = 0; i < n; ++i) a[i] = b[i] + a[i];\n        break;\n    }\n    case ORC_BF16",
                        "for (i = 0; i < n; ++i) a[i] = b[i] - a[i];\n        break;\n    }\n    case ORC_BF16"),
