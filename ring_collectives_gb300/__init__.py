@@ -84,6 +84,7 @@ def load() -> ctypes.CDLL:
         for name, (args, res) in _SIGNATURES.items():
             fn = getattr(L, name)   # AttributeError here: the library is older than this module
             fn.argtypes = args
+            fn.restype = res
         _lib = L
     return _lib
 

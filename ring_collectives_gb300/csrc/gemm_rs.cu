@@ -318,7 +318,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int P = p.P;
     const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
 
-    if (warp == 0 && lane == 0) {
+    // Producers: warp 0 loads the A halves (and, in the even CTA, arms the
+    // full barrier for all four loads of the stage); with RC_GEMM_SPLIT_PRODUCER
+    // warp 3 loads the B halves, so the two requests of a stage are in flight
+    // together instead of one after the other.
+    const bool a_producer = warp == 0 && lane == 0;
+    const bool b_producer = (RC_GEMM_SPLIT_PRODUCER ? warp == 3 : warp == 0) && lane == 0;
+    if (a_producer || b_producer) {
         // ---------------- TMA producer (both CTAs)
         uint32_t stage = 0, phase = 0;
         int issued[STAGES2] = {0, 0, 0};
@@ -333,11 +339,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    if (even) mbar_expect_tx(full_bar + 8 * stage, 2 * (A2_STAGE + B2_STAGE));
-                    tma_load_4d_pair(sA + stage * A2_STAGE, &map_a, 0, m * PM + (int)cta * HM, kb * 2, r,
-                                     full_even + 8 * stage);
-                    tma_load_4d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * 2, r,
-                                     full_even + 8 * stage);
+                    if (a_producer) {
+                        if (even) mbar_expect_tx(full_bar + 8 * stage, 2 * (A2_STAGE + B2_STAGE));
+                        tma_load_4d_pair(sA + stage * A2_STAGE, &map_a, 0, m * PM + (int)cta * HM, kb * 2, r,
+                                         full_even + 8 * stage);
+                    }
+                    if (b_producer)
+                        tma_load_4d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * 2, r,
+                                         full_even + 8 * stage);
                     issued[stage]++;
                     if (++stage == STAGES2) {
                         stage = 0;
@@ -348,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         // The even CTA's full barriers count both CTAs' bytes: once the last
         // phase armed on each has completed, no load of either CTA is in flight.
-        if (even && *(volatile int *)abort_flag) {
+        if (a_producer && even && *(volatile int *)abort_flag) {
             for (int s = 0; s < STAGES2; ++s)
                 if (issued[s] > 0) wait_bar(full_bar + 8 * s, (uint32_t)((issued[s] - 1) & 1), ab, 9, true);
         }

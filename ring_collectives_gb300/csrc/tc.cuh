@@ -10,6 +10,11 @@
 #include "internal.h"
 #include "ringcoll.h"
 
+// 1: the CTA-pair GEMMs issue their A and B tile loads from two warps.
+#ifndef RC_GEMM_SPLIT_PRODUCER
+#define RC_GEMM_SPLIT_PRODUCER 1
+#endif
+
 namespace rc {
 namespace tc {
 

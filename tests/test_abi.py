@@ -91,3 +91,20 @@ def test_python_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(rc, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         rc.load()
+
+
+def test_binding_declares_every_header_function_with_its_result_type():
+    """The ctypes table covers every function of include/ringcoll.h, with the
+    header's result type (size_t, const char *, or int)."""
+    import ctypes
+    import re
+    import ring_collectives_gb300 as rc
+    with open(os.path.join(ROOT, "include", "ringcoll.h"), encoding="utf-8") as f:
+        text = f.read()
+    decls = dict((name, ret.strip()) for ret, name in
+                 re.findall(r"^(int|size_t|const char \*)\s*(\w+)\(", text, flags=re.M))
+    assert set(decls) == set(rc._SIGNATURES), set(decls) ^ set(rc._SIGNATURES)
+    want = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "const char *": ctypes.c_char_p}
+    L = rc.load()
+    for name, ret in decls.items():
+        assert getattr(L, name).restype is want[ret], name
