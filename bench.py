@@ -10,8 +10,9 @@ steps) over the workload's synthetic inputs, which are resident in HBM when
 the timed region starts.  The in-place inputs are restored by a device copy
 before every step, outside the CUDA events that time the step.  The metric is
 GB/s of the ring schedule's algorithmic bytes 5(P-1)*N*e per all-reduce
-(roofline (a)); the fraction of the minimum-traffic roofline (b) = 2*P*N*e is
-reported beside it.
+(roofline (a)).  The `roofline` object is taken against the bytes that must
+cross HBM, 2*P*N*e (roofline (b)), since most of the schedule's traffic stays
+in L2; the fraction of (a) is reported beside it.
 
 Multi-GPU (torchrun, one process per GPU): every rank runs an independent
 replica of the workload on its own GPU (the logical ranks already live in
@@ -597,6 +598,7 @@ def run_ours(args, spec, rank, world, dist):
     peak, peak_kind = peaks()
     rb = ring_bytes(P, N, e)
     achieved = rb / (ms * 1e-3) / 1e9
+    achieved_b = min_bytes(P, N, e) / (ms * 1e-3) / 1e9
     value = replicas_value(world, rb, ms_max)
     cpu_gbs, cpu_sample, _, cpu_T = oracle_time_threads(spec, seconds=args.cpu_seconds)
     cpu1_gbs, cpu1_sample, _ = oracle_time(spec, seconds=args.cpu_seconds / 2, frac=1)
@@ -606,13 +608,19 @@ def run_ours(args, spec, rank, world, dist):
         "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
         "config": config_dict(spec, world),
         "frac_roofline_a": round(achieved / peak, 4),
-        "frac_roofline_b": round(min_bytes(P, N, e) / (ms * 1e-3) / 1e9 / peak, 4),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4),
+        "frac_roofline_b": round(achieved_b / peak, 4),
+        # The roofline object uses the bytes that must cross HBM, 2*P*N*e (one
+        # read and one write of every element of every slot: 2*e bytes per
+        # element-slot); the ring schedule's 5(P-1)*N*e (the value above) mostly
+        # stays in L2, so against it the fraction exceeds 1 (frac_roofline_a).
+        "roofline": {"bound": "hbm", "achieved": round(achieved_b, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved_b / peak, 4),
                      # the committed weak-scaling capture is for P=8
                      "traffic": profiled_traffic(spec["name"]) if spec["name"] != "weak" or P == 8 else None,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs, burst copy)",
-                     "algorithmic_bytes_per_launch": rb, "kernel": "k_ring (one launch per all-reduce)"},
+                     "algorithmic_bytes_per_launch": min_bytes(P, N, e),
+                     "algorithmic_bytes": "2*P*N*e: every element of every slot read once and written once",
+                     "ring_schedule_bytes_per_launch": rb, "kernel": "k_ring (one launch per all-reduce)"},
         "cpu_baseline": {"value": round(cpu_gbs, 3), "unit": "GB/s", "cores": cpu_T, "kind": "oracle",
                          "sample": cpu_sample,
                          "single_thread": {"value": round(cpu1_gbs, 3), "cores": 1, "sample": cpu1_sample}},
@@ -708,6 +716,7 @@ def run_row(args, rank, world, dist):
         alg = min_bytes(P, N, e)
         row_min = alg
         alg_text = "2*P*N*e (every input read once, every output written once)"
+        row_min_text = alg_text
         kern, sources = "k_fold_reg (register form, P=8)", FOLD_SOURCES
         metric = (f"{'fused ring-order' if name.startswith('fused') else 'psum'} single-pass all-reduce GB/s "
                   f"(2*P*N*e / time), P=8, 64 MiB/rank, f32, 1xGB300 per replica")
@@ -716,6 +725,7 @@ def run_row(args, rank, world, dist):
         fn = rc.ring_reduce_scatter if name == "reduce_scatter_bf16_64mib" else rc.ring_reduce_scatter_bidir
         call = lambda: fn(bufs, out, stream=stream)   # noqa: E731
         row_min = (P + 1) * N * e   # read every slot once, write one chunk per rank
+        row_min_text = "(P+1)*N*e: every slot read once, one reduced chunk written per rank"
         if name == "reduce_scatter_bf16_64mib":
             alg = 3 * (P - 1) * N * e
             alg_text = "3(P-1)*N*e (per rank P-1 steps of 2 chunk reads + 1 chunk write)"
@@ -733,6 +743,7 @@ def run_row(args, rank, world, dist):
         call = lambda: rc.ring_ppermute_right(pr, bufs, stream=stream)   # noqa: E731
         alg = row_min = 2 * P * N * e
         alg_text = "2*P*n*e (every source slot read once, every destination slot written once)"
+        row_min_text = alg_text
         kern, sources = "k_ppermute", KERNEL_SOURCES
         metric = "ppermute right-shift GB/s (2*P*n*e / time), P=8, 64 MiB/rank, f32, 1xGB300 per replica"
     else:
@@ -741,6 +752,7 @@ def run_row(args, rank, world, dist):
         call = lambda: rc.ring_all_gather(pr, out, stream=stream)   # noqa: E731
         alg = 2 * P * N * e + 2 * (P - 1) * P * N * e
         row_min = P * N * e + P * P * N * e
+        row_min_text = "P*n*e + P^2*n*e: every shard read once, every output written once"
         alg_text = "2*P*n*e (own shard) + 2(P-1)*P*n*e (P-1 ring steps of a read and a write of n)"
         kern, sources = "k_ring (all-gather mode)", KERNEL_SOURCES
         metric = "ring all_gather GB/s (2P*n*e*P / time), P=8, 8 MiB shards, f32, 1xGB300 per replica"
@@ -779,12 +791,16 @@ def run_row(args, rank, world, dist):
         "config": {"workload": name, "P": P, "N_per_rank": N, "bytes_per_rank": N * e, "replicas": world,
                    "l2": ("inputs larger than L2; in-place inputs restored by a device copy before every "
                           "step, outside the events")},
+        "frac_schedule_bytes": round(achieved / peak, 4),
         "frac_roofline_b": round(row_min / (ms * 1e-3) / 1e9 / peak, 4),
-        "roofline_b_bytes": row_min,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name, sources, prefix=""),
+        # roofline against the bytes that must cross HBM (the row's minimum);
+        # the schedule's own byte count is reported beside it
+        "roofline": {"bound": "hbm", "achieved": round(row_min / (ms * 1e-3) / 1e9, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(row_min / (ms * 1e-3) / 1e9 / peak, 4),
+                     "traffic": profiled_traffic(name, sources, prefix=""),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs, burst copy)",
-                     "algorithmic_bytes_per_launch": alg, "algorithmic_bytes": alg_text, "kernel": kern},
+                     "algorithmic_bytes_per_launch": row_min, "algorithmic_bytes": row_min_text,
+                     "schedule_bytes_per_launch": alg, "schedule_bytes": alg_text, "kernel": kern},
         "gpu_launches": args.steps, "clocks": clocks.summary(),
         "ms_min": round(min(times), 4), "ms_median": round(statistics.median(times), 4),
     }
