@@ -61,7 +61,8 @@ def check_c(A_bits, B_bits, C_gpu_bits, rows=None, cols=None, min_exact=0.95):
 
 @pytest.mark.parametrize("P,M_r,K,N,rank", [(1, 128, 64, 256, 0), (4, 128, 256, 256, 0), (4, 128, 256, 256, 2),
                                             (2, 256, 1024, 512, 1), (3, 384, 512, 768, 2), (4, 256, 256, 512, 3),
-                                            (1, 256, 128, 256, 0), (8, 512, 384, 1024, 5), (2, 256, 192, 256, 0)])
+                                            (1, 256, 128, 256, 0), (8, 512, 384, 1024, 5), (2, 256, 192, 256, 0),
+                                            (3, 768, 256, 512, 2), (5, 256, 128, 768, 4)])
 def test_ag_gemm_small_full_check(P, M_r, K, N, rank):
     """M_r a multiple of 256 and K of 128 run on CTA pairs (256x256 tiles,
     K=128 stages); the other shapes on single CTAs (128x256 tiles)."""

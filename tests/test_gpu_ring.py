@@ -262,6 +262,21 @@ def test_host_pipelined_segments_in_place_ragged():
     assert not np_of(h[:, N:]).any(), "wrote past N in the host slots"
 
 
+@pytest.mark.parametrize("P,c,dtype", [(16, 1_048_583, torch.int32), (3, 11_184_811, torch.float32)])
+def test_host_pipelined_segments_other_shapes(P, c, dtype):
+    """The segmented host path at P = 16 (int32, exact sums) and P = 3 (a
+    chunk length that is not a multiple of the slice granule), out of place."""
+    N = P * c
+    x = make(P, N, dtype, seed=P * 5 + 1)
+    h_in = x.pin_memory()
+    h_out = torch.zeros_like(x).pin_memory()
+    d = torch.empty((P, N), dtype=dtype, device=DEV)
+    rc.ring_allreduce_host(h_in, h_out, d)
+    torch.cuda.synchronize()
+    ok_status()
+    assert np.array_equal(np_of(h_out), oracle.ring_allreduce(np_of(x).copy(), NAME[dtype]))
+
+
 def test_host_pipelined_full_workload():
     """P=8 x 64 MiB fp32 through pinned host slots (the end-to-end leg of the
     benchmark): bit-exact with the oracle, twice in a row on one stream."""
