@@ -268,13 +268,23 @@ int ring_status(void *stream);
 /* Message describing the calling thread's most recent error ("" if none). */
 const char *ring_last_error(void);
 
-/* Bound on every device-side wait, in milliseconds (default 2000, 1..600000). */
+/* Bound on every device-side wait, in milliseconds (1..600000; initial value
+ * from the environment variable RC_TIMEOUT_MS, else 2000). */
 int ring_set_timeout_ms(unsigned ms);
 
 /*
- * Slices per rank for the ring kernels (0 = automatic).  Slice j of every
- * chunk is an independent ring with its own signals; the grid is P x slices
- * co-resident thread blocks.  Values above the co-residency limit are capped.
+ * Slices per rank for the ring kernels (0 = automatic; initial value from the
+ * environment variable RC_SLICES, else 0).  Slice j of every chunk is an
+ * independent ring with its own signals; the grid is P x slices co-resident
+ * thread blocks.  Values above the co-residency limit are capped.
+ *
+ * Other environment settings, read once: RC_DEBUG_SERIAL=1 makes every step
+ * of a ring launch also wait for all blocks of the launch (a bounded grid
+ * barrier; for debugging synchronisation, results are unchanged);
+ * RC_AG_BULK=0 moves all-gather steps with vector copies instead of bulk
+ * copies; RC_L2_LIVE_BYTES sets the chunk-segment budget; RC_HOST_SEGMENT_BYTES
+ * the host entry point's segment size; RC_GEMM_PAIRS=0 keeps the one-CTA
+ * GEMM kernels.
  */
 int ring_set_slices(int slices);
 

@@ -15,8 +15,20 @@
 namespace {
 
 thread_local std::string g_err;
-std::atomic<unsigned> g_timeout_ms{2000};
-std::atomic<int> g_slices{0};
+
+// Unsigned value of environment variable `name`, or `dflt` when it is unset
+// or malformed (initial values of the settings below; the setters override).
+unsigned env_uint(const char *name, unsigned dflt)
+{
+    const char *e = getenv(name);
+    if (!e || !*e) return dflt;
+    char *end = nullptr;
+    const unsigned long v = strtoul(e, &end, 10);
+    return (end && *end == 0 && v <= 0xFFFFFFFFul) ? (unsigned)v : dflt;
+}
+
+std::atomic<unsigned> g_timeout_ms{env_uint("RC_TIMEOUT_MS", 2000)};   // ring_set_timeout_ms
+std::atomic<int> g_slices{(int)env_uint("RC_SLICES", 0)};             // ring_set_slices
 std::atomic<int> g_skip_rank{-1}, g_skip_step{-1};
 std::atomic<unsigned long long *> g_trace{nullptr};
 std::atomic<size_t> g_trace_words{0};
@@ -56,6 +68,15 @@ int ag_bulk_default()
         if (e && e[0] == '1' && e[1] == 0) return 1;
         return 1;
     }();
+    return v;
+}
+// Debug knob, read once from the environment: RC_DEBUG_SERIAL=1 makes every
+// step of a ring launch also wait for all blocks of the launch (a bounded
+// grid barrier), ruling fine-grained synchronisation in or out as the cause
+// of a wrong result.
+int debug_serial()
+{
+    static const int v = env_uint("RC_DEBUG_SERIAL", 0) != 0;
     return v;
 }
 constexpr size_t kMinSliceBytes = 32 << 10; // a slice below this is not worth its own ring
@@ -262,6 +283,7 @@ int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda, void *ext_ws = 
     p.skip_step = g_skip_step.exchange(-1);
     p.trace = g_trace.load();
     p.trace_words = g_trace_words.load();
+    p.debug_serial = debug_serial();
     cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, st_cuda);
     if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
     if (!ext_ws) st->launches += (uint64_t)p.segments; // the launch advances the epoch by its segment count
@@ -798,6 +820,7 @@ int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int 
     p.segments = 1;
     p.chunk_stride = c;
     p.ag_bulk = ag_bulk_default();
+    p.debug_serial = debug_serial();
     cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, s);
     if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
     na.launches++;

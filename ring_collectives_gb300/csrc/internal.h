@@ -15,7 +15,7 @@ struct WsHeader {
     uint32_t err_rank;  // where the first failure happened
     uint32_t err_step;
     uint32_t err_slice;
-    uint32_t pad[26];
+    uint32_t pad[26];   // pad[0]: abort word of the running launch; pad[1]: debug grid-barrier counter
 };
 static_assert(sizeof(WsHeader) == 128, "header is one 128-byte line");
 
@@ -38,6 +38,7 @@ struct RingParams {
     int discard;         // 1: drop the L2 lines of reduce-scatter partials once read (their data is dead)
     int segments;        // chunk segments run one after another (keeps a step's live data in L2)
     int ag_bulk;         // 1: all-gather copies move through shared memory with bulk (TMA) copies
+    int debug_serial;    // 1: every step also waits for all blocks of the launch (debugging)
     int skip_rank, skip_step; // test hook: this rank skips its notify after this step (-1: none)
     unsigned long long timeout_ns;
     unsigned long long *trace; // optional step stamps (see ring_debug_set_trace); null: off

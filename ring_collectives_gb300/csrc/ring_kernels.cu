@@ -325,6 +325,48 @@ __device__ __forceinline__ void ag_copy(char *dst, const char *src, size_t n, Bu
     }
 }
 
+// ------------------------------------------------------------ debug grid barrier
+// RC_DEBUG_SERIAL: after every step, all blocks of the launch meet.  Thread 0
+// adds one arrival to a launch-wide counter (the header's pad[1], zero at the
+// start of every launch: the last block to finish resets it) and waits,
+// bounded like every other wait, until round * gridDim.x blocks have arrived.
+__device__ void grid_meet(const RingParams &p, uint32_t round, uint32_t E, uint32_t *abort_word, int r, int g, int j,
+                          int *abort_flag)
+{
+    __syncthreads();
+    if (threadIdx.x == 0 && !*abort_flag) {
+        uint32_t *ctr = &p.hdr->pad[1];
+        __threadfence();
+        atomicAdd(ctr, 1u);
+        const uint32_t goal = round * gridDim.x;
+        uint64_t t0 = 0;
+        for (uint32_t it = 0;; ++it) {
+            if ((int32_t)(ld_acquire_gpu(ctr) - goal) >= 0) break;
+            if ((it & 31u) == 31u) {
+                if (ld_relaxed_gpu(abort_word) == E) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint64_t now = global_timer_ns();
+                if (t0 == 0) {
+                    t0 = now;
+                } else if (now - t0 > p.timeout_ns) {
+                    if (atomicCAS(&p.hdr->status, 0u, (unsigned)RC_ERR_TIMEOUT) == 0u) {
+                        p.hdr->err_rank = (uint32_t)r;
+                        p.hdr->err_step = (uint32_t)g;
+                        p.hdr->err_slice = (uint32_t)j;
+                    }
+                    st_relaxed_gpu(abort_word, E);
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+            __nanosleep(32);
+        }
+    }
+    __syncthreads();
+}
+
 // ------------------------------------------------------------ the step engine
 // Segments: when one step's live data (P chunks) would not fit in L2, each
 // slice ring runs all its steps on segment 0 of the chunks, then segment 1,
@@ -396,6 +438,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
     char *my_slot = p.data + (size_t)r * p.data_stride;
     const char *from_slot = p.data + (size_t)from * p.data_stride;
     constexpr int T = kRingThreads;
+    uint32_t meet_round = 0;   // debug grid barriers passed (RC_DEBUG_SERIAL)
 
     for (int q = 0; q < p.segments; ++q) {
         const size_t seg_lo = range_lo + slice_begin(range_n, q, p.segments);
@@ -498,6 +541,10 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                     st_release_gpu(&s_to_rows[(size_t)(g + 1) * P + r], V);
             }
             if (threadIdx.x == 0 && s_stamp && q == 0) s_stamp[3 * g + 2] = global_timer_ns();
+            if (p.debug_serial) {
+                grid_meet(p, ++meet_round, E, abort_word, r, g, j, &s_abort);
+                if (s_abort) break;
+            }
         }
         if (s_abort) break;
     }
@@ -509,6 +556,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
         const uint32_t prev = atomicAdd(&p.hdr->done, 1u);
         if (prev == gridDim.x - 1) {
             p.hdr->done = 0;
+            p.hdr->pad[1] = 0;   // debug grid-barrier counter
             st_relaxed_gpu(&p.hdr->epoch, E0 + (uint32_t)p.segments);
         }
     }

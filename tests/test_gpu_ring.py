@@ -426,6 +426,77 @@ def test_vector_all_gather_copies_child():
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
 
 
+def test_serial_debug_mode_child():
+    """RC_DEBUG_SERIAL=1 (every step also waits for all blocks of the launch,
+    the barrier-injection debug mode): all-reduce, reduce-scatter and
+    all-gather stay bit-exact, and the next launches (which reuse the barrier
+    counter) too."""
+    import os
+    import subprocess
+    import sys
+    from tests.conftest import ROOT
+    env = dict(os.environ, RC_DEBUG_SERIAL="1")
+    r = subprocess.run([sys.executable, "-c", _SEGMENT_CHILD, ROOT], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+_POISON = 0x7FC0DEAD   # a quiet-NaN payload no computation here produces
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
+def test_poisoned_padding_is_never_touched(dtype):
+    """Slots padded with a NaN pattern: every collective reads and writes only
+    the first N elements of each slot (and of each output row); the padding
+    keeps its pattern bit for bit and no poison reaches a result."""
+    P, c, pad = 5, 64 * 41 + 3, 37
+    N = P * c
+    es = torch.tensor([], dtype=dtype).element_size()
+    word = torch.tensor([_POISON], dtype=torch.int32)
+    def poisoned(rows, cols):
+        t = torch.empty((rows, cols), dtype=dtype, device=DEV)
+        t.view(torch.uint8).copy_(word.view(torch.uint8).repeat(rows * cols * es // 4).view(rows, cols * es))
+        return t
+    def pad_intact(t, used):
+        ref = poisoned(t.size(0), t.size(1))
+        assert torch.equal(t[:, used:].view(torch.uint8), ref[:, used:].view(torch.uint8)), "padding changed"
+    x = make(P, N, dtype, seed=77)
+    xn = np_of(x)
+    name = NAME[dtype]
+    b = poisoned(P, N + pad)
+    b[:, :N] = x.to(DEV)
+    rc.ring_allreduce(b, N=N)
+    ok_status()
+    assert np.array_equal(np_of(b[:, :N]), oracle.ring_allreduce(xn.copy(), name))
+    pad_intact(b, N)
+    b[:, :N] = x.to(DEV)
+    out = poisoned(P, c + pad)
+    rc.ring_reduce_scatter(b, out, N=N)
+    ok_status()
+    assert np.array_equal(np_of(out[:, :c]), oracle.reduce_scatter(xn.copy(), name))
+    pad_intact(out, c)
+    pad_intact(b, N)
+    shards = poisoned(P, c + pad)
+    shards[:, :c] = x[:, :c].to(DEV)
+    gat = poisoned(P, P * c + pad)
+    rc.ring_all_gather(shards, gat, n=c)
+    ok_status()
+    assert np.array_equal(np_of(gat[:, :P * c]), oracle.all_gather(np_of(x[:, :c].contiguous()), name))
+    pad_intact(gat, P * c)
+    dst = poisoned(P, N + pad)
+    rc.ring_ppermute_right(b[:, :N + pad], dst, n=N)
+    ok_status()
+    pad_intact(dst, N)
+    for fn, want in ((rc.ring_allreduce_fused, oracle.ring_allreduce(xn.copy(), name)),
+                     (rc.ring_psum, oracle.psum(xn.copy(), name))):
+        f = poisoned(P, N + pad)
+        f[:, :N] = x.to(DEV)
+        fn(f, N) if fn is rc.ring_allreduce_fused else fn(f, n=N)
+        torch.cuda.synchronize()
+        assert np.array_equal(np_of(f[:, :N]), want)
+        pad_intact(f, N)
+
+
 # ------------------------------------------------------------------ bidirectional reduce-scatter
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
 @pytest.mark.parametrize("P,c", [(1, 100), (2, 2), (2, 7), (3, 1), (4, 256), (4, 2048), (5, 1001), (8, 64 * 33 + 6),
