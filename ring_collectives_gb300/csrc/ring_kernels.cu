@@ -384,7 +384,9 @@ __device__ void grid_meet(const RingParams &p, uint32_t round, uint32_t E, uint3
 // bottom) holds for chunk (r+1+s) resp. (r-1-s) to its own contribution; in
 // step P-1 it copies the finished chunk r from that neighbour to out_r.  Each
 // chunk half is written once, so no buffer is ever overwritten while read.
-template <int DT, int MODE>
+// SERIAL: the barrier-injection debug variant (RingParams::debug_serial); a
+// separate instantiation, so the normal kernels carry none of its state.
+template <int DT, int MODE, bool SERIAL>
 __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const RingParams p)
 {
     constexpr size_t ES = DT == 1 ? 2 : 4;
@@ -541,7 +543,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                     st_release_gpu(&s_to_rows[(size_t)(g + 1) * P + r], V);
             }
             if (threadIdx.x == 0 && s_stamp && q == 0) s_stamp[3 * g + 2] = global_timer_ns();
-            if (p.debug_serial) {
+            if constexpr (SERIAL) {
                 grid_meet(p, ++meet_round, E, abort_word, r, g, j, &s_abort);
                 if (s_abort) break;
             }
@@ -581,23 +583,30 @@ __global__ void __launch_bounds__(256) k_ppermute(const char *src, size_t ss, ch
 }
 
 // ------------------------------------------------------------ host launchers
-template <int DT>
+template <int DT, bool SERIAL>
 static const void *ring_fn_mode(int mode)
 {
     switch (mode) {
-    case MODE_ALLREDUCE: return (const void *)k_ring<DT, MODE_ALLREDUCE>;
-    case MODE_REDUCE_SCATTER: return (const void *)k_ring<DT, MODE_REDUCE_SCATTER>;
-    case MODE_ALL_GATHER: return (const void *)k_ring<DT, MODE_ALL_GATHER>;
-    default: return (const void *)k_ring<DT, MODE_RS_BIDIR>;
+    case MODE_ALLREDUCE: return (const void *)k_ring<DT, MODE_ALLREDUCE, SERIAL>;
+    case MODE_REDUCE_SCATTER: return (const void *)k_ring<DT, MODE_REDUCE_SCATTER, SERIAL>;
+    case MODE_ALL_GATHER: return (const void *)k_ring<DT, MODE_ALL_GATHER, SERIAL>;
+    default: return (const void *)k_ring<DT, MODE_RS_BIDIR, SERIAL>;
     }
 }
 
-static const void *ring_fn(int dtype, int mode)
+static const void *ring_fn(int dtype, int mode, bool serial = false)
 {
+    if (serial) {
+        switch (dtype) {
+        case 0: return ring_fn_mode<0, true>(mode);
+        case 1: return ring_fn_mode<1, true>(mode);
+        default: return ring_fn_mode<2, true>(mode);
+        }
+    }
     switch (dtype) {
-    case 0: return ring_fn_mode<0>(mode);
-    case 1: return ring_fn_mode<1>(mode);
-    default: return ring_fn_mode<2>(mode);
+    case 0: return ring_fn_mode<0, false>(mode);
+    case 1: return ring_fn_mode<1, false>(mode);
+    default: return ring_fn_mode<2, false>(mode);
     }
 }
 
@@ -614,10 +623,10 @@ cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks)
     int sms = 0, best = 1 << 30;
     cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
-    for (int mode = 0; mode < 4; ++mode) {
+    for (int mode = 0; mode < 8; ++mode) {   // four modes, normal and serial-debug variants
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_fn(dtype, mode), threads,
-                                                          ring_dyn_smem(mode, 1));
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_fn(dtype, mode & 3, mode >= 4), threads,
+                                                          ring_dyn_smem(mode & 3, 1));
         if (e != cudaSuccess) return e;
         if (per_sm < best) best = per_sm;
     }
@@ -631,8 +640,8 @@ cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_
     if (copy.chunk_stride == 0) copy.chunk_stride = copy.chunk;   // chunks back to back
     void *args[] = {(void *)&copy};
     const unsigned blocks = (unsigned)(p.P * p.S) * (p.mode == MODE_RS_BIDIR ? 2u : 1u);
-    return cudaLaunchCooperativeKernel(ring_fn(dtype, p.mode), dim3(blocks), dim3((unsigned)threads), args,
-                                       ring_dyn_smem(copy.mode, copy.ag_bulk), st);
+    return cudaLaunchCooperativeKernel(ring_fn(dtype, copy.mode, copy.debug_serial != 0), dim3(blocks),
+                                       dim3((unsigned)threads), args, ring_dyn_smem(copy.mode, copy.ag_bulk), st);
 }
 
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P, size_t n,
