@@ -40,7 +40,8 @@ constexpr int kMaxDevices = 64;
 // kDefaultL2LiveBytes run one after another, so the partial sums of a step
 // stay in L2 until the next step reads them.  Both measured on GB300
 // (126 MB L2): up to 64 MiB of live chunks one pass is fastest (each segment
-// adds 2(P-1) signal steps); above it, 48 MiB segments beat 64 and 100 MiB.
+// adds 2(P-1) signal steps); above it, 48 MiB segments beat 32, 64 and
+// 96 MiB by 1-7 % (checked at P = 8, 16 and 32 with 16 MiB chunks).
 constexpr size_t kDefaultL2LiveBytes = 48ull << 20;
 constexpr size_t kL2NoSplitBytes = 64ull << 20;
 
