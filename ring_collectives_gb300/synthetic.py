@@ -21,6 +21,9 @@ Workloads (the names used by the tests and the benchmark):
 * ``ag_gemm``   -- P=8 row shards A_r [1024,4096] and the weight B
                    [4096,4096], bf16 ~ N(0, 0.02^2), seed 4 (A's slots use
                    streams (4, r), B uses (4, P)).
+
+``bf16_bit_patterns`` draws very large bf16 inputs cheaply (finite values of
+random sign with exponents in [2^-8, 2^8), as raw 16-bit patterns).
 """
 from __future__ import annotations
 
@@ -59,6 +62,41 @@ def _uniform_pm1(g, row):
 
 def _normal(g, row):
     g.standard_normal(out=row, dtype=np.float32)
+
+
+def bf16_bit_patterns(P: int, N: int, seed: int = 5, device=None) -> torch.Tensor:
+    """[P, N] bf16 whose 16-bit patterns are uniform over the finite values
+    with exponent field 0x77..0x86 (magnitudes in [2^-8, 2^8)) and a random
+    sign, drawn as integers with no floating-point arithmetic.  With a CUDA
+    ``device`` the bits come from a seeded torch generator on that device
+    (for inputs of billions of elements; copy the result to the host for
+    anything that needs the same bytes there), else from numpy as above."""
+    if device is not None and torch.device(device).type == "cuda":
+        g = torch.Generator(device=device).manual_seed(seed)
+        out_d = torch.empty((P, N), dtype=torch.int16, device=device)
+        step = 1 << 28
+        for r in range(P):
+            for i in range(0, N, step):
+                n = min(step, N - i)
+                w = torch.randint(-32768, 32768, (n,), dtype=torch.int16, device=device, generator=g)
+                # keep sign and mantissa bits; 4 random bits pick the exponent 0x77..0x86
+                out_d[r, i:i + n] = (w & -32641) | ((((w >> 7) & 0xF) + 0x77) << 7)   # -32641 == 0x807F
+        return out_d.view(torch.bfloat16)
+    out = np.empty((P, N), dtype=np.uint16)
+
+    def one(r):
+        g = np.random.default_rng([seed, r])
+        step = 1 << 26
+        for i in range(0, N, step):
+            n = min(step, N - i)
+            w = np.frombuffer(g.bytes(2 * n), dtype=np.uint16)
+            # keep sign and mantissa bits; 4 random bits pick the exponent 0x77..0x86
+            out[r, i:i + n] = (w & np.uint16(0x807F)) | (((w >> np.uint16(7)) & np.uint16(0xF)) + np.uint16(0x77)) << np.uint16(7)
+
+    workers = max(1, min(P, os.cpu_count() or 1))
+    with ThreadPoolExecutor(workers) as ex:
+        list(ex.map(one, range(P)))
+    return torch.from_numpy(out.view(np.int16)).view(torch.bfloat16)
 
 
 def uniform01(P: int, N: int, seed: int = 0) -> torch.Tensor:

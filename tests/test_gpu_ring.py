@@ -497,6 +497,40 @@ def test_poisoned_padding_is_never_touched(dtype):
         pad_intact(f, N)
 
 
+def test_slots_beyond_2_to_31_elements():
+    """Maximum sizes: P=2 slots of 2^31 + 256 bf16 (4 GiB each, element
+    offsets past 32 bits) through the ring all-reduce (64 chunk segments)
+    and the single-pass fold: both ranks identical, and equal to the
+    oracle's closed form at both ends of every chunk, around element 2^31 and
+    at random indices."""
+    P, N = 2, (1 << 31) + 256
+    c = N // P
+    x = synthetic.bf16_bit_patterns(P, N, seed=6, device=DEV)
+    xh = np_of(x)
+    rng = np.random.default_rng(6)
+    idx = np.unique(np.concatenate([np.arange(P) * c, np.arange(1, P + 1) * c - 1,
+                                    np.array([(1 << 31) - 1, 1 << 31, (1 << 31) + 1, N - 1]),
+                                    rng.integers(0, N, 4096)])).astype(np.int64)
+    want = oracle.ring_fold_at(xh, "bf16", idx)
+    idx_d = torch.from_numpy(idx).to(DEV)
+    b = x.clone()
+    rc.ring_allreduce(b)
+    ok_status()
+    got = np_of(b[:, idx_d])
+    for r in range(P):
+        assert np.array_equal(got[r], want)
+    assert torch.equal(b[0], b[1])
+    del b
+    rc.ring_allreduce_fused(x)
+    torch.cuda.synchronize()
+    got = np_of(x[:, idx_d])
+    for r in range(P):
+        assert np.array_equal(got[r], want)
+    assert torch.equal(x[0], x[1])
+    del x
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ bidirectional reduce-scatter
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
 @pytest.mark.parametrize("P,c", [(1, 100), (2, 2), (2, 7), (3, 1), (4, 256), (4, 2048), (5, 1001), (8, 64 * 33 + 6),
