@@ -531,6 +531,40 @@ def test_slots_beyond_2_to_31_elements():
     torch.cuda.empty_cache()
 
 
+def test_trace_stamps_are_complete_ordered_and_causal():
+    """ring_debug_set_trace: every block writes its three stamps per step
+    (wait start, wait end, step end), in order within the block; a block's
+    wait for step g ends no earlier than its left neighbour's wait for step
+    g-1 ended (the notify it waits for comes after that); results are
+    unchanged, and nothing is written once tracing is off."""
+    P, S, c = 8, 4, 64 * 200
+    N = P * c
+    steps = 2 * (P - 1)
+    rc.ring_set_slices(S)
+    try:
+        x = make(P, N, torch.float32, seed=5)
+        buf = torch.zeros(P * S * steps * 3, dtype=torch.int64, device=DEV)
+        rc.ring_debug_set_trace(buf)
+        b = x.to(DEV)
+        rc.ring_allreduce(b)
+        ok_status()
+        rc.ring_debug_set_trace(None)
+        assert np.array_equal(np_of(b), oracle.ring_allreduce(np_of(x).copy(), "f32"))
+        t = buf.view(P, S, steps, 3).cpu().numpy()          # block b = rank * S + slice
+        assert (t > 0).all(), "missing stamps"
+        assert (np.diff(t.reshape(P * S, steps * 3), axis=1) >= 0).all(), "stamps out of order in a block"
+        for r in range(P):
+            left = (r - 1) % P
+            assert (t[r, :, 1:, 1] >= t[left, :, :-1, 1]).all(), f"rank {r} passed a wait before its left neighbour"
+        buf.zero_()
+        rc.ring_allreduce(x.to(DEV))
+        ok_status()
+        assert not buf.any(), "a launch wrote stamps after tracing was turned off"
+    finally:
+        rc.ring_debug_set_trace(None)
+        rc.ring_set_slices(0)
+
+
 # ------------------------------------------------------------------ bidirectional reduce-scatter
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.int32])
 @pytest.mark.parametrize("P,c", [(1, 100), (2, 2), (2, 7), (3, 1), (4, 256), (4, 2048), (5, 1001), (8, 64 * 33 + 6),
