@@ -395,6 +395,27 @@ def bf16_peak():
         return 1900.0, "fallback burst"
 
 
+def cublas_same_shape(A, Bt, stream, args):
+    """Context for the tensor-core rows: cuBLAS (torch.matmul, bf16 in and
+    out, fp32 accumulate) on one GEMM with the row's M, N and total K, timed
+    like the row (CUDA events per call, mean after warm-up).  Not on the
+    product path; its own accumulation order differs."""
+    out = torch.empty((A.shape[0], Bt.shape[0]), dtype=torch.bfloat16, device=A.device)
+    for _ in range(max(args.warmup, 3)):
+        torch.matmul(A, Bt.t(), out=out)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for x, y in ev:
+        x.record(stream)
+        torch.matmul(A, Bt.t(), out=out)
+        y.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(x.elapsed_time(y) for x, y in ev)
+    flop = 2 * A.shape[0] * Bt.shape[0] * A.shape[1]
+    return {"ms": round(ms, 4), "TFLOP/s": round(flop / (ms * 1e-3) / 1e12, 1),
+            "shape": f"{A.shape[0]}x{Bt.shape[0]}x{A.shape[1]}", "call": "torch.matmul (cuBLAS), bf16"}
+
+
 def ag_gemm_secondary(rc, dev, stream, args):
     """All-gather + GEMM at P=8, shards [1024,4096], B [4096,4096] bf16 (tensor-bound)."""
     P, M_r, K, N = 8, 1024, 4096, 4096
@@ -417,9 +438,11 @@ def ag_gemm_secondary(rc, dev, stream, args):
     flop = 2 * P * M_r * N * K
     peak, kind = bf16_peak()
     tf = flop / (ms * 1e-3) / 1e12
+    cb = cublas_same_shape(ag, bd, stream, args)
     return {"ag_gemm_p8_8192x4096x4096": {
         "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peak, 4),
         "peak": peak, "peak_kind": kind, "flop_per_call": flop,
+        "cublas_same_shape": cb, "frac_of_cublas_same_shape": round(tf / cb["TFLOP/s"], 4),
         "note": "gather of the 8 shards (64 MiB) + C = A_g.B^T, one tcgen05 launch"}}
 
 
@@ -479,9 +502,13 @@ def gemm_rs_secondary(rc, dev, stream, args):
     flop = 2 * P * M * N * K
     peak, kind = bf16_peak()
     tf = flop / (ms * 1e-3) / 1e12
+    # the same flops as one GEMM: sum_q A_q.B_q^T = [A_0 .. A_7] . [B_0 .. B_7]^T (K = P*512)
+    cb = cublas_same_shape(ad.permute(1, 0, 2).reshape(M, P * K).contiguous(),
+                           bd.permute(1, 0, 2).reshape(N, P * K).contiguous(), stream, args)
     return {"gemm_rs_p8_8192x4096x512": {
         "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peak, 4), "peak": peak,
         "peak_kind": kind, "flop_per_call": flop,
+        "cublas_same_shape": cb, "frac_of_cublas_same_shape": round(tf / cb["TFLOP/s"], 4),
         "note": "8 partial products folded in ring order in the epilogue; output [8,8192,512] bf16"}}
 
 
@@ -679,6 +706,8 @@ def run_ag_gemm(args, rank, world, dist):
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(tf / peak, 4), "traffic": None, "peak_kind": kind,
                      "algorithmic_flop_per_launch": flop, "kernel": kern},
+        "cublas_same_shape": res["cublas_same_shape"],
+        "frac_of_cublas_same_shape": res["frac_of_cublas_same_shape"],
         "gpu_launches": args.steps, "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)

@@ -36,6 +36,7 @@
 #include <cstdlib>
 #include <mutex>
 
+#include "gemm_cfg.h"
 #include "tc.cuh"
 
 namespace rc {
@@ -88,6 +89,41 @@ __device__ __forceinline__ void unit_of(const Params &p, int u, int &mb, int &pi
     const int others = p.g_total_m - p.g_per_pe;
     const int order = i < others ? i + p.g_per_pe : i - others;
     mb = (order + p.rank * p.g_per_pe) % p.g_total_m;
+}
+
+// Waits until the BM/PIECE_ROWS ready flags of one 128-row block of A_g have
+// reached the launch's epoch.  The flags are read together (relaxed loads,
+// one round trip per poll instead of one per flag); the fence.acq_rel after
+// the poll that saw them all makes those reads an acquire, so with the gather
+// producers' release stores every copy into the block precedes what follows.
+// Bounded like every other wait.
+__device__ bool wait_block_flags(const uint32_t *f, uint32_t E, const Abort &ab, int where)
+{
+    constexpr int NF = BM / PIECE_ROWS;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t v[NF];
+#pragma unroll
+        for (int q = 0; q < NF; ++q) v[q] = ld_relaxed_gpu(f + q);
+        bool all = true;
+#pragma unroll
+        for (int q = 0; q < NF; ++q) all = all && epoch_reached(v[q], E);
+        if (all) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            return true;
+        }
+        if ((it & 15u) == 15u) {
+            if (*(volatile int *)ab.flag) return false;
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > ab.timeout_ns) {
+                record_timeout(ab, where);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -155,11 +191,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int src_rank = (m * BM) / p.M_r;
             const bool own = src_rank == p.rank;
             if (!own) {
-                bool ok = true;
-                for (int q = 0; q < BM / PIECE_ROWS && ok; ++q)
-                    ok = wait_flag(&p.flags[m * (BM / PIECE_ROWS) + q], E, ab, 1);
-                if (!ok) break;
-                fence_proxy_async_global(); // the generic-proxy flag orders the async-proxy reads below
+                if (!wait_block_flags(&p.flags[m * (BM / PIECE_ROWS)], E, ab, 1)) break;
+                fence_proxy_async_global(); // the generic-proxy flags order the async-proxy reads below
             }
             const int row_in_shard = (m * BM) % p.M_r;
             bool ok = true;
@@ -323,10 +356,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 // their own 128 rows of D.  Each CTA waits only on the ready flags of its own
 // 128 A rows; the gather producer runs in every CTA, as in the one-CTA form.
 constexpr int PM = 256, PN = 256, HM = 128, HN = 128;
-constexpr int BK2 = 128;
-constexpr int STAGES2 = 3;
+constexpr int BK2 = RC_GEMM_PAIR_BK;     // K per stage: KSUB2 64-column swizzled sub-tiles
+constexpr int KSUB2 = BK2 / 64;
+constexpr int STAGES2 = RC_GEMM_PAIR_STAGES;
 constexpr int A2_SUB = HM * 64 * 2, B2_SUB = HN * 64 * 2;   // 16 KiB K sub-tiles
-constexpr int A2_STAGE = 2 * A2_SUB, B2_STAGE = 2 * B2_SUB;  // 32 KiB
+constexpr int A2_STAGE = KSUB2 * A2_SUB, B2_STAGE = KSUB2 * B2_SUB;
 constexpr int SMEM2_BYTES = STAGES2 * (A2_STAGE + B2_STAGE) + 2 * STAGING + 1024 + 256;
 constexpr uint32_t kIdesc2 = idesc_bf16_f32(PM, PN);
 
@@ -404,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (a_producer || b_producer) {
         // ---------------- TMA producer (both CTAs): this CTA's halves of A and B
         uint32_t stage = 0, phase = 0;
-        int issued[STAGES2] = {0, 0, 0};
+        int issued[STAGES2] = {};
         for (int t = pair; t < p.total_tiles && !*(volatile int *)abort_flag; t += npairs) {
             int m, n;
             tile_of(p, t, m, n);
@@ -412,11 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int src_rank = row0 / p.M_r;
             const bool own = src_rank == p.rank;
             if (!own && a_producer) {
-                const int mb = row0 / BM;
-                bool ok = true;
-                for (int q = 0; q < BM / PIECE_ROWS && ok; ++q)
-                    ok = wait_flag(&p.flags[mb * (BM / PIECE_ROWS) + q], E, ab, 1);
-                if (!ok) break;
+                if (!wait_block_flags(&p.flags[(row0 / BM) * (BM / PIECE_ROWS)], E, ab, 1)) break;
                 fence_proxy_async_global();
             }
             const int row_in_shard = row0 % p.M_r;
@@ -429,13 +459,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (a_producer) {
                     if (even) mbar_expect_tx(full_bar + 8 * stage, 2 * (A2_STAGE + B2_STAGE));
                     if (own)
-                        tma_load_4d_pair(sA + stage * A2_STAGE, &map_sh, 0, row_in_shard, kb * 2, src_rank,
+                        tma_load_4d_pair(sA + stage * A2_STAGE, &map_sh, 0, row_in_shard, kb * KSUB2, src_rank,
                                          full_even + 8 * stage);
                     else
-                        tma_load_3d_pair(sA + stage * A2_STAGE, &map_ag, 0, row0, kb * 2, full_even + 8 * stage);
+                        tma_load_3d_pair(sA + stage * A2_STAGE, &map_ag, 0, row0, kb * KSUB2, full_even + 8 * stage);
                 }
                 if (b_producer)
-                    tma_load_3d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * 2,
+                    tma_load_3d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * KSUB2,
                                      full_even + 8 * stage);
                 issued[stage]++;
                 if (++stage == STAGES2) {
@@ -624,7 +654,7 @@ static int make_map_k2(CUtensorMap *map, const void *ptr, int rank, const cuuint
 {
     auto fn = encode_fn();
     if (!fn) return set_error(RC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
-    cuuint32_t box[4] = {64, box_rows, 2, 1};
+    cuuint32_t box[4] = {64, box_rows, (cuuint32_t)KSUB2, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

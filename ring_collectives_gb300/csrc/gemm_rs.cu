@@ -28,6 +28,7 @@
 #include <cstdlib>
 #include <mutex>
 
+#include "gemm_cfg.h"
 #include "tc.cuh"
 
 namespace rc {
@@ -236,29 +237,45 @@ __global__ void __launch_bounds__(THREADS, 1)
 // tcgen05.mma.cta_group::2 (M=256, N=256, K=16), which reads both CTAs'
 // halves and leaves each CTA's 128 rows of D in its own TMEM.
 // Operand staging is sized to the tile loader (TMA): measured on GB300, one
-// SM's tiled loads top out near 70 bytes per clock, and a request of 16 KiB
-// costs as long as one of 32 KiB.  So a stage is K=128 deep and each operand
-// half arrives as one 32 KiB request (a box of two 64-column K blocks of 128
-// rows): 64 KiB per CTA per 1024 MMA clocks, under that ceiling, where the
-// one-CTA 128x256 tile needs 94 bytes per clock.
-//   even CTA: warp 0 producer (arms the stage's full barrier for the bytes of
-//             both CTAs), warp 1 MMA issuer, warps 4-7 epilogue.
-//   odd CTA:  warp 0 producer (its loads complete on the even CTA's full
-//             barrier), warps 4-7 epilogue (arrive on the even CTA's
+// SM's tiled loads top out near 70 bytes per clock.  A stage is K=128 deep by
+// default (gemm_cfg.h) and each operand half arrives as one 32 KiB request (a
+// box of two 64-column K blocks of 128 rows): 64 KiB per CTA per 1024 MMA
+// clocks, under that ceiling, where the one-CTA 128x256 tile needs 94 bytes
+// per clock.  With P=1 this kernel is a plain GEMM: 8192x4096x4096 bf16 runs
+// in 0.154 ms on GB300, 91 % of cuBLAS on the same shape.
+//   even CTA: warp 0 A producer (arms the stage's full barrier for the bytes
+//             of both CTAs), warp 3 B producer, warp 1 MMA issuer, warps 4..
+//             epilogue.
+//   odd CTA:  warps 0 and 3 producers (their loads complete on the even CTA's
+//             full barrier), warps 4.. epilogue (arrive on the even CTA's
 //             accumulator-empty barrier).
 // Both CTAs allocate TMEM together (.cta_group::2) and meet at cluster
 // barriers after set-up and before freeing TMEM.
 constexpr int PM = 256;                 // pair tile rows
 constexpr int PN = 256;                 // pair tile columns
 constexpr int HM = 128, HN = 128;       // per-CTA halves of A rows and B rows
-constexpr int BK2 = 128;                // K per stage: two 64-column swizzled sub-tiles
-constexpr int STAGES2 = 3;
+constexpr int BK2 = RC_GEMM_PAIR_BK;    // K per stage: KSUB2 64-column swizzled sub-tiles
+constexpr int KSUB2 = BK2 / 64;
+constexpr int STAGES2 = RC_GEMM_PAIR_STAGES;
 constexpr int A2_SUB = HM * 64 * 2;     // 16 KiB: one K sub-tile of the A half
 constexpr int B2_SUB = HN * 64 * 2;
-constexpr int A2_STAGE = 2 * A2_SUB;    // 32 KiB
-constexpr int B2_STAGE = 2 * B2_SUB;    // 32 KiB
+constexpr int A2_STAGE = KSUB2 * A2_SUB;
+constexpr int B2_STAGE = KSUB2 * B2_SUB;
 constexpr int SMEM2_BYTES = STAGES2 * (A2_STAGE + B2_STAGE) + 1024 + 256;
 constexpr uint32_t kIdesc2 = idesc_bf16_f32(PM, PN);
+// Epilogue warps of the pair kernel: 4 (one per TMEM lane quadrant, all 256
+// columns each) or 8 (two per quadrant, 128 columns each).  Every partial
+// product of a tile must be folded before the MMA warp needs its accumulator
+// again, i.e. within the 32 K=16 MMAs of one partial (K=512 per rank).
+// Measured on GB300 (P=8, 8192x4096x512 per rank): 4 warps 0.1779 ms,
+// 8 warps 0.1776-0.1789 ms -- the fold keeps up with 4.
+#ifndef RC_GRS_EPI_WARPS
+#define RC_GRS_EPI_WARPS 4
+#endif
+constexpr int EPI2 = RC_GRS_EPI_WARPS;
+static_assert(EPI2 == 4 || EPI2 == 8, "one or two epilogue warps per TMEM lane quadrant");
+constexpr int THREADS2 = 128 + 32 * EPI2;
+constexpr int CW2 = PN / (EPI2 / 4);     // accumulator columns per epilogue warp
 // 1: the last partial's fold stores each finished 32-column group at once
 // (measured on GB300: 0.1757-0.1771 ms vs 0.1786-0.1788 ms storing the tile
 // after the fold).
@@ -266,7 +283,7 @@ constexpr uint32_t kIdesc2 = idesc_bf16_f32(PM, PN);
 #define RC_GRS_STORE_IN_FOLD 1
 #endif
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
     k_gemm_rs2(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -293,7 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar + 8 * a, 1);
-            mbar_init(tempty_bar + 8 * a, 8);    // four epilogue warps of each CTA
+            mbar_init(tempty_bar + 8 * a, 2 * EPI2);   // every epilogue warp of both CTAs
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -333,7 +350,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (a_producer || b_producer) {
         // ---------------- TMA producer (both CTAs)
         uint32_t stage = 0, phase = 0;
-        int issued[STAGES2] = {0, 0, 0};
+        int issued[STAGES2] = {};
         bool ok = true;
         for (int t = pair; t < p.total_tiles && ok; t += npairs) {
             const int m = t / p.n_tiles, n = t % p.n_tiles;
@@ -347,11 +364,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     }
                     if (a_producer) {
                         if (even) mbar_expect_tx(full_bar + 8 * stage, 2 * (A2_STAGE + B2_STAGE));
-                        tma_load_4d_pair(sA + stage * A2_STAGE, &map_a, 0, m * PM + (int)cta * HM, kb * 2, r,
+                        tma_load_4d_pair(sA + stage * A2_STAGE, &map_a, 0, m * PM + (int)cta * HM, kb * KSUB2, r,
                                          full_even + 8 * stage);
                     }
                     if (b_producer)
-                        tma_load_4d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * 2, r,
+                        tma_load_4d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * KSUB2, r,
                                          full_even + 8 * stage);
                     issued[stage]++;
                     if (++stage == STAGES2) {
@@ -409,17 +426,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tc_commit_pair_mc(drain_bar, 1);
         wait_bar(drain_bar, 0, ab, 10, true);
     } else if (warp >= 4) {
-        // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair tile
-        const int q = warp - 4;
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair tile.
+        // Warp 4+e reads TMEM lane quadrant e % 4 (a warp may only access the
+        // 32 lanes of its own warp index modulo 4) and columns [c0, c0 + CW2).
+        const int e = warp - 4;
+        const int q = e & 3;
+        const int c0 = (e >> 2) * CW2;
         int it = 0;
         bool ok = true;
         for (int t = pair; t < p.total_tiles && ok; t += npairs) {
             const int m = t / p.n_tiles, n = t % p.n_tiles;
             const int k = (n * PN) / p.n_chunk;
             const size_t row = (size_t)m * PM + cta * HM + q * 32 + lane;
-            const size_t col = (size_t)n * PN - (size_t)k * p.n_chunk;
+            const size_t col = (size_t)n * PN - (size_t)k * p.n_chunk + (size_t)c0;
             char *dst = p.out + (size_t)k * p.out_stride + (row * (size_t)p.n_chunk + col) * 2;
-            uint32_t acc[PN / 2];
+            uint32_t acc[CW2 / 2];
             for (int jj = 1; jj <= P; ++jj, ++it) {
                 const uint32_t buf = it & 1;
                 const uint32_t buf_phase = (it >> 1) & 1;
@@ -434,11 +455,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 // The last partial's fold stores each finished 32-column group at once
                 // (RC_GRS_STORE_IN_FOLD), so the tile's stores overlap its TMEM loads.
                 const bool last = RC_GRS_STORE_IN_FOLD && jj == P;
-                const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + buf * PN;
+                const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + buf * PN + (uint32_t)c0;
                 uint32_t va[32], vb[32];
                 tmem_ld32_async(trow, va);
 #pragma unroll
-                for (int cc = 0; cc < PN / 32; cc += 2) {
+                for (int cc = 0; cc < CW2 / 32; cc += 2) {
                     tmem_wait_ld32(va);
                     tmem_ld32_async(trow + (cc + 1) * 32, vb);
 #pragma unroll
@@ -453,7 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                                                                      acc[cc * 16 + 4 * w + 2], acc[cc * 16 + 4 * w + 3]));
                     }
                     tmem_wait_ld32(vb);
-                    if (cc + 2 < PN / 32) tmem_ld32_async(trow + (cc + 2) * 32, va);
+                    if (cc + 2 < CW2 / 32) tmem_ld32_async(trow + (cc + 2) * 32, va);
 #pragma unroll
                     for (int w = 0; w < 16; ++w) {
                         const uint32_t c = pack_bf16x2(vb[2 * w], vb[2 * w + 1]);
@@ -479,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if (!ok) break;
             if (!RC_GRS_STORE_IN_FOLD) {
 #pragma unroll
-                for (int w = 0; w < PN / 8; ++w)
+                for (int w = 0; w < CW2 / 8; ++w)
                     st_v4(dst + w * 16, make_uint4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]));
             }
         }
@@ -545,7 +566,7 @@ static int make_map4(CUtensorMap *map, const void *ptr, size_t K, size_t rows, i
     if (!fn) return set_error(RC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)K / 64, (cuuint64_t)P};
     cuuint64_t strides[3] = {(cuuint64_t)K * 2, 128, (cuuint64_t)rank_stride};
-    cuuint32_t box[4] = {64, box_rows, 2, 1};
+    cuuint32_t box[4] = {64, box_rows, (cuuint32_t)KSUB2, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -621,7 +642,7 @@ extern "C" int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_s
         p.total_tiles = p.m_tiles * p.n_tiles;
         int clusters = sm_count / 2;
         if (clusters > p.total_tiles) clusters = p.total_tiles;
-        k_gemm_rs2<<<2 * clusters, THREADS, SMEM2_BYTES, (cudaStream_t)stream>>>(map_a, map_b, p);
+        k_gemm_rs2<<<2 * clusters, THREADS2, SMEM2_BYTES, (cudaStream_t)stream>>>(map_a, map_b, p);
     } else {
         p.m_tiles = M / BM;
         p.n_tiles = N / BN;
