@@ -62,12 +62,31 @@ struct Params {
     int P, rank, M_r, N, K;
     int total_m, tiles_per_pe, n_tiles, total_tiles, units;  // tile schedule (tile rows: BM, or PM for pairs)
     int g_total_m, g_per_pe;   // gather schedule, in 128-row blocks (8 units of 16 rows each)
+    int st32;                  // 1: rows of C start on 32-byte boundaries (full-sector stores)
     unsigned long long timeout_ns;
 };
 
 // ------------------------------------------------------------ PTX wrappers (tc.cuh)
 using namespace tc;
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+
+// Stores the 32 columns of one TMEM load (fp32, rounded to bf16) of this
+// lane's row of C.  Each lane owns a row, so a warp's store touches 32 rows;
+// 32-byte stores fill whole sectors (measured on GB300: the 16-byte form
+// costs the epilogue about twice the store time).
+__device__ __forceinline__ void store_row32(char *dst, const uint32_t (&v)[32], bool st32)
+{
+    uint32_t b[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) b[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    if (st32) {
+        st8<kStNormal>(dst, make_uint4(b[0], b[1], b[2], b[3]), make_uint4(b[4], b[5], b[6], b[7]));
+        st8<kStNormal>(dst + 32, make_uint4(b[8], b[9], b[10], b[11]), make_uint4(b[12], b[13], b[14], b[15]));
+    } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) st_v4(dst + w * 16, make_uint4(b[4 * w], b[4 * w + 1], b[4 * w + 2], b[4 * w + 3]));
+    }
+}
 
 // ------------------------------------------------------------ tile order
 // Tile t of the persistent schedule -> (m block, n block).  Raw M order is
@@ -314,17 +333,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int cc = 0; cc < BN / 32; ++cc) {
                 uint32_t v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + cc * 32, v);
-                uint4 o[4];
-                o[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                  pack_bf16x2(v[6], v[7]));
-                o[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
-                                  pack_bf16x2(v[14], v[15]));
-                o[2] = make_uint4(pack_bf16x2(v[16], v[17]), pack_bf16x2(v[18], v[19]),
-                                  pack_bf16x2(v[20], v[21]), pack_bf16x2(v[22], v[23]));
-                o[3] = make_uint4(pack_bf16x2(v[24], v[25]), pack_bf16x2(v[26], v[27]),
-                                  pack_bf16x2(v[28], v[29]), pack_bf16x2(v[30], v[31]));
-#pragma unroll
-                for (int w = 0; w < 4; ++w) st_v4(crow + cc * 64 + w * 16, o[w]);
+                store_row32(crow + cc * 64, v, p.st32);
             }
             tc_fence_before();
             __syncwarp();
@@ -572,20 +581,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             for (int cc = 0; cc < PN / 32; cc += 2) {
                 tmem_wait_ld32(va);
                 tmem_ld32_async(trow + (cc + 1) * 32, vb);
-#pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    st_v4(crow + cc * 64 + w * 16,
-                          make_uint4(pack_bf16x2(va[8 * w], va[8 * w + 1]), pack_bf16x2(va[8 * w + 2], va[8 * w + 3]),
-                                     pack_bf16x2(va[8 * w + 4], va[8 * w + 5]),
-                                     pack_bf16x2(va[8 * w + 6], va[8 * w + 7])));
+                store_row32(crow + cc * 64, va, p.st32);
                 tmem_wait_ld32(vb);
                 if (cc + 2 < PN / 32) tmem_ld32_async(trow + (cc + 2) * 32, va);
-#pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    st_v4(crow + (cc + 1) * 64 + w * 16,
-                          make_uint4(pack_bf16x2(vb[8 * w], vb[8 * w + 1]), pack_bf16x2(vb[8 * w + 2], vb[8 * w + 3]),
-                                     pack_bf16x2(vb[8 * w + 4], vb[8 * w + 5]),
-                                     pack_bf16x2(vb[8 * w + 6], vb[8 * w + 7])));
+                store_row32(crow + (cc + 1) * 64, vb, p.st32);
             }
             tc_fence_before();
             __syncwarp();
@@ -720,6 +719,7 @@ extern "C" int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, 
     p.g_total_m = (int)(M / BM);
     p.g_per_pe = M_r / BM;
     p.units = p.g_total_m * (BM / PIECE_ROWS);
+    p.st32 = (((uintptr_t)C | (size_t)N * 2) & 31u) == 0;
     int sm_count = 0;
     int rc_ = prepare_workspace((size_t)p.units, &p.hdr, &p.flags, &sm_count, &p.timeout_ns);
     if (rc_) return rc_;

@@ -66,6 +66,7 @@ struct Params {
     int P, M, N, K;          // K: per-rank inner dimension
     int n_chunk;             // N / P columns per rank
     int m_tiles, n_tiles, total_tiles;
+    int st32;                // 1: output rows start on 32-byte boundaries (full-sector stores)
     unsigned long long timeout_ns;
 };
 
@@ -232,9 +233,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             const size_t row = (size_t)m * BM + q * 32 + lane;
             const size_t col = (size_t)n * BN - (size_t)k * p.n_chunk;   // column inside chunk k
             char *dst = p.out + (size_t)k * p.out_stride + (row * (size_t)p.n_chunk + col) * 2;
+            if (p.st32) {
 #pragma unroll
-            for (int w = 0; w < BN / 8; ++w)
-                st_v4(dst + w * 16, make_uint4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]));
+                for (int w = 0; w < BN / 16; ++w)   // one full 32-byte sector per lane and store
+                    st8<kStNormal>(dst + w * 32, make_uint4(acc[8 * w], acc[8 * w + 1], acc[8 * w + 2], acc[8 * w + 3]),
+                                   make_uint4(acc[8 * w + 4], acc[8 * w + 5], acc[8 * w + 6], acc[8 * w + 7]));
+            } else {
+#pragma unroll
+                for (int w = 0; w < BN / 8; ++w)
+                    st_v4(dst + w * 16, make_uint4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]));
+            }
         }
     }
 
@@ -483,11 +491,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
                         const uint32_t c = pack_bf16x2(va[2 * w], va[2 * w + 1]);
                         acc[cc * 16 + w] = jj == 1 ? c : fold_add_bf16x2(acc[cc * 16 + w], c);
                     }
-                    if (last) {
+                    if (last && p.st32) {
+#pragma unroll
+                        for (int w = 0; w < 2; ++w)   // one full 32-byte sector per lane and store
+                            st8<kStNormal>(dst + cc * 64 + w * 32,
+                                           make_uint4(acc[cc * 16 + 8 * w], acc[cc * 16 + 8 * w + 1],
+                                                      acc[cc * 16 + 8 * w + 2], acc[cc * 16 + 8 * w + 3]),
+                                           make_uint4(acc[cc * 16 + 8 * w + 4], acc[cc * 16 + 8 * w + 5],
+                                                      acc[cc * 16 + 8 * w + 6], acc[cc * 16 + 8 * w + 7]));
+                    } else if (last) {
 #pragma unroll
                         for (int w = 0; w < 4; ++w)
-                            st_v4(dst + cc * 64 + w * 16, make_uint4(acc[cc * 16 + 4 * w], acc[cc * 16 + 4 * w + 1],
-                                                                     acc[cc * 16 + 4 * w + 2], acc[cc * 16 + 4 * w + 3]));
+                            st_v4(dst + cc * 64 + w * 16,
+                                  make_uint4(acc[cc * 16 + 4 * w], acc[cc * 16 + 4 * w + 1],
+                                             acc[cc * 16 + 4 * w + 2], acc[cc * 16 + 4 * w + 3]));
                     }
                     tmem_wait_ld32(vb);
                     if (cc + 2 < CW2 / 32) tmem_ld32_async(trow + (cc + 2) * 32, va);
@@ -496,7 +513,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
                         const uint32_t c = pack_bf16x2(vb[2 * w], vb[2 * w + 1]);
                         acc[(cc + 1) * 16 + w] = jj == 1 ? c : fold_add_bf16x2(acc[(cc + 1) * 16 + w], c);
                     }
-                    if (last) {
+                    if (last && p.st32) {
+#pragma unroll
+                        for (int w = 0; w < 2; ++w)   // one full 32-byte sector per lane and store
+                            st8<kStNormal>(dst + (cc + 1) * 64 + w * 32,
+                                           make_uint4(acc[(cc + 1) * 16 + 8 * w], acc[(cc + 1) * 16 + 8 * w + 1],
+                                                      acc[(cc + 1) * 16 + 8 * w + 2], acc[(cc + 1) * 16 + 8 * w + 3]),
+                                           make_uint4(acc[(cc + 1) * 16 + 8 * w + 4], acc[(cc + 1) * 16 + 8 * w + 5],
+                                                      acc[(cc + 1) * 16 + 8 * w + 6], acc[(cc + 1) * 16 + 8 * w + 7]));
+                    } else if (last) {
 #pragma unroll
                         for (int w = 0; w < 4; ++w)
                             st_v4(dst + (cc + 1) * 64 + w * 16,
@@ -514,7 +539,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
                 }
             }
             if (!ok) break;
-            if (!RC_GRS_STORE_IN_FOLD) {
+            if (!RC_GRS_STORE_IN_FOLD && p.st32) {
+#pragma unroll
+                for (int w = 0; w < CW2 / 16; ++w)
+                    st8<kStNormal>(dst + w * 32, make_uint4(acc[8 * w], acc[8 * w + 1], acc[8 * w + 2], acc[8 * w + 3]),
+                                   make_uint4(acc[8 * w + 4], acc[8 * w + 5], acc[8 * w + 6], acc[8 * w + 7]));
+            } else if (!RC_GRS_STORE_IN_FOLD) {
 #pragma unroll
                 for (int w = 0; w < CW2 / 8; ++w)
                     st_v4(dst + w * 16, make_uint4(acc[4 * w], acc[4 * w + 1], acc[4 * w + 2], acc[4 * w + 3]));
@@ -629,6 +659,7 @@ extern "C" int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_s
     p.N = N;
     p.K = K;
     p.n_chunk = (int)n_chunk;
+    p.st32 = (((uintptr_t)out | p.out_stride | n_chunk * 2) & 31u) == 0;
     int sm_count = 0;
     uint32_t *unused = nullptr;
     int rc_ = prepare_workspace(0, &p.hdr, &unused, &sm_count, &p.timeout_ns);

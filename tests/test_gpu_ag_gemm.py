@@ -88,6 +88,23 @@ def test_ag_gemm_full_size_sampled():
     check_c(A_bits, synthetic.bf16_bits(b), Cb[np.ix_(rows, cols)], rows, cols)
 
 
+@pytest.mark.parametrize("P,M_r,K,N,rank", [(2, 256, 1024, 512, 1), (4, 128, 256, 256, 2)])
+def test_ag_gemm_output_16_byte_aligned(P, M_r, K, N, rank):
+    """C starting 16 bytes past a 32-byte boundary takes the 16-byte store
+    path (the full-sector stores need 32-byte rows): same bits as an aligned C
+    (the pair form and the one-CTA form)."""
+    a, b, ag, C = run(P, M_r, K, N, rank)
+    buf = torch.full((P * M_r * N + 8,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    C2 = buf[8:].view(P * M_r, N)
+    assert C2.data_ptr() % 32 == 16
+    ag2 = torch.full_like(ag, float("nan"))
+    rc.ag_gemm(a.to(DEV), ag2, b.to(DEV), C2, rank)
+    assert rc.ring_status() == 0, rc.ring_last_error()
+    assert torch.equal(ag2, ag)
+    assert np.array_equal(bits(C2), bits(C))
+    assert torch.isnan(buf[:8]).all(), "a store landed before C"
+
+
 def test_ag_gemm_repeated_calls_and_ranks():
     """Ready flags are epoch-valued: repeated launches and different ranks reuse them."""
     P, M_r, K, N = 4, 256, 512, 256

@@ -99,6 +99,25 @@ def test_gemm_rs_full_size_sampled_rows():
     check(8, 8192, 4096, 512, seed=11, rows=rows)
 
 
+@pytest.mark.parametrize("P,M,N,K", [(2, 512, 512, 128), (3, 128, 768, 256)])
+def test_gemm_rs_output_16_byte_aligned(P, M, N, K):
+    """An output that starts 16 bytes past a 32-byte boundary takes the
+    16-byte store path (the full-sector stores need 32-byte rows); both give
+    the same bits (the pair form and the one-CTA form)."""
+    a, b = inputs(P, M, N, K, seed=13)
+    ad, bd = a.to(DEV), b.to(DEV)
+    nc = N // P
+    out = torch.full((P, M, nc), float("nan"), dtype=torch.bfloat16, device=DEV)
+    rc.gemm_rs(ad, bd, out)
+    buf = torch.full((P * M * nc + 8,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    shifted = buf[8:].view(P, M, nc)
+    assert shifted.data_ptr() % 32 == 16
+    rc.gemm_rs(ad, bd, shifted)
+    assert rc.ring_status() == 0, rc.ring_last_error()
+    assert np.array_equal(bits(shifted), bits(out))
+    assert torch.isnan(buf[:8]).all(), "a store landed before the output"
+
+
 def test_gemm_rs_rejects_bad_shapes():
     a = torch.zeros((2, 128, 64), dtype=torch.bfloat16, device=DEV)
     b = torch.zeros((2, 200, 64), dtype=torch.bfloat16, device=DEV)
