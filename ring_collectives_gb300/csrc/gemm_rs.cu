@@ -50,6 +50,17 @@ __device__ __forceinline__ uint32_t fold_add_bf16x2(uint32_t a, uint32_t b)
     return r;
 }
 
+// The odd CTA's epilogue tells the even CTA's MMA warp that it has read its
+// half of an accumulator.  Those TMEM loads have completed (tcgen05.wait::ld)
+// before the arrival and the arrival publishes nothing else, so it needs no
+// release semantics: a relaxed arrival at cluster scope.  Measured on GB300
+// (P=8, 8192x4096x512 per rank, an accumulator handed back every K=512):
+// 0.1627-0.1630 ms with a release arrival, 0.1555-0.1560 ms relaxed.
+__device__ __forceinline__ void arrive_remote_relaxed(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
 constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;   // 16 KiB
@@ -535,7 +546,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
                     if (even)
                         mbar_arrive(tempty_bar + 8 * buf);
                     else
-                        mbar_arrive_remote(tempty_even + 8 * buf);
+                        arrive_remote_relaxed(tempty_even + 8 * buf);
                 }
             }
             if (!ok) break;
