@@ -416,6 +416,29 @@ def cublas_same_shape(A, Bt, stream, args):
             "shape": f"{A.shape[0]}x{Bt.shape[0]}x{A.shape[1]}", "call": "torch.matmul (cuBLAS), bf16"}
 
 
+def plain_gemm_same_kernel(rc, A, Bt, stream, args):
+    """Context for the tensor-core rows: the library's own CTA-pair GEMM
+    (gemm_rs with P=1, i.e. C = A.B^T with no reduction) on the same M, N and
+    total K, timed like the row."""
+    a1, b1 = A.reshape(1, *A.shape), Bt.reshape(1, *Bt.shape)
+    out = torch.empty((1, A.shape[0], Bt.shape[0]), dtype=torch.bfloat16, device=A.device)
+    for _ in range(max(args.warmup, 3)):
+        rc.gemm_rs(a1, b1, out, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for x, y in ev:
+        x.record(stream)
+        rc.gemm_rs(a1, b1, out, stream=stream)
+        y.record(stream)
+    torch.cuda.synchronize()
+    if rc.ring_status(stream) != 0:
+        raise RuntimeError(rc.ring_last_error())
+    ms = statistics.mean(x.elapsed_time(y) for x, y in ev)
+    flop = 2 * A.shape[0] * Bt.shape[0] * A.shape[1]
+    return {"ms": round(ms, 4), "TFLOP/s": round(flop / (ms * 1e-3) / 1e12, 1),
+            "shape": f"{A.shape[0]}x{Bt.shape[0]}x{A.shape[1]}", "call": "gemm_rs with P=1 (k_gemm_rs2)"}
+
+
 def ag_gemm_secondary(rc, dev, stream, args):
     """All-gather + GEMM at P=8, shards [1024,4096], B [4096,4096] bf16 (tensor-bound)."""
     P, M_r, K, N = 8, 1024, 4096, 4096
@@ -439,10 +462,13 @@ def ag_gemm_secondary(rc, dev, stream, args):
     peak, kind = bf16_peak()
     tf = flop / (ms * 1e-3) / 1e12
     cb = cublas_same_shape(ag, bd, stream, args)
+    own = plain_gemm_same_kernel(rc, ag, bd, stream, args)
+    own["frac_of_cublas_same_shape"] = round(own["TFLOP/s"] / cb["TFLOP/s"], 4)
     return {"ag_gemm_p8_8192x4096x4096": {
         "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peak, 4),
         "peak": peak, "peak_kind": kind, "flop_per_call": flop,
         "cublas_same_shape": cb, "frac_of_cublas_same_shape": round(tf / cb["TFLOP/s"], 4),
+        "plain_gemm_same_kernel": own,
         "note": "gather of the 8 shards (64 MiB) + C = A_g.B^T, one tcgen05 launch"}}
 
 
@@ -503,12 +529,16 @@ def gemm_rs_secondary(rc, dev, stream, args):
     peak, kind = bf16_peak()
     tf = flop / (ms * 1e-3) / 1e12
     # the same flops as one GEMM: sum_q A_q.B_q^T = [A_0 .. A_7] . [B_0 .. B_7]^T (K = P*512)
-    cb = cublas_same_shape(ad.permute(1, 0, 2).reshape(M, P * K).contiguous(),
-                           bd.permute(1, 0, 2).reshape(N, P * K).contiguous(), stream, args)
+    a_cat = ad.permute(1, 0, 2).reshape(M, P * K).contiguous()
+    b_cat = bd.permute(1, 0, 2).reshape(N, P * K).contiguous()
+    cb = cublas_same_shape(a_cat, b_cat, stream, args)
+    own = plain_gemm_same_kernel(rc, a_cat, b_cat, stream, args)
+    own["frac_of_cublas_same_shape"] = round(own["TFLOP/s"] / cb["TFLOP/s"], 4)
     return {"gemm_rs_p8_8192x4096x512": {
         "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peak, 4), "peak": peak,
         "peak_kind": kind, "flop_per_call": flop,
         "cublas_same_shape": cb, "frac_of_cublas_same_shape": round(tf / cb["TFLOP/s"], 4),
+        "plain_gemm_same_kernel": own,
         "note": "8 partial products folded in ring order in the epilogue; output [8,8192,512] bf16"}}
 
 
@@ -708,6 +738,7 @@ def run_ag_gemm(args, rank, world, dist):
                      "algorithmic_flop_per_launch": flop, "kernel": kern},
         "cublas_same_shape": res["cublas_same_shape"],
         "frac_of_cublas_same_shape": res["frac_of_cublas_same_shape"],
+        "plain_gemm_same_kernel": res["plain_gemm_same_kernel"],
         "gpu_launches": args.steps, "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
