@@ -58,6 +58,39 @@ size_t l2_live_bytes()
     }();
     return v;
 }
+// Phase-shifted slice rings.  The first step of a reduce-scatter reads two
+// chunks from HBM per rank and is bound by HBM, while the later steps move
+// data that is mostly in L2 and are bound by L2; when every slice ring runs
+// in step, all of them are in the HBM-bound step at once.  Slice j therefore
+// starts (j % G) * D later, G groups and D a fifth of the first step's time
+// at ~6.5 TB/s (its HBM bytes / 32500 ns per byte, capped at 50 us), so the
+// groups' first steps overlap the others' L2-bound steps.  Measured on GB300
+// (P=8 x 64 MiB fp32 all-reduce, D = 4.1 us): G=1 0.2155-0.2173 ms, G=2
+// 0.2134-0.2143, G=3 0.2113-0.2119.  Only the all-reduce uses it: the
+// standalone reduce-scatter has no all-gather phase to absorb the later
+// groups' tail (0.1389-0.1394 -> 0.1407-0.1408 ms at P=8 x 64 MiB bf16), and
+// the all-gather and bidirectional reduce-scatter measured no change.  Knob,
+// read once: RC_RING_STAGGER = G (1 = off; unset or malformed = 3).
+int stagger_groups_default()
+{
+    static const int v = [] {
+        const char *e = getenv("RC_RING_STAGGER");
+        if (!e || !*e) return 3;
+        char *end = nullptr;
+        const long x = strtol(e, &end, 10);
+        return (end && *end == 0 && x >= 1 && x <= 16) ? (int)x : 3;
+    }();
+    return v;
+}
+
+void set_stagger(rc::RingParams &p, size_t es)
+{
+    p.stagger_groups = p.mode == rc::MODE_ALLREDUCE ? stagger_groups_default() : 1;
+    const double first_step_bytes = 2.0 * p.P * ((double)p.chunk / (double)p.segments) * (double)es;
+    const double ns = first_step_bytes / 32500.0;
+    p.stagger_ns = p.stagger_groups > 1 ? (unsigned)(ns < 50000.0 ? ns : 50000.0) : 0u;
+}
+
 // Tuning knob, read once from the environment: RC_AG_BULK (1 = all-gather
 // copies with bulk copies through shared memory, 0 = 32-byte vector loads
 // and stores; unset or malformed = the default).
@@ -248,6 +281,7 @@ int plan_ring(rc::RingParams &p, int dtype, DeviceState *st)
     }
     p.ag_bulk = ag_bulk_default();
     if (p.chunk_stride == 0) p.chunk_stride = p.chunk;
+    set_stagger(p, es);
     return rc_;
 }
 
@@ -822,6 +856,7 @@ int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int 
     p.chunk_stride = c;
     p.ag_bulk = ag_bulk_default();
     p.debug_serial = debug_serial();
+    set_stagger(p, elem_size(dtype));
     cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, s);
     if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
     na.launches++;

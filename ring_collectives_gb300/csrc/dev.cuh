@@ -146,7 +146,13 @@ __device__ __forceinline__ void discard_l2_line(const void *p)
 // f32: IEEE binary32 add, round to nearest even, subnormals kept (the library
 //      is built without fast math / flush-to-zero).
 // bf16: both operands widened to binary32 (exact), added in binary32, the sum
-//      rounded to bf16 to nearest even by the hardware conversion.
+//      rounded to bf16 to nearest even.  Computed as one add.rn.bf16x2 (the
+//      exact sum rounded once to bf16), which gives the same bits for every
+//      pair of bf16 operands: whenever the binary32 sum is inexact, the
+//      exponents differ by more than 16, the smaller operand lies below a
+//      quarter of the larger's bf16 spacing, and both forms return the
+//      larger operand.  Compared on GB300 for all 2^32 operand pairs: equal
+//      except NaN payloads (both results are NaN for the same pairs).
 // i32: two's-complement wrapping add.
 __device__ __forceinline__ uint32_t add_f32_bits(uint32_t a, uint32_t b)
 {
@@ -156,12 +162,8 @@ __device__ __forceinline__ uint32_t add_f32_bits(uint32_t a, uint32_t b)
 // Two packed bf16 (low half = element 0) -> two packed bf16 sums.
 __device__ __forceinline__ uint32_t add_bf16x2_bits(uint32_t a, uint32_t b)
 {
-    const float alo = __uint_as_float(a << 16), ahi = __uint_as_float(a & 0xFFFF0000u);
-    const float blo = __uint_as_float(b << 16), bhi = __uint_as_float(b & 0xFFFF0000u);
-    const float slo = __fadd_rn(alo, blo), shi = __fadd_rn(ahi, bhi);
     uint32_t r;
-    // cvt packs its first source into the upper half, the second into the lower.
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(shi), "f"(slo));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 

@@ -36,20 +36,6 @@ namespace grs {
 
 using namespace tc;
 
-// The fold's hop add on two packed bf16 in one instruction.  For bf16
-// operands the exact sum rounded once to bf16 (add.rn.bf16x2) equals the hop
-// add as defined (widen to binary32, add, round to bf16): whenever the
-// binary32 sum is inexact the exponents differ by more than 16, the smaller
-// operand is below a quarter of the larger's bf16 spacing, and both give the
-// larger operand.  Compared on GB300 for all 2^32 operand pairs: identical
-// bits except NaN payloads (the two results are NaN for the same pairs).
-__device__ __forceinline__ uint32_t fold_add_bf16x2(uint32_t a, uint32_t b)
-{
-    uint32_t r;
-    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
 // The odd CTA's epilogue tells the even CTA's MMA warp that it has read its
 // half of an accumulator.  Those TMEM loads have completed (tcgen05.wait::ld)
 // before the arrival and the arrival publishes nothing else, so it needs no
@@ -233,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int w = 0; w < 16; ++w) {
                         const uint32_t c = pack_bf16x2(v[2 * w], v[2 * w + 1]);   // C_r = bf16(partial)
-                        acc[cc * 16 + w] = jj == 1 ? c : fold_add_bf16x2(acc[cc * 16 + w], c);
+                        acc[cc * 16 + w] = jj == 1 ? c : add_bf16x2_bits(acc[cc * 16 + w], c);
                     }
                 }
                 tc_fence_before();
@@ -302,7 +288,7 @@ constexpr uint32_t kIdesc2 = idesc_bf16_f32(PM, PN);
 // again, i.e. within the 32 K=16 MMAs of one partial (K=512 per rank).
 // Measured on GB300 (P=8, 8192x4096x512 per rank): 4 warps 0.1779 ms,
 // 8 warps 0.1776-0.1789 ms with the two-step hop add; 0.1698 vs 0.1697 ms
-// with the one-instruction add (fold_add_bf16x2).
+// with the one-instruction add (add_bf16x2_bits in dev.cuh).
 #ifndef RC_GRS_EPI_WARPS
 #define RC_GRS_EPI_WARPS 4
 #endif
@@ -500,7 +486,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
 #pragma unroll
                     for (int w = 0; w < 16; ++w) {
                         const uint32_t c = pack_bf16x2(va[2 * w], va[2 * w + 1]);
-                        acc[cc * 16 + w] = jj == 1 ? c : fold_add_bf16x2(acc[cc * 16 + w], c);
+                        acc[cc * 16 + w] = jj == 1 ? c : add_bf16x2_bits(acc[cc * 16 + w], c);
                     }
                     if (last && p.st32) {
 #pragma unroll
@@ -522,7 +508,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
 #pragma unroll
                     for (int w = 0; w < 16; ++w) {
                         const uint32_t c = pack_bf16x2(vb[2 * w], vb[2 * w + 1]);
-                        acc[(cc + 1) * 16 + w] = jj == 1 ? c : fold_add_bf16x2(acc[(cc + 1) * 16 + w], c);
+                        acc[(cc + 1) * 16 + w] = jj == 1 ? c : add_bf16x2_bits(acc[(cc + 1) * 16 + w], c);
                     }
                     if (last && p.st32) {
 #pragma unroll

@@ -39,6 +39,8 @@ struct RingParams {
     int segments;        // chunk segments run one after another (keeps a step's live data in L2)
     int ag_bulk;         // 1: all-gather copies move through shared memory with bulk (TMA) copies
     int debug_serial;    // 1: every step also waits for all blocks of the launch (debugging)
+    int stagger_groups;  // > 1: slice j starts (j % stagger_groups) * stagger_ns later (phase-shifted rings)
+    unsigned stagger_ns;
     int skip_rank, skip_step; // test hook: this rank skips its notify after this step (-1: none)
     unsigned long long timeout_ns;
     unsigned long long *trace; // optional step stamps (see ring_debug_set_trace); null: off

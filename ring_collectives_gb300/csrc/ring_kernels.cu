@@ -430,6 +430,16 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                       : nullptr;
     }
     __syncthreads();
+    if (p.stagger_groups > 1) {
+        // Phase-shifted slice rings (RingParams::stagger_*): every block of
+        // slice j, i.e. the whole ring, starts (j % groups) * stagger_ns later.
+        const unsigned g = (unsigned)j % (unsigned)p.stagger_groups;
+        if (g && threadIdx.x == 0) {
+            const uint64_t t0 = global_timer_ns(), d = (uint64_t)g * p.stagger_ns;
+            while (global_timer_ns() - t0 < d) __nanosleep(128);
+        }
+        __syncthreads();
+    }
     const uint32_t E0 = s_epoch0;
     const uint32_t E = E0 + 1u;   // identifies this launch (abort word)
     const size_t c = p.chunk;
