@@ -65,8 +65,9 @@ size_t l2_live_bytes()
 // starts (j % G) * D later, G groups and D a fifth of the first step's time
 // at ~6.5 TB/s (its HBM bytes / 32500 ns per byte, capped at 50 us), so the
 // groups' first steps overlap the others' L2-bound steps.  Measured on GB300
-// (P=8 x 64 MiB fp32 all-reduce, D = 4.1 us): G=1 0.2155-0.2173 ms, G=2
-// 0.2134-0.2143, G=3 0.2113-0.2119.  Only the all-reduce uses it: the
+// (P=8 x 64 MiB fp32 all-reduce, D = 4.1 us): G=1 0.2150-0.2173 ms, G=2
+// 0.2134-0.2143, G=3 0.2110-0.2119, G=4 0.2151-0.2154, G=5 0.2153-0.2160,
+// G=6 0.2194-0.2201 (bf16: G=1 0.2152-0.2154, G=3 0.2123-0.2126).  Only the all-reduce uses it: the
 // standalone reduce-scatter has no all-gather phase to absorb the later
 // groups' tail (0.1389-0.1394 -> 0.1407-0.1408 ms at P=8 x 64 MiB bf16), and
 // the all-gather and bidirectional reduce-scatter measured no change.  Knob,
