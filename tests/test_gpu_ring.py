@@ -441,6 +441,62 @@ def test_serial_debug_mode_child():
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
 
 
+@pytest.mark.parametrize("groups", ["1", "6"])
+def test_stagger_settings_child(groups):
+    """RC_RING_STAGGER only shifts when the all-reduce's slice rings start:
+    off (1) and six groups give the same bits as the default three."""
+    import os
+    import subprocess
+    import sys
+    from tests.conftest import ROOT
+    env = dict(os.environ, RC_RING_STAGGER=groups)
+    r = subprocess.run([sys.executable, "-c", _SEGMENT_CHILD, ROOT], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+def wide_bf16(P, N, seed):
+    """bf16 bit patterns over most of the finite range: random sign, exponent
+    field 0..0xF0 (zeros and subnormals included, no sum of <= 64 values can
+    overflow), random mantissa, plus exact +-0 and values a tie apart."""
+    rng = np.random.default_rng(seed)
+    sign = rng.integers(0, 2, (P, N), dtype=np.uint16) << 15
+    expo = rng.integers(0, 0xF1, (P, N), dtype=np.uint16) << 7
+    mant = rng.integers(0, 128, (P, N), dtype=np.uint16)
+    h = sign | expo | mant
+    h[:, ::17] &= 0x8000                       # +-0
+    h[:, 5::23] = (h[:, 5::23] & 0x807F) | (0x80 << 7)   # exponent 0x80 pairs: near-tie sums
+    h[:, 6::23] = (h[:, 6::23] & 0x8000) | (0x78 << 7) | 0x40   # 2^-8 of the above (a half spacing)
+    return torch.from_numpy(h.view(np.int16)).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("P,c", [(2, 64 * 37 + 5), (5, 64 * 19), (8, 64 * 61 + 3)])
+def test_bf16_wide_range_bit_exact(P, c):
+    """The bf16 hop add is one add.rn.bf16x2 in the kernels and widen/add/round
+    in the oracle: equal for every pair of bf16 operands.  Subnormals, signed
+    zeros, exponent gaps beyond 16 and ties go through the ring all-reduce,
+    both reduce-scatters, the fused all-reduce and psum, bit for bit."""
+    N = P * c
+    x = wide_bf16(P, N, seed=P * 1000 + c)
+    xn = np_of(x)
+    b = x.to(DEV)
+    rc.ring_allreduce(b)
+    o = torch.empty((P, c), dtype=torch.bfloat16, device=DEV)
+    rc.ring_reduce_scatter(x.to(DEV), o)
+    ob = torch.empty((P, c), dtype=torch.bfloat16, device=DEV)
+    rc.ring_reduce_scatter_bidir(x.to(DEV), ob)
+    f = x.to(DEV)
+    rc.ring_allreduce_fused(f)
+    q = x.to(DEV)
+    rc.ring_psum(q)
+    ok_status()
+    assert np.array_equal(np_of(b), oracle.ring_allreduce(xn.copy(), "bf16"))
+    assert np.array_equal(np_of(o), oracle.reduce_scatter(xn.copy(), "bf16"))
+    assert np.array_equal(np_of(ob), oracle.reduce_scatter_bidir(xn.copy(), "bf16"))
+    assert np.array_equal(np_of(f), oracle.ring_allreduce(xn.copy(), "bf16"))
+    assert np.array_equal(np_of(q), oracle.psum(xn.copy(), "bf16"))
+
+
 _POISON = 0x7FC0DEAD   # a quiet-NaN payload no computation here produces
 
 
