@@ -285,8 +285,8 @@ int ring_set_timeout_ms(unsigned ms);
  * copies; RC_L2_LIVE_BYTES sets the chunk-segment budget; RC_HOST_SEGMENT_BYTES
  * the host entry point's segment size; RC_GEMM_PAIRS=0 keeps the one-CTA
  * GEMM kernels; RC_RING_STAGGER=G (default 3, 1 = off) starts slice j of a
- * ring all-reduce (j % G) times a fifth of its first step's estimated time
- * later.
+ * ring all-reduce or reduce-scatter (j % G) times a fifth of its first
+ * step's estimated time later.
  */
 int ring_set_slices(int slices);
 

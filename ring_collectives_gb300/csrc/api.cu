@@ -67,11 +67,12 @@ size_t l2_live_bytes()
 // groups' first steps overlap the others' L2-bound steps.  Measured on GB300
 // (P=8 x 64 MiB fp32 all-reduce, D = 4.1 us): G=1 0.2150-0.2173 ms, G=2
 // 0.2134-0.2143, G=3 0.2110-0.2119, G=4 0.2151-0.2154, G=5 0.2153-0.2160,
-// G=6 0.2194-0.2201 (bf16: G=1 0.2152-0.2154, G=3 0.2123-0.2126).  Only the all-reduce uses it: the
-// standalone reduce-scatter has no all-gather phase to absorb the later
-// groups' tail (0.1389-0.1394 -> 0.1407-0.1408 ms at P=8 x 64 MiB bf16), and
-// the all-gather and bidirectional reduce-scatter measured no change.  Knob,
-// read once: RC_RING_STAGGER = G (1 = off; unset or malformed = 3).
+// G=6 0.2194-0.2201 (bf16: G=1 0.2152-0.2154, G=3 0.2123-0.2126).  The
+// reduce-scatters use it too (P=8 x 64 MiB bf16: G=1 0.1356-0.1357 ms,
+// G=2 0.1362-0.1364, G=3 0.1297-0.1300; bidirectional 0.1710-0.1715 ->
+// 0.1697-0.1700 at G=3); the all-gather, whose first step is the own shard's
+// copy, does not.  Knob, read once: RC_RING_STAGGER = G (1 = off; unset or
+// malformed = 3).
 int stagger_groups_default()
 {
     static const int v = [] {
@@ -86,7 +87,7 @@ int stagger_groups_default()
 
 void set_stagger(rc::RingParams &p, size_t es)
 {
-    p.stagger_groups = p.mode == rc::MODE_ALLREDUCE ? stagger_groups_default() : 1;
+    p.stagger_groups = p.mode != rc::MODE_ALL_GATHER ? stagger_groups_default() : 1;
     const double first_step_bytes = 2.0 * p.P * ((double)p.chunk / (double)p.segments) * (double)es;
     const double ns = first_step_bytes / 32500.0;
     p.stagger_ns = p.stagger_groups > 1 ? (unsigned)(ns < 50000.0 ? ns : 50000.0) : 0u;

@@ -443,8 +443,9 @@ def test_serial_debug_mode_child():
 
 @pytest.mark.parametrize("groups", ["1", "6"])
 def test_stagger_settings_child(groups):
-    """RC_RING_STAGGER only shifts when the all-reduce's slice rings start:
-    off (1) and six groups give the same bits as the default three."""
+    """RC_RING_STAGGER only shifts when the slice rings of an all-reduce or
+    reduce-scatter start: off (1) and six groups give the same bits as the
+    default three."""
     import os
     import subprocess
     import sys
