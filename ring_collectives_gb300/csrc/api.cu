@@ -63,7 +63,7 @@ size_t l2_live_bytes()
 // data that is mostly in L2 and are bound by L2; when every slice ring runs
 // in step, all of them are in the HBM-bound step at once.  Slice j therefore
 // starts (j % G) * D later, G groups and D a fifth of the first step's time
-// at ~6.5 TB/s (its HBM bytes / 32500 ns per byte, capped at 50 us), so the
+// at ~6.5 TB/s (D in ns = its HBM bytes / 32500, capped at 50 us), so the
 // groups' first steps overlap the others' L2-bound steps.  Measured on GB300
 // (P=8 x 64 MiB fp32 all-reduce, D = 4.1 us): G=1 0.2150-0.2173 ms, G=2
 // 0.2134-0.2143, G=3 0.2110-0.2119, G=4 0.2151-0.2154, G=5 0.2153-0.2160,
