@@ -18,12 +18,15 @@
 //
 // Integer adds make every order give the same sum, so the model also checks
 // its results against plain sums.  Variant "early_notify" signals before the
-// step's stores (a planted protocol error that ThreadSanitizer must report).
+// step's stores (a planted protocol error that ThreadSanitizer must report);
+// variant "stagger" starts slice j's threads (j % 3) x 50 us late, like the
+// kernel's phase-shifted slice rings.
 //
-// Usage: ring_protocol_model MODE P S SEGMENTS LAUNCHES N_PER_RANK [early_notify]
+// Usage: ring_protocol_model MODE P S SEGMENTS LAUNCHES N_PER_RANK [early_notify|stagger]
 //   MODE: allreduce | reduce_scatter | all_gather | rs_bidir
 // Exit status 0 with "ok" when every launch produced the expected result.
 #include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -49,6 +52,7 @@ struct Launch {
     std::atomic<uint32_t> *done;
     int total_threads;
     bool early_notify;
+    bool stagger;
 };
 
 bool reached(uint32_t v, uint32_t want) { return (int32_t)(v - want) >= 0; }
@@ -67,6 +71,7 @@ void block(const Launch &L, int h, int r, int j)
     const int from = (bidir && h == 0) ? right : left;
     const int to = (bidir && h == 0) ? left : right;
     const uint32_t E0 = L.epoch->load(std::memory_order_relaxed);
+    if (L.stagger && j % 3) std::this_thread::sleep_for(std::chrono::microseconds(50 * (j % 3)));
     std::atomic<uint32_t> *my_rows = L.sig + ((size_t)j * P + r) * L.rows * P + (size_t)h * L.nsteps * P;
     std::atomic<uint32_t> *to_rows = L.sig + ((size_t)j * P + to) * L.rows * P + (size_t)h * L.nsteps * P;
     const size_t c = L.chunk, half = c / 2;
@@ -141,6 +146,7 @@ int main(int argc, char **argv)
     const int P = std::atoi(argv[2]), S = std::atoi(argv[3]), G = std::atoi(argv[4]), launches = std::atoi(argv[5]);
     const size_t npr = (size_t)std::atoll(argv[6]);
     const bool early = argc > 7 && std::string(argv[7]) == "early_notify";
+    const bool stagger = argc > 7 && std::string(argv[7]) == "stagger";
     if (P < 2 || S < 1 || G < 1 || launches < 1 || (mode != ALL_GATHER && npr % (size_t)P)) return 2;
     const size_t chunk = mode == ALL_GATHER ? npr : npr / (size_t)P;
     const size_t slot = mode == ALL_GATHER ? (size_t)P * npr : npr;
@@ -168,7 +174,7 @@ int main(int argc, char **argv)
             data = x;
         }
         Launch L{mode, P, S, G, rows, nsteps, chunk, data.data(), slot, in.data(), out.data(), sig.data(),
-                 &epoch, &done, P * S * halves, early};
+                 &epoch, &done, P * S * halves, early, stagger};
         std::vector<std::thread> th;
         for (int h = 0; h < halves; ++h)
             for (int r = 0; r < P; ++r)

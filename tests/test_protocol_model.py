@@ -50,6 +50,15 @@ def test_protocol_is_race_free_and_correct(model, mode, P, S, G, launches, n):
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr[-2000:]
 
 
+@pytest.mark.parametrize("mode", ["allreduce", "reduce_scatter", "rs_bidir"])
+def test_staggered_slice_starts_are_race_free(model, mode):
+    """Slice rings that start at different times (the kernel's phase-shifted
+    rings) keep the protocol race-free and the results exact."""
+    r = run(model, mode, 4, 3, 2, 3, 4096, "stagger")
+    assert "WARNING: ThreadSanitizer" not in r.stderr, r.stderr[-3000:]
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr[-2000:]
+
+
 @pytest.mark.parametrize("mode", ["allreduce", "reduce_scatter", "all_gather", "rs_bidir"])
 def test_early_notify_is_reported(model, mode):
     """Planted error: signalling the next step before this step's stores lets
