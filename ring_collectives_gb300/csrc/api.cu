@@ -71,7 +71,10 @@ size_t l2_live_bytes()
 // reduce-scatters use it too (P=8 x 64 MiB bf16: G=1 0.1356-0.1357 ms,
 // G=2 0.1362-0.1364, G=3 0.1297-0.1300; bidirectional 0.1710-0.1715 ->
 // 0.1697-0.1700 at G=3); the all-gather, whose first step is the own shard's
-// copy, does not.  Knob, read once: RC_RING_STAGGER = G (1 = off; unset or
+// copy, does not.  D as a seventh, a quarter or a third of the first step
+// measured the same or slower (f32 0.2137-0.2139 / 0.2126-0.2139 /
+// 0.2148 ms against 0.2130-0.2135; reduce-scatter 0.1307-0.1319 against
+// 0.1298-0.1301).  Knob, read once: RC_RING_STAGGER = G (1 = off; unset or
 // malformed = 3).
 int stagger_groups_default()
 {
