@@ -49,6 +49,76 @@ def test_bf16_rne_matches_torch_on_random_and_special_values():
     assert np.array_equal(got, want)
 
 
+def _bf16_exact_sum_rounded(a: int, b: int) -> int:
+    """bf16 bits of the exact sum of two finite bf16 values (bit patterns),
+    rounded once to bf16, nearest even, IEEE signed-zero and overflow rules;
+    written from the definition with exact rationals."""
+    from fractions import Fraction
+
+    def val(h):
+        s, e, m = h >> 15, (h >> 7) & 0xFF, h & 0x7F
+        mag = Fraction(m, 128) * Fraction(2) ** -126 if e == 0 else (1 + Fraction(m, 128)) * Fraction(2) ** (e - 127)
+        return -mag if s else mag
+
+    q = val(a) + val(b)
+    if q == 0:   # x + (-x) is +0 under round-to-nearest; -0 + -0 is -0
+        return 0x8000 if (a == 0x8000 and b == 0x8000) else 0
+    sign = 0x8000 if q < 0 else 0
+    q = abs(q)
+    e = q.numerator.bit_length() - q.denominator.bit_length()   # 2^e <= q < 2^(e+2)
+    while Fraction(2) ** e > q:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= q:
+        e += 1
+    e = max(e, -126)                        # below 2^-126: the subnormal spacing 2^-133
+    quantum = Fraction(2) ** (e - 7)
+    m, rem = divmod(q, quantum)
+    m = int(m)
+    if rem > quantum / 2 or (rem == quantum / 2 and m % 2 == 1):
+        m += 1
+    if m == 256:                            # carry into the next binade
+        m, e = 128, e + 1
+    if e > 127:
+        return sign | 0x7F80                # overflow to infinity
+    if m < 128:                             # subnormal (e == -126)
+        return sign | m
+    return sign | ((e + 127) << 7) | (m - 128)
+
+
+def test_bf16_hop_add_is_the_correctly_rounded_sum():
+    """The oracle's bf16 hop add (widen to binary32, add, round to bf16) equals
+    the exact sum rounded once to bf16 -- the fact that lets a kernel compute
+    the hop add with one bf16 addition.  Random finite pairs over the whole
+    exponent range, plus large exponent gaps, ties, subnormals and signed
+    zeros; a P=2 ring all-reduce is exactly one hop add per element."""
+    rng = np.random.default_rng(12)
+    n = 20000
+    a = rng.integers(0, 0x10000, n, dtype=np.uint32)
+    b = rng.integers(0, 0x10000, n, dtype=np.uint32)
+    edge_a, edge_b = [], []
+    for e in (0, 1, 60, 127, 200, 254):
+        for gap in (0, 1, 8, 15, 16, 17, 18, 24, 40):
+            for m in (0, 1, 0x40, 0x7F):
+                if e - gap >= 0:
+                    edge_a.append((e << 7) | m)
+                    edge_b.append(((e - gap) << 7) | (0x7F - m))
+                    edge_a.append((e << 7) | m)
+                    edge_b.append(0x8000 | ((e - gap) << 7) | m)
+    edge_a += [0, 0x8000, 0x8000, 0x0001, 0x007F, 0x7F7F, 0x7F7F]
+    edge_b += [0x8000, 0x8000, 0, 0x8001, 0x0001, 0x7F7F, 0x0001]
+    a = np.concatenate([a, np.array(edge_a, dtype=np.uint32)])
+    b = np.concatenate([b, np.array(edge_b, dtype=np.uint32)])
+    finite = ((a & 0x7F80) != 0x7F80) & ((b & 0x7F80) != 0x7F80)
+    a, b = a[finite].astype(np.uint16), b[finite].astype(np.uint16)
+    if a.size % 2:                          # the all-reduce wants N divisible by P=2
+        a, b = np.append(a, np.uint16(0)), np.append(b, np.uint16(0))
+    got = oracle.ring_allreduce(np.stack([a, b]).copy(), "bf16")
+    assert np.array_equal(got[0], got[1])
+    want = np.array([_bf16_exact_sum_rounded(int(x), int(y)) for x, y in zip(a, b)], dtype=np.uint16)
+    bad = np.nonzero(got[0] != want)[0]
+    assert bad.size == 0, [(hex(a[i]), hex(b[i]), hex(got[0][i]), hex(want[i])) for i in bad[:5]]
+
+
 def test_bf16_nan_stays_nan_and_roundtrip():
     f = np.array([np.nan, -np.nan, np.float32(1.5), np.float32(-2.25)], dtype=np.float32)
     h = oracle.bf16_from_f32(f)
