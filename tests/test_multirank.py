@@ -36,7 +36,7 @@ def _worker(rank, world, port, q):
         ms = 1.0 + rank * 0.5                 # rank 1 is the slow replica
         ms_max = bench.max_over_ranks(ms, dist, "cpu")
         value = bench.replicas_value(world, 2.0e9, ms_max)
-        args = bench.parse_args_for_tests(["--impl", "reference", "--steps", "1", "--warmup", "0"])
+        args = bench.parse_args_for_tests(["--impl", "reference", "--gpus", str(world), "--steps", "1", "--warmup", "0"])
         spec = bench.workload_spec("f32_64mib", 8, 8 * 64)
         out = io.StringIO()
         with contextlib.redirect_stdout(out):
@@ -63,3 +63,13 @@ def test_replica_harness_two_gloo_ranks():
         assert rc == 0
     assert '"impl": "reference"' in res[0][4]               # rank 0 prints the line
     assert res[1][4] == ""                                  # other ranks exit without work
+    import json
+    line = json.loads(res[0][4].strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["n_gpus"] == 2 and line["higher_is_better"] is True and line["vs_baseline"] is None
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["unit"] == line["unit"]
+    assert "workload" in line["config"]
