@@ -281,8 +281,9 @@ int ring_set_timeout_ms(unsigned ms);
  * Other environment settings, read once: RC_DEBUG_SERIAL=1 makes every step
  * of a ring launch also wait for all blocks of the launch (a bounded grid
  * barrier; for debugging synchronisation, results are unchanged);
- * RC_AG_BULK=0 moves all-gather steps with vector copies instead of bulk
- * copies; RC_L2_LIVE_BYTES sets the chunk-segment budget; RC_HOST_SEGMENT_BYTES
+ * RC_AG_BULK=0 / 1 moves the all-gather steps of every collective with
+ * vector copies / bulk copies (default: vector in the all-reduce, bulk in the
+ * all-gather); RC_L2_LIVE_BYTES sets the chunk-segment budget; RC_HOST_SEGMENT_BYTES
  * the host entry point's segment size; RC_GEMM_PAIRS=0 keeps the one-CTA
  * GEMM kernels; RC_RING_STAGGER=G (default 3, 1 = off) starts slice j of a
  * ring all-reduce or reduce-scatter (j % G) times a fifth of its first

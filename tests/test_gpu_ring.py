@@ -413,14 +413,28 @@ def test_segments_forced_in_a_child_process():
 
 
 def test_vector_all_gather_copies_child():
-    """RC_AG_BULK=0 (all-gather steps as 32-byte vector copies instead of bulk
-    copies through shared memory): all-reduce, reduce-scatter and all-gather
-    stay bit-exact."""
+    """RC_AG_BULK=0 (all-gather steps as 32-byte vector copies in every
+    collective, the standalone all-gather included): all-reduce,
+    reduce-scatter and all-gather stay bit-exact."""
     import os
     import subprocess
     import sys
     from tests.conftest import ROOT
     env = dict(os.environ, RC_AG_BULK="0")
+    r = subprocess.run([sys.executable, "-c", _SEGMENT_CHILD, ROOT], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+def test_bulk_all_gather_copies_child():
+    """RC_AG_BULK=1 (all-gather steps as bulk copies through shared memory in
+    every collective, the all-reduce included): all-reduce, reduce-scatter
+    and all-gather stay bit-exact."""
+    import os
+    import subprocess
+    import sys
+    from tests.conftest import ROOT
+    env = dict(os.environ, RC_AG_BULK="1")
     r = subprocess.run([sys.executable, "-c", _SEGMENT_CHILD, ROOT], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
