@@ -21,7 +21,9 @@
 //
 // Data movement: reduce-scatter steps stream 32-byte vectors through
 // registers (two loads, one hop add, one store per vector); all-gather steps
-// move their slice with bulk (TMA) copies staged in shared memory.
+// move their slice with 32-byte vector copies (all-reduce) or with bulk (TMA)
+// copies staged in shared memory (standalone all-gather), as RingParams::ag_bulk
+// says.
 //
 // Why no extra guard against overwriting data a neighbour still reads: rank
 // r reads its left neighbour's chunk (r-s-2) in round s; the left neighbour
