@@ -636,7 +636,7 @@ def run_ours(args, spec, rank, world, dist):
             "bf16_64mib_reduce_scatter_bidir": {
                 "ms": round(statistics.mean(tbi), 4),
                 "GB/s": round(3 * 7 * Nb * 2 / statistics.mean(tbi) / 1e6, 1),
-                "note": "Pallas-style bidirectional reduce-scatter: P steps, top halves left, bottoms right"},
+                "note": "Pallas-style bidirectional reduce-scatter: P-1 steps, top halves left, bottoms right, last add stored in the owner's output"},
             "bf16_64mib_reduce_scatter": {"ms": round(mrs, 4),
                                           "GB/s": round(3 * 7 * Nb * 2 / mrs / 1e6, 1),
                                           "frac_a": round(3 * 7 * Nb * 2 / mrs / 1e6 / peaks()[0], 4)},
@@ -792,10 +792,11 @@ def run_row(args, rank, world, dist):
             kern = "k_ring (reduce-scatter mode)"
             metric = "ring reduce_scatter GB/s (3(P-1)*N*e / time), P=8, 64 MiB/rank, bf16, 1xGB300 per replica"
         else:
-            alg = (3 * (P - 1) + 2) * N * e
-            alg_text = "(3(P-1)+2)*N*e (P-1 steps of 2 half-chunk reads + 1 write per direction, then a chunk copy)"
+            alg = 3 * (P - 1) * N * e
+            alg_text = ("3(P-1)*N*e (P-1 steps of 2 half-chunk reads + 1 write per direction; the last write "
+                        "goes to the owner's output)")
             kern = "k_ring (bidirectional reduce-scatter mode)"
-            metric = ("bidirectional reduce_scatter GB/s ((3(P-1)+2)*N*e / time), P=8, 64 MiB/rank, bf16, "
+            metric = ("bidirectional reduce_scatter GB/s (3(P-1)*N*e / time), P=8, 64 MiB/rank, bf16, "
                       "1xGB300 per replica")
         sources = KERNEL_SOURCES
     elif name == "ppermute_f32_64mib":

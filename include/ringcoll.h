@@ -33,6 +33,12 @@
  *     stream, or order the streams.
  *   - Return values are rc_status codes; ring_last_error() describes the most
  *     recent failure of the calling thread.
+ *   - NaN.  The floating-point collectives are bit-identical to the fold
+ *     orders stated below for every element whose result is not a NaN.  An
+ *     element whose result is a NaN (a NaN input is folded into it, or +inf
+ *     and -inf meet in one hop add) is a NaN here as well, but its sign and
+ *     payload are unspecified: the hardware add returns its own NaN pattern,
+ *     not one of the operands'.  Integer data has no such exception.
  */
 #ifndef RINGCOLL_H
 #define RINGCOLL_H
@@ -95,6 +101,7 @@ int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_
  *     R[k] = ((x_{k+1} + x_{k+2}) + ... + x_{k+P-1}) + x_k   (indices mod P)
  * with "+" the element type's hop add (f32: IEEE binary32 add; bf16: add in
  * binary32, round the partial sum to bf16 at every hop; i32: wrapping add).
+ * NaN results: bit-identity excludes them, see "NaN" above.
  * bufs slots: [N] elements at bufs_base + r*bufs_stride; CLOBBERED: their
  *     contents are undefined after the call (they hold partial sums, and the
  *     L2 lines of partials that are dead are dropped without write-back).
@@ -117,6 +124,11 @@ int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, siz
  *     top:    ((x_r + x_{r-1}) + x_{r-2}) + ... + x_{r+1}
  *     bottom: ((x_r + x_{r+1}) + x_{r+2}) + ... + x_{r-1}   (indices mod P)
  * ("+" the element type's hop add), the order of the page's state tables.
+ * NaN results: bit-identity excludes them, see "NaN" above.
+ * In round s = 0..P-2 every rank adds its own contribution to the partial
+ * its upstream neighbour holds; round P-2 completes each half at the rank
+ * one hop before its owner, which stores it straight into the owner's out
+ * slot (the page's last hop, a plain transfer, is folded into that store).
  * bufs slots: [N] elements at bufs_base + r*bufs_stride; CLOBBERED (contents
  *     undefined afterwards, as for ring_reduce_scatter).
  * out slots:  [N/P] elements at out_base + r*out_stride (written).
@@ -137,7 +149,8 @@ int ring_reduce_scatter_bidir(void *bufs_base, size_t bufs_stride, void *out_bas
  * Synchronisation is neighbour-local (per-step signal rows, release/acquire),
  * with no grid-wide barrier.
  * Result: every slot holds R[0] | R[1] | ... | R[P-1] (R as for
- * ring_reduce_scatter), bit-identical on every rank.
+ * ring_reduce_scatter), bit-identical on every rank (NaN results: see "NaN"
+ * above; they are NaN on every rank).
  * bufs slots: [N] elements at bufs_base + r*stride, read and written in place.
  * N must be a multiple of P (RC_ERR_INVALID otherwise).  P = 1 is a no-op.
  */
@@ -155,7 +168,8 @@ int ring_allreduce(void *bufs_base, size_t stride, int P, size_t N, int dtype, v
  *     in flight) before about 2^30 calls.
  *   ws_bytes: at least ring_allreduce_workspace_bytes(P, N, dtype) for the
  *     current device (RC_ERR_INVALID otherwise).
- * Device-side timeouts are recorded in the workspace, not read by ring_status.
+ * Device-side timeouts are recorded in the workspace: read (and clear) them
+ * with ring_status_ex(workspace, stream); ring_status() does not see them.
  * (The pages' signals live in per-rank signal buffers; this variant lets the
  * caller place them.)
  */
@@ -174,7 +188,7 @@ size_t ring_allreduce_workspace_bytes(int P, size_t N, int dtype);
  * (section "走读") produce.  Instead of 2(P-1) ring steps over HBM, each
  * element position of all P slots is read once, folded on chip and written
  * to all P slots: 2*P*N*e bytes, the minimum for an all-reduce.  Uses no
- * signal workspace.
+ * signal workspace.  NaN results: as for ring_allreduce.
  */
 int ring_allreduce_fused(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream);
 
@@ -186,6 +200,7 @@ int ring_allreduce_fused(void *bufs_base, size_t stride, int P, size_t N, int dt
  *     o_r = (((0 + x_{r-1}) + x_{r-2}) + ...) + x_r       (indices mod P)
  * ("+" the element type's hop add).  Each rank folds in its own order, so
  * floating-point results may differ between ranks (unlike ring_allreduce).
+ * NaN results: bit-identity excludes them, see "NaN" above.
  * bufs slots: [n] elements at bufs_base + r*stride, replaced by o_r in place.
  * n need not be a multiple of P.  P = 1: o_0 = 0 + x_0.
  */
@@ -258,12 +273,24 @@ int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_stride, void
 
 /*
  * ring_status -- waits for `stream`, then returns and clears the device
- * status of the calling device's workspace: RC_OK, or RC_ERR_TIMEOUT when a
- * bounded wait in a kernel ran out (ring_last_error() then names the rank,
- * step and slice that gave up).  A timed-out call leaves its outputs
- * undefined; later calls are unaffected.
+ * status of the library's own signal areas on the calling device: the
+ * workspace of the regular entry points and the fixed array of
+ * ring_allreduce_noalloc.  RC_OK, or RC_ERR_TIMEOUT when a bounded wait in a
+ * kernel ran out (ring_last_error() then names the rank, step and slice that
+ * gave up, and says whether it was an allocation-free call).  A timed-out
+ * call leaves its outputs undefined; later calls are unaffected.  Reading the
+ * status allocates nothing (a copy to host stack memory and a memset, both
+ * on `stream`).
  */
 int ring_status(void *stream);
+
+/*
+ * ring_status_ex -- ring_status for a caller-owned workspace (the one given
+ * to ring_allreduce_ex): waits for `stream`, then returns and clears the
+ * status recorded in `workspace` (DEVICE pointer, 16-byte aligned; null or
+ * misaligned gives RC_ERR_INVALID).  RC_OK or RC_ERR_TIMEOUT as above.
+ */
+int ring_status_ex(void *workspace, void *stream);
 
 /* Message describing the calling thread's most recent error ("" if none). */
 const char *ring_last_error(void);
@@ -293,17 +320,19 @@ int ring_set_slices(int slices);
 
 /*
  * Test hook for failure detection: the next ring launch (ring_all_gather,
- * ring_reduce_scatter or ring_allreduce) on any thread skips the notify that
- * rank `rank` would send after global step `step`, in every slice.  Its right
- * neighbour's bounded wait then runs out and ring_status() reports
- * RC_ERR_TIMEOUT; no fault is raised and the device stays usable.
- * (-1, -1) cancels a pending skip.
+ * ring_reduce_scatter, ring_reduce_scatter_bidir, ring_allreduce,
+ * ring_allreduce_ex or ring_allreduce_noalloc) on any thread skips the
+ * notify that rank `rank` would send after global step `step`, in every
+ * slice.  Its neighbour's bounded wait then runs out and ring_status() (or
+ * ring_status_ex() for a caller's workspace) reports RC_ERR_TIMEOUT; no
+ * fault is raised and the device stays usable.  (-1, -1) cancels a pending
+ * skip.
  */
 int ring_debug_skip_notify(int rank, int step);
 
 /*
  * Tracing hook: while dev_buf is set (a device buffer of `bytes` bytes), every
- * ring launch (ring_all_gather, ring_reduce_scatter, ring_allreduce) has
+ * ring launch (the entry points listed for ring_debug_skip_notify) has
  * thread 0 of block b (rank b / slices, slice b % slices) write three
  * %globaltimer stamps (ns) per global step g at word (b*steps + g)*3: the
  * start of the wait on the left neighbour, its end, and the end of the step
@@ -334,10 +363,13 @@ int ring_finalize(void);
  * cudaFree or other allocating routine.
  *
  * Arguments, layout, validation and result: as ring_allreduce (the same
- * kernel runs; the result is bit-identical).  Additional limit: the signal
- * rows of one call, slices*P*2(P-1)*P words plus a 128-byte header, must fit
- * in the array; the slice count is reduced to fit, and P for which even one
- * slice does not fit (P > 32) is rejected with RC_ERR_INVALID.
+ * kernel runs with the same chunk segments; the result is bit-identical).
+ * Additional limit: the signal rows of one call, slices*P*2(P-1)*P words plus
+ * a 128-byte header, must fit in the array; the slice count is reduced to
+ * fit (at P = 8 at most 73 slices, where ring_allreduce may use up to 152:
+ * large calls then stream with fewer thread blocks and run slower), and P for
+ * which even one slice does not fit (P > 32) is rejected with
+ * RC_ERR_INVALID.
  *
  * Set-up: the first call on a device (with that device current) looks up the
  * array's device address with cudaGetSymbolAddress and clears the array with
@@ -347,7 +379,8 @@ int ring_finalize(void);
  * between calls).  Calls that overlap on the GPU -- on different streams
  * without ordering, or on different host threads -- race on the array and
  * give undefined results; issue them in stream order.  Errors raised by a
- * device wait are reported in the array, not read by ring_status().
+ * device wait are recorded in the array's header and read (and cleared) by
+ * ring_status(), which allocates nothing either.
  */
 #define RC_NOALLOC_SCRATCH_BYTES (256u * 1024u)
 int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream);

@@ -26,6 +26,7 @@ __all__ = [
     "RingError", "ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_reduce_scatter_bidir",
     "ring_allreduce", "ring_allreduce_ex", "ring_allreduce_workspace_bytes", "ring_allreduce_host",
     "ring_allreduce_fused", "ring_psum", "ring_allreduce_noalloc", "ag_gemm", "gemm_rs", "ring_status",
+    "ring_status_ex",
     "ring_last_error", "ring_set_timeout_ms", "ring_set_slices", "ring_debug_skip_notify",
     "ring_debug_set_trace", "ring_finalize", "library_path", "load",
 ]
@@ -53,6 +54,7 @@ _SIGNATURES = {
     "ag_gemm": ([_vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp], _i),
     "gemm_rs": ([_vp, _sz, _vp, _sz, _vp, _sz, _i, _i, _i, _i, _vp], _i),
     "ring_status": ([_vp], _i),
+    "ring_status_ex": ([_vp, _vp], _i),
     "ring_last_error": ([], ctypes.c_char_p),
     "ring_set_timeout_ms": ([_u], _i),
     "ring_set_slices": ([_i], _i),
@@ -283,6 +285,15 @@ def ring_status(stream=None, device=None) -> int:
         return load().ring_status(_stream(stream, dev))
 
 
+def ring_status_ex(workspace: torch.Tensor, stream=None) -> int:
+    """Waits for the stream and returns (and clears) the status recorded in a
+    caller-owned workspace (the one given to :func:`ring_allreduce_ex`)."""
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    with torch.cuda.device(workspace.device):
+        return load().ring_status_ex(workspace.data_ptr(), _stream(stream, workspace.device))
+
+
 def ring_set_timeout_ms(ms: int) -> None:
     _check(load().ring_set_timeout_ms(ms))
 
@@ -313,7 +324,8 @@ def ring_allreduce_noalloc(bufs: torch.Tensor, N: int | None = None, stream=None
     """ring_allreduce without any device allocation by the library: the signal
     rows live in a fixed 256 KiB array compiled into the library (P <= 32).
     For callers that cannot let a library allocate device memory; see the
-    declaration in include/ringcoll.h for set-up and ordering rules."""
+    declaration in include/ringcoll.h for set-up and ordering rules.  Device
+    timeouts of these calls are read with :func:`ring_status`."""
     L = load()
     fn = L.ring_allreduce_noalloc
     bp, bs, dt = _slots(bufs, "bufs")

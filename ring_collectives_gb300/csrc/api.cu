@@ -523,7 +523,7 @@ int ring_reduce_scatter_bidir(void *bufs_base, size_t bufs_stride, void *out_bas
     p.out_stride = out_stride;
     p.chunk = c;
     p.P = P;
-    p.rows = 2 * P;   // P steps for each of the two halves
+    p.rows = 2 * (P - 1);   // P-1 steps for each of the two halves
     p.mode = rc::MODE_RS_BIDIR;
     p.discard = 1;
     return run_ring(p, dtype, (cudaStream_t)stream);
@@ -777,24 +777,65 @@ int ring_allreduce_host(const void *h_in, size_t h_in_stride, void *h_out, size_
     return RC_OK;
 }
 
+// Reads the header of the signal area at `ws` (device memory) after `stream`
+// has completed, and clears its status word if it is set.  Returns the status
+// (0 = OK) and fills *h.  Allocates nothing: the read lands in *h and the
+// clear is a memset on `stream`.
+static int read_and_clear_status(void *ws, cudaStream_t stream, rc::WsHeader *h, const char *what)
+{
+    cudaError_t e = cudaMemcpyAsync(h, ws, sizeof *h, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    if (h->status == 0) return RC_OK;
+    e = cudaMemsetAsync((char *)ws + offsetof(rc::WsHeader, status), 0, sizeof(uint32_t), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    return (int)h->status;
+}
+
+static void *noalloc_scratch_if_set_up(int dev);
+
 int ring_status(void *stream)
 {
-    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RC_OK;
-    std::lock_guard<std::mutex> lock(g_mu);
-    DeviceState &st = g_dev[dev];
-    if (!st.ws) return RC_OK;
-    rc::WsHeader h;
-    e = cudaMemcpy(&h, st.ws, sizeof h, cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "status read");
-    if (h.status == 0) return RC_OK;
-    e = cudaMemset((char *)st.ws + offsetof(rc::WsHeader, status), 0, sizeof(uint32_t));
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(e, "status clear");
-    return fail((int)h.status, "device wait timed out: rank %u, step %u, slice %u", h.err_rank, h.err_step,
-                h.err_slice);
+    // The library's two signal areas on this device: the workspace of the
+    // regular entry points and the fixed array of ring_allreduce_noalloc.
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        ws = g_dev[dev].ws;
+    }
+    void *na = noalloc_scratch_if_set_up(dev);
+    rc::WsHeader h{}, hn{};
+    const int st_ws = ws ? read_and_clear_status(ws, s, &h, "status read") : RC_OK;
+    if (st_ws == RC_ERR_CUDA) return st_ws;
+    const int st_na = na ? read_and_clear_status(na, s, &hn, "status read (allocation-free array)") : RC_OK;
+    if (st_na == RC_ERR_CUDA) return st_na;
+    if (st_ws && st_na)
+        return fail(st_ws, "device wait timed out: rank %u, step %u, slice %u (and in an allocation-free call: "
+                    "rank %u, step %u, slice %u)", h.err_rank, h.err_step, h.err_slice, hn.err_rank, hn.err_step,
+                    hn.err_slice);
+    if (st_ws)
+        return fail(st_ws, "device wait timed out: rank %u, step %u, slice %u", h.err_rank, h.err_step,
+                    h.err_slice);
+    if (st_na)
+        return fail(st_na, "device wait timed out in an allocation-free call: rank %u, step %u, slice %u",
+                    hn.err_rank, hn.err_step, hn.err_slice);
+    return RC_OK;
+}
+
+int ring_status_ex(void *workspace, void *stream)
+{
+    if (!workspace) return fail(RC_ERR_INVALID, "null workspace");
+    if ((uintptr_t)workspace & 15u) return fail(RC_ERR_INVALID, "workspace must be 16-byte aligned");
+    rc::WsHeader h{};
+    const int st = read_and_clear_status(workspace, (cudaStream_t)stream, &h, "status read");
+    if (st == RC_OK || st == RC_ERR_CUDA) return st;
+    return fail(st, "device wait timed out: rank %u, step %u, slice %u", h.err_rank, h.err_step, h.err_slice);
 }
 
 // ---------------------------------------------------------------------------
@@ -813,31 +854,33 @@ NoAllocState g_noalloc[kMaxDevices];
 std::mutex g_noalloc_mu;
 } // namespace
 
+static void *noalloc_scratch_if_set_up(int dev)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    return g_noalloc[dev].ptr;
+}
+
 int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream)
 {
-    const size_t es = elem_size(dtype);
-    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
-    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
-    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
-    if (N == 0 || P == 1) return RC_OK;
-    if (!bufs_base) return fail(RC_ERR_INVALID, "null slot base");
-    if (stride < N * es) return fail(RC_ERR_INVALID, "stride %zu below the %zu bytes of a slot", stride, N * es);
-    if (!elem_aligned(bufs_base, stride, es))
-        return fail(RC_ERR_INVALID, "slot base and stride must be multiples of the %zu-byte element", es);
-    const size_t rows = 2 * (size_t)(P - 1);
+    rc::RingParams p;
+    int rc_ = allreduce_params(bufs_base, stride, P, N, dtype, p);
+    if (rc_ < 0) return RC_OK;
+    if (rc_) return rc_;
     const size_t avail_words = (RC_NOALLOC_SCRATCH_BYTES - sizeof(rc::WsHeader)) / 4;
-    const size_t words_per_slice = (size_t)P * rows * (size_t)P;
+    const size_t words_per_slice = (size_t)P * (size_t)p.rows * (size_t)P;
     if (words_per_slice > avail_words)
         return fail(RC_ERR_INVALID, "P=%d needs %zu signal words per slice; the static scratch holds %zu (P <= 32)",
                     P, words_per_slice, avail_words);
 
     int dev;
     DeviceState *st = nullptr;
-    int rc_ = current_device(&dev, &st);
+    rc_ = current_device(&dev, &st);
     if (rc_) return rc_;
-    const size_t c = N / (size_t)P;
-    rc::RingParams p{};
-    rc_ = choose_slices(*st, dtype, P, c, c * es, &p.S);
+    // The launch shape of ring_allreduce (slices, chunk segments, phase-shifted
+    // rings), with the slice count then lowered until the signal rows fit in
+    // the array.  Fewer slices keep every slice non-empty for the planned
+    // segment count, so the segments stand.
+    rc_ = plan_ring(p, dtype, st);
     if (rc_) return rc_;
     if ((size_t)p.S * words_per_slice > avail_words) p.S = (int)(avail_words / words_per_slice);
 
@@ -856,26 +899,17 @@ int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int 
         if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch");
         na.launches = 0;
     }
-    p.data = (char *)bufs_base;
-    p.data_stride = stride;
-    p.chunk = c;
-    p.P = P;
-    p.rows = (int)rows;
-    p.mode = rc::MODE_ALLREDUCE;
-    p.discard = 1;
     p.hdr = (rc::WsHeader *)na.ptr;
     p.sig = (uint32_t *)((char *)na.ptr + sizeof(rc::WsHeader));
     p.timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
-    p.skip_rank = -1;
-    p.skip_step = -1;
-    p.segments = 1;
-    p.chunk_stride = c;
-    p.ag_bulk = ag_bulk_for(p.mode);
+    p.skip_rank = g_skip_rank.exchange(-1);
+    p.skip_step = g_skip_step.exchange(-1);
+    p.trace = g_trace.load();
+    p.trace_words = g_trace_words.load();
     p.debug_serial = debug_serial();
-    set_stagger(p, elem_size(dtype));
     cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, s);
     if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
-    na.launches++;
+    na.launches += (uint64_t)p.segments; // the launch advances the epoch by its segment count
     return RC_OK;
 }
 

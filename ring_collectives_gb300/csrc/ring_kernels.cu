@@ -381,11 +381,15 @@ __device__ void grid_meet(const RingParams &p, uint32_t round, uint32_t E, uint3
 // MODE_RS_BIDIR (the bidirectional reduce-scatter of "Pallas TPU Distributed
 // Collectives 复习文档", section 4): block (h, r, j) runs half h of every
 // chunk (h = 0: the top half [0, c/2), which travels left; h = 1: the bottom
-// half [c/2, c), which travels right) as its own ring.  In step s < P-1 rank
-// r adds the partial its upstream neighbour (right for the top, left for the
-// bottom) holds for chunk (r+1+s) resp. (r-1-s) to its own contribution; in
-// step P-1 it copies the finished chunk r from that neighbour to out_r.  Each
-// chunk half is written once, so no buffer is ever overwritten while read.
+// half [c/2, c), which travels right) as its own ring.  In step s = 0..P-2
+// rank r adds the partial its upstream neighbour (right for the top, left for
+// the bottom) holds for chunk (r+1+s) resp. (r-1-s) to its own contribution.
+// Step P-2 completes chunk (r-1) resp. (r+1) -- the chunk of the very
+// neighbour this block notifies -- and stores it straight into that rank's
+// out slot: the page's last hop only moves the finished sum to its owner, so
+// folding it into the store saves a read and a write of every half and one
+// signalled step.  Each chunk half is written once, so no buffer is ever
+// overwritten while read.
 // SERIAL: the barrier-injection debug variant (RingParams::debug_serial); a
 // separate instantiation, so the normal kernels carry none of its state.
 template <int DT, int MODE, bool SERIAL>
@@ -402,7 +406,7 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
     const int to = (BIDIR && h == 0) ? left : right;   // whom this block notifies
     // The abort word is the header's pad[0]: a launch that gives up stores its epoch there.
     uint32_t *abort_word = &p.hdr->pad[0];
-    const int nsteps = MODE == MODE_ALLREDUCE ? 2 * (P - 1) : BIDIR ? P : P - 1;
+    const int nsteps = MODE == MODE_ALLREDUCE ? 2 * (P - 1) : P - 1;
 
     // State only thread 0 uses (signal rows, step stamps) lives in shared
     // memory so it does not hold registers through the streaming loops.
@@ -504,19 +508,17 @@ __global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS) k_ring(const
                 else
                     ag_copy<ES, false>(my_slot + off, from_slot + off, n, bc, p, r, g, j, &s_abort);
             } else if (BIDIR) {
-                if (g < P - 1) {
-                    // partial for chunk k: the upstream neighbour's partial (+) own contribution
-                    const int k = h == 0 ? (r + 1 + g) % P : (r - 1 - g + 2 * P) % P;
-                    const size_t off = ((size_t)k * cs + lo) * ES;
-                    // The partial read here is dead afterwards (no one reads or
-                    // rewrites it again): its lines are dropped from step s = 1 on.
+                // partial for chunk k: the upstream neighbour's partial (+) own contribution
+                const int k = h == 0 ? (r + 1 + g) % P : (r - 1 - g + 2 * P) % P;
+                const size_t off = ((size_t)k * cs + lo) * ES;
+                // The partial read here is dead afterwards (no one reads or
+                // rewrites it again): its lines are dropped from step s = 1 on.
+                if (last) // k == to: the finished sum goes to its owner's out slot
+                    add_range<DT, T, kStNormal>(p.out + (size_t)k * p.out_stride + lo * ES, from_slot + off,
+                                                my_slot + off, n, p.discard && g >= 1);
+                else
                     add_range<DT, T, kStEvictLast>(my_slot + off, from_slot + off, my_slot + off, n,
                                                    p.discard && g >= 1);
-                } else {
-                    // the neighbour's partial for chunk r is complete: deliver it
-                    copy_range<ES, T, kStNormal>(p.out + (size_t)r * p.out_stride + lo * ES,
-                                                 from_slot + ((size_t)r * cs + lo) * ES, n);
-                }
             } else if (g < P - 1) {
                 const int s = g;
                 const int k = (r - s - 2 + P) % P; // recv_add_idx == left_send_idx

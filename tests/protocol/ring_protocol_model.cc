@@ -14,7 +14,8 @@
 // the left neighbour's chunk (r-s-2+P)%P into the own chunk of that index;
 // all-gather round t copies chunk (r-1-t+P)%P from the left neighbour; the
 // bidirectional variant follows "Pallas TPU Distributed Collectives 复习文档",
-// section 4 (top halves travel left, bottom halves right, P steps).
+// section 4 (top halves travel left, bottom halves right, P-1 steps; the
+// last add stores the finished half straight into its owner's output).
 //
 // Integer adds make every order give the same sum, so the model also checks
 // its results against plain sums.  Variant "early_notify" signals before the
@@ -107,13 +108,10 @@ void block(const Launch &L, int h, int r, int j)
                 const int k = (r - 1 - g + P) % P;
                 for (size_t i = 0; i < n; ++i) my[(size_t)k * c + lo + i] = fr[(size_t)k * c + lo + i];
             } else if (bidir) {
-                if (g < P - 1) {
-                    const int k = h == 0 ? (r + 1 + g) % P : (r - 1 - g + 2 * P) % P;
-                    for (size_t i = 0; i < n; ++i) my[(size_t)k * c + lo + i] += fr[(size_t)k * c + lo + i];
-                } else {
-                    for (size_t i = 0; i < n; ++i)
-                        L.out[(size_t)r * c + lo + i] = fr[(size_t)r * c + lo + i];
-                }
+                const int k = h == 0 ? (r + 1 + g) % P : (r - 1 - g + 2 * P) % P;
+                // the last step finishes chunk k == to and stores it in that rank's output
+                uint32_t *dst = g == P - 2 ? L.out + (size_t)k * c : my + (size_t)k * c;
+                for (size_t i = 0; i < n; ++i) dst[lo + i] = my[(size_t)k * c + lo + i] + fr[(size_t)k * c + lo + i];
             } else if (g < P - 1) {
                 const int k = (r - g - 2 + P) % P;
                 uint32_t *dst = (L.mode == REDUCE_SCATTER && g == P - 2) ? L.out + (size_t)r * c : my + (size_t)k * c;
@@ -151,7 +149,7 @@ int main(int argc, char **argv)
     const size_t chunk = mode == ALL_GATHER ? npr : npr / (size_t)P;
     const size_t slot = mode == ALL_GATHER ? (size_t)P * npr : npr;
     const int halves = mode == RS_BIDIR ? 2 : 1;
-    const int nsteps = mode == ALLREDUCE ? 2 * (P - 1) : mode == RS_BIDIR ? P : P - 1;
+    const int nsteps = mode == ALLREDUCE ? 2 * (P - 1) : P - 1;
     const int rows = nsteps * halves;
     std::vector<uint32_t> data((size_t)P * slot), in((size_t)P * npr), out((size_t)P * chunk);
     std::vector<std::atomic<uint32_t>> sig((size_t)S * P * rows * P);

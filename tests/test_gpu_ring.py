@@ -685,6 +685,55 @@ def test_allreduce_ex_concurrent_streams_with_own_workspaces():
         rc.ring_allreduce_ex(xs[0].to(DEV), small)
 
 
+def test_allreduce_ex_timeout_is_read_from_the_callers_workspace():
+    """A skipped notify in a ring_allreduce_ex launch (host-side test hook)
+    makes a neighbour's bounded wait run out: ring_status_ex reports
+    RC_ERR_TIMEOUT from the caller's workspace (ring_status, which reads the
+    library's own areas, does not), clears it, and the next call on the same
+    workspace is bit-exact against the oracle."""
+    P, c = 4, 64 * 64
+    x = make(P, P * c, torch.float32, seed=41)
+    want = oracle.ring_allreduce(np_of(x).copy(), "f32")
+    ws = torch.zeros(rc.ring_allreduce_workspace_bytes(P, P * c), dtype=torch.uint8, device=DEV)
+    rc.ring_set_timeout_ms(100)
+    try:
+        b = x.to(DEV)
+        rc.ring_debug_skip_notify(2, 1)
+        rc.ring_allreduce_ex(b, ws)
+        assert rc.ring_status() == rc.RC_OK
+        assert rc.ring_status_ex(ws) == rc.RC_ERR_TIMEOUT
+        assert "timed out" in rc.ring_last_error()
+        assert rc.ring_status_ex(ws) == rc.RC_OK      # read and cleared
+        b = x.to(DEV)
+        rc.ring_allreduce_ex(b, ws)
+        assert rc.ring_status_ex(ws) == rc.RC_OK, rc.ring_last_error()
+        assert np.array_equal(np_of(b), want)
+    finally:
+        rc.ring_set_timeout_ms(2000)
+        rc.ring_debug_skip_notify(-1, -1)
+
+
+@pytest.mark.parametrize("fn", ["reduce_scatter", "bidir"])
+def test_reduce_scatter_timeouts_are_reported(fn):
+    """The skip hook reaches both reduce-scatters; the next call is exact."""
+    P, c = 4, 64 * 32 + 2
+    x = make(P, P * c, torch.bfloat16, seed=43)
+    f = rc.ring_reduce_scatter if fn == "reduce_scatter" else rc.ring_reduce_scatter_bidir
+    want = (oracle.reduce_scatter if fn == "reduce_scatter" else oracle.reduce_scatter_bidir)(np_of(x).copy(), "bf16")
+    out = torch.empty((P, c), dtype=torch.bfloat16, device=DEV)
+    rc.ring_set_timeout_ms(100)
+    try:
+        rc.ring_debug_skip_notify(1, 0)
+        f(x.to(DEV), out)
+        assert rc.ring_status() == rc.RC_ERR_TIMEOUT
+        f(x.to(DEV), out)
+        ok_status()
+        assert np.array_equal(np_of(out), want)
+    finally:
+        rc.ring_set_timeout_ms(2000)
+        rc.ring_debug_skip_notify(-1, -1)
+
+
 def test_allreduce_replayed_from_a_cuda_graph():
     """The launch epoch lives in device memory, so a captured all-reduce can
     be replayed: every replay signals with a fresh epoch and stays bit-exact."""
