@@ -64,7 +64,8 @@ def parse(argv=None):
     ap.add_argument("--P", type=int, default=8)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--sweep", action="store_true", help="add the weak-scaling sweep (P=2..32) to the line")
+    ap.add_argument("--sweep", action="store_true",
+                    help="(kept for old command lines: the default line always carries the weak-scaling sweep)")
     ap.add_argument("--n-per-rank", type=int, default=0,
                     help="override N per rank (a smaller case of the same workload, e.g. for profiling)")
     return ap.parse_args(argv)
@@ -472,39 +473,6 @@ def ag_gemm_secondary(rc, dev, stream, args):
         "note": "gather of the 8 shards (64 MiB) + C = A_g.B^T, one tcgen05 launch"}}
 
 
-def fold_secondary(rc, dev, stream, args):
-    """Single-pass all-reduces on the benchmark workload: the fused ring-order
-    fold (same bits as ring_allreduce) and the Pallas psum order; both move
-    the minimum 2*P*N*e bytes (roofline (b))."""
-    x = synthetic.workload("f32_64mib")
-    pr = x.to(dev)
-    del x
-    bf = torch.empty_like(pr)
-    P, N = pr.shape
-    out = {}
-    peak = peaks()[0]
-    for name, fn in (("fused_allreduce_f32_64mib", rc.ring_allreduce_fused), ("psum_f32_64mib", rc.ring_psum)):
-        for _ in range(args.warmup):
-            bf.copy_(pr)
-            fn(bf, stream=stream)
-        torch.cuda.synchronize()
-        ev = []
-        for _ in range(args.steps):
-            bf.copy_(pr)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn(bf, stream=stream)
-            b.record(stream)
-            ev.append((a, b))
-        torch.cuda.synchronize()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-        gbs = min_bytes(P, N, 4) / (ms * 1e-3) / 1e9
-        out[name] = {"ms": round(ms, 4), "GB/s_min_bytes": round(gbs, 1), "frac_b": round(gbs / peak, 4),
-                     "ring_bytes_GB/s": round(ring_bytes(P, N, 4) / (ms * 1e-3) / 1e9, 1)}
-    return out
-
-
 def gemm_rs_secondary(rc, dev, stream, args):
     """Matmul + ring reduce-scatter at P=8, A [8192,512] and B [4096,512] per
     rank (bf16): the mirror of the all-gather + GEMM workload, 275 GFLOP."""
@@ -543,21 +511,111 @@ def gemm_rs_secondary(rc, dev, stream, args):
 
 
 def weak_sweep(rc, dev, stream, args):
-    """Chunk 4M fp32 per rank-step, P in {2,4,8,16,32}: time per ring step."""
+    """The weak-scaling workload: chunk N/P = 4M fp32 ~ U[-1,1) (seed 3), P in
+    {2,4,8,16,32}; per P the all-reduce time, the time per ring step
+    T/(2(P-1)), and GB/s and the fraction of the HBM roofline against the
+    minimum bytes 2*P*N*e.  The inputs are drawn on the device by a seeded
+    torch generator (timing does not depend on the values; parity at these
+    sizes is tested against the oracle with the host-drawn bytes)."""
     out = {}
+    peak = peaks()[0]
     for P in (2, 4, 8, 16, 32):
         N = (4 << 20) * P
-        x = synthetic.workload("weak", P=P)
-        pr = x.to(dev)
-        del x
+        g = torch.Generator(device=dev).manual_seed(3)
+        pr = torch.empty((P, N), dtype=torch.float32, device=dev).uniform_(-1.0, 1.0, generator=g)
         bf = torch.empty_like(pr)
-        ts = time_allreduce(rc, bf, pr, N, max(3, args.steps // 2), args.warmup, stream)
+        ts = time_allreduce(rc, bf, pr, N, max(3, min(args.steps, 10)), max(3, args.warmup), stream)
+        if rc.ring_status(stream) != 0:
+            raise RuntimeError(rc.ring_last_error())
         ms = statistics.mean(ts)
+        gb_min = min_bytes(P, N, 4) / (ms * 1e-3) / 1e9
         out[f"P{P}"] = {"ms": round(ms, 4), "us_per_step": round(1e3 * ms / (2 * (P - 1)), 2),
                         "per_rank_step_bytes": 5 * (4 << 20) * 4 // 2,
-                        "GB/s_ring_bytes": round(ring_bytes(P, N, 4) / (ms * 1e-3) / 1e9, 1)}
+                        "GB/s_ring_bytes": round(ring_bytes(P, N, 4) / (ms * 1e-3) / 1e9, 1),
+                        "GB/s_min_bytes": round(gb_min, 1), "frac": round(gb_min / peak, 4),
+                        "traffic": profiled_traffic("weak") if P == 8 else None}
         del pr, bf
         torch.cuda.empty_cache()
+    return out
+
+
+def ring_bound(rc, dev, stream, spec, ms):
+    """What bounds the ring all-reduce, measured in this run.
+    (1) The L2 step rates: the library's own copy and add loops
+    (ring_debug_l2_rate) over buffers that stay in L2 (16 MiB each), in the
+    ring's launch shape -- the fastest an all-gather step (copy) or a
+    reduce-scatter step (add) can move data that is already on chip.  The
+    schedule's bytes at those rates give the L2 floor of one all-reduce.
+    (2) Where the time of one traced all-reduce goes: per-step stamps of every
+    block (ring_debug_set_trace), as the share of block time spent waiting for
+    the left neighbour and the mean time of the first step, the other
+    reduce-scatter steps and the all-gather steps."""
+    nb = 16 << 20
+    a = torch.randn(nb // 4, device=dev)
+    b = torch.randn(nb // 4, device=dev)
+    d = torch.empty(nb // 4, device=dev)
+    reps = 200
+    rates = {}
+    for name, bb, factor in (("copy", None, 2), ("add", b, 3)):
+        rc.ring_debug_l2_rate(d, a, bb, reps=5, stream=stream)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(5):
+            x = torch.cuda.Event(enable_timing=True)
+            y = torch.cuda.Event(enable_timing=True)
+            x.record(stream)
+            rc.ring_debug_l2_rate(d, a, bb, reps=reps, stream=stream)
+            y.record(stream)
+            torch.cuda.synchronize()
+            t = x.elapsed_time(y)
+            best = t if best is None else min(best, t)
+        rates[name] = factor * nb * reps / (best * 1e-3) / 1e9
+    P, N, e = spec["P"], spec["N"], ES[spec["dtype"]]
+    c = N // P
+    rs_bytes = 3 * (P - 1) * P * c * e
+    ag_bytes = 2 * (P - 1) * P * c * e
+    floor_ms = (rs_bytes / rates["add"] + ag_bytes / rates["copy"]) / 1e6
+    out = {"l2_copy_GB/s": round(rates["copy"], 1), "l2_add_GB/s": round(rates["add"], 1),
+           "l2_floor_ms": round(floor_ms, 4), "frac_of_l2_floor": round(floor_ms / ms, 4),
+           "l2_probe": ("ring_debug_l2_rate: the ring's 32-byte vector copy / f32 add loop, 8 blocks x 128 "
+                        "threads per SM, 16 MiB buffers resident in L2, 200 passes per launch, best of 5"),
+           "l2_floor": "3(P-1)*N*e at the add rate + 2(P-1)*N*e at the copy rate (reduce-scatter + all-gather)"}
+    # (2) one traced all-reduce
+    x = host_workload(spec["name"], P=P, N=N)
+    if x is not None:
+        pr = x.to(dev)
+        nsteps = 2 * (P - 1)
+        words = 3 * nsteps * 8 * 1216 * 4   # generous: 3 stamps x steps x blocks (up to 4x the co-resident count)
+        tb = torch.zeros(words, dtype=torch.int64, device=dev)
+        rc.ring_allreduce(pr, stream=stream)     # warm
+        pr.copy_(x.to(dev))
+        torch.cuda.synchronize()
+        rc.ring_debug_set_trace(tb)
+        try:
+            rc.ring_allreduce(pr, stream=stream)
+            torch.cuda.synchronize()
+        finally:
+            rc.ring_debug_set_trace(None)
+        if rc.ring_status(stream) != 0:
+            raise RuntimeError(rc.ring_last_error())
+        st = tb.view(-1, nsteps, 3).cpu().numpy().astype("float64")
+        st = st[(st[:, :, 2] > 0).all(axis=1)]          # blocks that ran (all stamps written)
+        if len(st):
+            span = st[:, -1, 2] - st[:, 0, 0]
+            wait = (st[:, 1:, 1] - st[:, 1:, 0]).sum(axis=1)
+            step = st[:, :, 2] - st[:, :, 0]
+            out.update({
+                "trace_blocks": int(len(st)),
+                "wait_share": round(float((wait / span).mean()), 4),
+                "first_step_us": round(float(step[:, 0].mean()) / 1e3, 2),
+                "rs_step_us": round(float(step[:, 1:P - 1].mean()) / 1e3, 2),
+                "ag_step_us": round(float(step[:, P - 1:].mean()) / 1e3, 2),
+                "trace": ("one all-reduce with ring_debug_set_trace: per block, waits for the left neighbour "
+                          "(steps >= 1) over its first-wait-to-last-step span, mean over blocks; step times are "
+                          "wait start to step end, mean over blocks")})
+        del pr, tb
+    del a, b, d
+    torch.cuda.empty_cache()
     return out
 
 
@@ -571,7 +629,7 @@ def run_ours(args, spec, rank, world, dist):
     stream = torch.cuda.current_stream(dev)
     P, N, dt = spec["P"], spec["N"], spec["dtype"]
     e = ES[dt]
-    x = synthetic.workload(spec["name"], P=P, N=N)
+    x = host_workload(spec["name"], P=P, N=N)
     pristine = x.to(dev)
     bufs = torch.empty_like(pristine)
 
@@ -615,39 +673,33 @@ def run_ours(args, spec, rank, world, dist):
         raise RuntimeError(rc.ring_last_error())
 
     secondary = {}
+    if not args.no_secondary:
+        secondary["ring_bound"] = ring_bound(rc, dev, stream, spec, ms)
     if not args.no_secondary and spec["name"] == "f32_64mib":
-        # bf16 gradient-bucket workload: all-reduce and standalone reduce-scatter
+        # bf16 gradient-bucket workload: the all-reduce
         del h_in, h_out
-        xb = synthetic.workload("bf16_64mib")
+        xb = host_workload("bf16_64mib")
         pb = xb.to(dev)
         bb = torch.empty_like(pb)
         Nb = xb.shape[1]
         tb = time_allreduce(rc, bb, pb, Nb, args.steps, args.warmup, stream)
-        out = torch.empty((8, Nb // 8), dtype=torch.bfloat16, device=dev)
-        trs = time_reduce_scatter(rc, bb, out, pb, Nb, args.steps, args.warmup, stream)
-        tbi = time_reduce_scatter(rc, bb, out, pb, Nb, args.steps, args.warmup, stream,
-                                  fn=rc.ring_reduce_scatter_bidir)
         if rc.ring_status(stream) != 0:
             raise RuntimeError(rc.ring_last_error())
-        mb, mrs = statistics.mean(tb), statistics.mean(trs)
-        secondary = {
-            "bf16_64mib_allreduce": {"ms": round(mb, 4), "GB/s": round(ring_bytes(8, Nb, 2) / mb / 1e6, 1),
-                                     "frac_a": round(ring_bytes(8, Nb, 2) / mb / 1e6 / peaks()[0], 4)},
-            "bf16_64mib_reduce_scatter_bidir": {
-                "ms": round(statistics.mean(tbi), 4),
-                "GB/s": round(3 * 7 * Nb * 2 / statistics.mean(tbi) / 1e6, 1),
-                "note": "Pallas-style bidirectional reduce-scatter: P-1 steps, top halves left, bottoms right, last add stored in the owner's output"},
-            "bf16_64mib_reduce_scatter": {"ms": round(mrs, 4),
-                                          "GB/s": round(3 * 7 * Nb * 2 / mrs / 1e6, 1),
-                                          "frac_a": round(3 * 7 * Nb * 2 / mrs / 1e6 / peaks()[0], 4)},
-        }
-        del pb, bb, out
-
-    if not args.no_secondary and spec["name"] == "f32_64mib":
-        secondary.update(fold_secondary(rc, dev, stream, args))
+        mb = statistics.mean(tb)
+        secondary["bf16_64mib_allreduce"] = {
+            "ms": round(mb, 4), "GB/s": round(ring_bytes(8, Nb, 2) / mb / 1e6, 1),
+            "frac_a": round(ring_bytes(8, Nb, 2) / mb / 1e6 / peaks()[0], 4),
+            "frac": round(min_bytes(8, Nb, 2) / mb / 1e6 / peaks()[0], 4),
+            "traffic": profiled_traffic("bf16_64mib")}
+        del pb, bb
+        # every other HBM-bound row of the hot path, each against its own minimum bytes
+        for name in ROW_WORKLOADS:
+            rs = row_spec(rc, name, dev, stream)
+            secondary[name] = row_summary(rs, statistics.mean(row_time(rc, rs, args.steps, args.warmup, stream)))
+            del rs
+            torch.cuda.empty_cache()
         secondary.update(ag_gemm_secondary(rc, dev, stream, args))
         secondary.update(gemm_rs_secondary(rc, dev, stream, args))
-    if args.sweep:
         secondary["weak_scaling"] = weak_sweep(rc, dev, stream, args)
 
     if rank != 0:
@@ -745,30 +797,32 @@ def run_ag_gemm(args, rank, world, dist):
     return 0
 
 
-def run_row(args, rank, world, dist):
-    """--workload <row>: one HBM-bound row of the hot path on its own line,
-    timed like the headline (inputs resident, restored by a device copy
-    outside the events), against the row's algorithmic bytes."""
-    import ring_collectives_gb300 as rc
-    import __graft_entry__
-    __graft_entry__.build()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream(dev)
-    name = args.workload
+_HOST_INPUTS = {}
+
+
+def host_workload(name, **kw):
+    """Seeded host inputs, drawn once per process (several rows share them)."""
+    key = (name, tuple(sorted(kw.items())))
+    if key not in _HOST_INPUTS:
+        _HOST_INPUTS[key] = synthetic.workload(name, **kw)
+    return _HOST_INPUTS[key]
+
+
+def row_spec(rc, name, dev, stream):
+    """Device inputs, the call and the byte counts of one HBM-bound row of
+    the hot path (the --workload rows; the default line times them all)."""
     restore = True
     if name in ("fused_f32_64mib", "psum_f32_64mib", "ppermute_f32_64mib"):
-        x = synthetic.workload("f32_64mib")
+        x = host_workload("f32_64mib")
         e, dt = 4, "f32"
     elif name == "all_gather_f32_8mib":
-        x = synthetic.workload("f32_64mib", N=2 << 20)   # shards of 2M fp32 (8 MiB); outputs 64 MiB per rank
+        x = host_workload("f32_64mib", N=2 << 20)   # shards of 2M fp32 (8 MiB); outputs 64 MiB per rank
         e, dt = 4, "f32"
     else:
-        x = synthetic.workload("bf16_64mib")
+        x = host_workload("bf16_64mib")
         e, dt = 2, "bf16"
     P, N = x.shape
     pr = x.contiguous().to(dev)
-    del x
     bufs = torch.empty_like(pr)
     if name.startswith("fused") or name.startswith("psum"):
         fn = rc.ring_allreduce_fused if name.startswith("fused") else rc.ring_psum
@@ -786,19 +840,18 @@ def run_row(args, rank, world, dist):
         call = lambda: fn(bufs, out, stream=stream)   # noqa: E731
         row_min = (P + 1) * N * e   # read every slot once, write one chunk per rank
         row_min_text = "(P+1)*N*e: every slot read once, one reduced chunk written per rank"
+        alg = 3 * (P - 1) * N * e
+        sources = KERNEL_SOURCES
         if name == "reduce_scatter_bf16_64mib":
-            alg = 3 * (P - 1) * N * e
             alg_text = "3(P-1)*N*e (per rank P-1 steps of 2 chunk reads + 1 chunk write)"
             kern = "k_ring (reduce-scatter mode)"
             metric = "ring reduce_scatter GB/s (3(P-1)*N*e / time), P=8, 64 MiB/rank, bf16, 1xGB300 per replica"
         else:
-            alg = 3 * (P - 1) * N * e
             alg_text = ("3(P-1)*N*e (P-1 steps of 2 half-chunk reads + 1 write per direction; the last write "
                         "goes to the owner's output)")
             kern = "k_ring (bidirectional reduce-scatter mode)"
             metric = ("bidirectional reduce_scatter GB/s (3(P-1)*N*e / time), P=8, 64 MiB/rank, bf16, "
                       "1xGB300 per replica")
-        sources = KERNEL_SOURCES
     elif name == "ppermute_f32_64mib":
         restore = False
         call = lambda: rc.ring_ppermute_right(pr, bufs, stream=stream)   # noqa: E731
@@ -817,39 +870,75 @@ def run_row(args, rank, world, dist):
         alg_text = "2*P*n*e (own shard) + 2(P-1)*P*n*e (P-1 ring steps of a read and a write of n)"
         kern, sources = "k_ring (all-gather mode)", KERNEL_SOURCES
         metric = "ring all_gather GB/s (2P*n*e*P / time), P=8, 8 MiB shards, f32, 1xGB300 per replica"
-    for _ in range(args.warmup):
-        if restore:
-            bufs.copy_(pr)
-        call()
+    return dict(name=name, P=P, N=N, e=e, dt=dt, pr=pr, bufs=bufs, call=call, restore=restore, alg=alg,
+                alg_text=alg_text, row_min=row_min, row_min_text=row_min_text, kern=kern, sources=sources,
+                metric=metric)
+
+
+def row_time(rc, spec, steps, warmup, stream):
+    """Event times (ms) of `steps` calls after `warmup`; in-place inputs are
+    restored by a device copy before every call, outside the events."""
+    for _ in range(warmup):
+        if spec["restore"]:
+            spec["bufs"].copy_(spec["pr"])
+        spec["call"]()
     torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
     ev = []
-    with ClockSampler(dev.index) as clocks:
-        for _ in range(args.steps):
-            if restore:
-                bufs.copy_(pr)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            call()
-            b.record(stream)
-            ev.append((a, b))
-        torch.cuda.synchronize()
+    for _ in range(steps):
+        if spec["restore"]:
+            spec["bufs"].copy_(spec["pr"])
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        spec["call"]()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
     if rc.ring_status(stream) != 0:
         raise RuntimeError(rc.ring_last_error())
-    times = [a.elapsed_time(b) for a, b in ev]
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def row_summary(spec, ms):
+    """GB/s and roofline fractions of one row against its minimum bytes and
+    its schedule's bytes, with the DRAM traffic of its committed profile."""
+    peak = peaks()[0]
+    gbs_min = spec["row_min"] / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "GB/s_min_bytes": round(gbs_min, 1), "frac": round(gbs_min / peak, 4),
+            "GB/s_schedule_bytes": round(spec["alg"] / (ms * 1e-3) / 1e9, 1),
+            "frac_schedule_bytes": round(spec["alg"] / (ms * 1e-3) / 1e9 / peak, 4),
+            "min_bytes_per_launch": spec["row_min"], "min_bytes": spec["row_min_text"],
+            "traffic": profiled_traffic(spec["name"], spec["sources"], prefix=""),
+            "kernel": spec["kern"]}
+
+
+def run_row(args, rank, world, dist):
+    """--workload <row>: one HBM-bound row of the hot path on its own line,
+    timed like the headline (inputs resident, restored by a device copy
+    outside the events), against the row's algorithmic bytes."""
+    import ring_collectives_gb300 as rc
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    spec = row_spec(rc, args.workload, dev, stream)
+    if dist is not None:
+        dist.barrier()
+    with ClockSampler(dev.index) as clocks:
+        times = row_time(rc, spec, args.steps, args.warmup, stream)
     ms = statistics.mean(times)
     ms_max = max_over_ranks(ms, dist, dev)
     if rank != 0:
         return 0
     peak, peak_kind = peaks()
+    P, N, e, alg, row_min = spec["P"], spec["N"], spec["e"], spec["alg"], spec["row_min"]
     achieved = alg / (ms * 1e-3) / 1e9
     line = {
-        "metric": metric, "value": round(replicas_value(world, alg, ms_max), 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
-        "config": {"workload": name, "P": P, "N_per_rank": N, "bytes_per_rank": N * e, "replicas": world,
+        "metric": spec["metric"], "value": round(replicas_value(world, alg, ms_max), 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec["dt"], "data": "synthetic",
+        "config": {"workload": spec["name"], "P": P, "N_per_rank": N, "bytes_per_rank": N * e, "replicas": world,
                    "l2": ("inputs larger than L2; in-place inputs restored by a device copy before every "
                           "step, outside the events")},
         "frac_schedule_bytes": round(achieved / peak, 4),
@@ -858,10 +947,10 @@ def run_row(args, rank, world, dist):
         # the schedule's own byte count is reported beside it
         "roofline": {"bound": "hbm", "achieved": round(row_min / (ms * 1e-3) / 1e9, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(row_min / (ms * 1e-3) / 1e9 / peak, 4),
-                     "traffic": profiled_traffic(name, sources, prefix=""),
+                     "traffic": profiled_traffic(spec["name"], spec["sources"], prefix=""),
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs, burst copy)",
-                     "algorithmic_bytes_per_launch": row_min, "algorithmic_bytes": row_min_text,
-                     "schedule_bytes_per_launch": alg, "schedule_bytes": alg_text, "kernel": kern},
+                     "algorithmic_bytes_per_launch": row_min, "algorithmic_bytes": spec["row_min_text"],
+                     "schedule_bytes_per_launch": alg, "schedule_bytes": spec["alg_text"], "kernel": spec["kern"]},
         "gpu_launches": args.steps, "clocks": clocks.summary(),
         "ms_min": round(min(times), 4), "ms_median": round(statistics.median(times), 4),
     }

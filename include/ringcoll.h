@@ -342,6 +342,21 @@ int ring_debug_skip_notify(int rank, int step);
  */
 int ring_debug_set_trace(void *dev_buf, size_t bytes);
 
+/*
+ * Measurement hook: the step-rate ceiling of the ring kernels.  Runs the
+ * ring kernel's own streaming loop `reps` times over one range of `bytes`
+ * bytes, in one launch of the ring's shape (8 blocks of 128 threads per SM,
+ * block i taking the i-th equal share): add = 0 copies a to dst (an
+ * all-gather step: one read and one write per byte); add = 1 stores the f32
+ * sum a + b to dst (a reduce-scatter step: two reads and one write).  DEVICE
+ * pointers, 256-byte aligned, bytes a multiple of 256, dst overlapping
+ * neither input (RC_ERR_INVALID otherwise); 1 <= reps <= 100000.  With the
+ * buffers small enough to stay in L2 (together well under its size), the
+ * time of the launch gives the L2 rate that bounds a ring step whose data is
+ * already on chip.  Not part of any collective.
+ */
+int ring_debug_l2_rate(void *dst, const void *a, const void *b, size_t bytes, int reps, int add, void *stream);
+
 /* Frees the signal workspaces of all devices.  No call may be in flight. */
 int ring_finalize(void);
 

@@ -28,7 +28,7 @@ __all__ = [
     "ring_allreduce_fused", "ring_psum", "ring_allreduce_noalloc", "ag_gemm", "gemm_rs", "ring_status",
     "ring_status_ex",
     "ring_last_error", "ring_set_timeout_ms", "ring_set_slices", "ring_debug_skip_notify",
-    "ring_debug_set_trace", "ring_finalize", "library_path", "load",
+    "ring_debug_set_trace", "ring_debug_l2_rate", "ring_finalize", "library_path", "load",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -60,6 +60,7 @@ _SIGNATURES = {
     "ring_set_slices": ([_i], _i),
     "ring_debug_skip_notify": ([_i, _i], _i),
     "ring_debug_set_trace": ([_vp, _sz], _i),
+    "ring_debug_l2_rate": ([_vp, _vp, _vp, _sz, _i, _i, _vp], _i),
     "ring_finalize": ([], _i),
 }
 
@@ -318,6 +319,22 @@ def ring_debug_set_trace(buf) -> None:
         _check(fn(None, 0))
     else:
         _check(fn(buf.data_ptr(), buf.numel() * buf.element_size()))
+
+
+def ring_debug_l2_rate(dst: torch.Tensor, a: torch.Tensor, b: torch.Tensor | None = None, reps: int = 1,
+                       stream=None) -> None:
+    """The ring kernel's copy (b None) or f32 add (dst = a + b) loop, ``reps``
+    times over the bytes of ``dst`` in one launch (see include/ringcoll.h)."""
+    fn = load().ring_debug_l2_rate
+    for name, t in (("dst", dst), ("a", a)) + ((("b", b),) if b is not None else ()):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA tensor")
+    nb = dst.numel() * dst.element_size()
+    if a.numel() * a.element_size() < nb or (b is not None and b.numel() * b.element_size() < nb):
+        raise ValueError("inputs are shorter than dst")
+    with torch.cuda.device(dst.device):
+        _check(fn(dst.data_ptr(), a.data_ptr(), None if b is None else b.data_ptr(), nb, reps,
+                  0 if b is None else 1, _stream(stream, dst.device)))
 
 
 def ring_allreduce_noalloc(bufs: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:

@@ -416,6 +416,25 @@ int ring_debug_skip_notify(int rank, int step)
     return RC_OK;
 }
 
+int ring_debug_l2_rate(void *dst, const void *a, const void *b, size_t bytes, int reps, int add, void *stream)
+{
+    if (!dst || !a || (add && !b)) return fail(RC_ERR_INVALID, "null pointer");
+    if (reps < 1 || reps > 100000) return fail(RC_ERR_INVALID, "reps %d outside 1..100000", reps);
+    if (bytes % 256 || ((uintptr_t)dst | (uintptr_t)a | (uintptr_t)(add ? b : a)) % 256)
+        return fail(RC_ERR_INVALID, "pointers and size must be multiples of 256 bytes");
+    if (regions_overlap(dst, 0, bytes, a, 0, bytes, 1) || (add && regions_overlap(dst, 0, bytes, b, 0, bytes, 1)))
+        return fail(RC_ERR_INVALID, "dst overlaps an input");
+    if (bytes == 0) return RC_OK;
+    int dev;
+    DeviceState *st = nullptr;
+    int rc_ = current_device(&dev, &st);
+    if (rc_) return rc_;
+    cudaError_t e = rc::launch_l2_rate((char *)dst, (const char *)a, (const char *)b, bytes, reps, add ? 1 : 0,
+                                       st->sm_count, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "probe kernel launch");
+    return RC_OK;
+}
+
 int ring_debug_set_trace(void *dev_buf, size_t bytes)
 {
     if (!dev_buf) bytes = 0;

@@ -55,6 +55,9 @@ cudaError_t launch_fold(char *data, size_t stride, int P, size_t N, size_t chunk
                         cudaStream_t st);
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P,
                             size_t n, int esize, int sm_count, cudaStream_t st);
+// k_l2_rate: the ring's copy (add = 0) or f32 add (add = 1) loop, `reps` times over one range.
+cudaError_t launch_l2_rate(char *dst, const char *a, const char *b, size_t bytes, int reps, int add, int sm_count,
+                           cudaStream_t st);
 
 // Host helpers implemented in api.cu and shared with ag_gemm.cu.
 // set_error: records the calling thread's message; returns `code`.

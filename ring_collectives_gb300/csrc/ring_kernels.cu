@@ -596,6 +596,28 @@ __global__ void __launch_bounds__(256) k_ppermute(const char *src, size_t ss, ch
     if (b0 < b1) copy_range<ES, 256, kStEvictFirst>(d + b0 * ES, s + b0 * ES, b1 - b0);
 }
 
+// ------------------------------------------------------------ L2 step-rate probe
+// The ring's own streaming loops, run `reps` times over one range: with the
+// range's buffers resident in L2 this measures how fast an all-gather step
+// (copy: 1 read + 1 write) or a reduce-scatter step (add: 2 reads + 1 write)
+// can move data through L2, the ceiling of every ring step after the first.
+// Block i of the grid takes bytes [i*per, (i+1)*per) of the range.
+template <bool ADD>
+__global__ void __launch_bounds__(kRingThreads, RC_RING_MIN_BLOCKS)
+    k_l2_rate(char *dst, const char *a, const char *b, size_t bytes, size_t per, int reps)
+{
+    const size_t lo = (size_t)blockIdx.x * per;
+    if (lo >= bytes) return;
+    const size_t n = (bytes - lo < per ? bytes - lo : per) / 4;
+    for (int i = 0; i < reps; ++i) {
+        if (ADD)
+            add_range<0, kRingThreads, kStNormal>(dst + lo, a + lo, b + lo, n, false);
+        else
+            copy_range<4, kRingThreads, kStNormal>(dst + lo, a + lo, n);
+        __syncthreads();
+    }
+}
+
 // ------------------------------------------------------------ host launchers
 template <int DT, bool SERIAL>
 static const void *ring_fn_mode(int mode)
@@ -656,6 +678,20 @@ cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_
     const unsigned blocks = (unsigned)(p.P * p.S) * (p.mode == MODE_RS_BIDIR ? 2u : 1u);
     return cudaLaunchCooperativeKernel(ring_fn(dtype, copy.mode, copy.debug_serial != 0), dim3(blocks),
                                        dim3((unsigned)threads), args, ring_dyn_smem(copy.mode, copy.ag_bulk), st);
+}
+
+cudaError_t launch_l2_rate(char *dst, const char *a, const char *b, size_t bytes, int reps, int add, int sm_count,
+                           cudaStream_t st)
+{
+    // the ring's launch shape: RC_RING_MIN_BLOCKS blocks of kRingThreads per SM
+    const unsigned blocks = (unsigned)(sm_count * RC_RING_MIN_BLOCKS);
+    size_t per = (bytes + blocks - 1) / blocks;
+    per = (per + 255) & ~(size_t)255;   // whole 256-byte runs per block
+    if (add)
+        k_l2_rate<true><<<blocks, kRingThreads, 0, st>>>(dst, a, b, bytes, per, reps);
+    else
+        k_l2_rate<false><<<blocks, kRingThreads, 0, st>>>(dst, a, b, bytes, per, reps);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_ppermute(const char *src, size_t src_stride, char *dst, size_t dst_stride, int P, size_t n,

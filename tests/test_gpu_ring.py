@@ -757,3 +757,21 @@ def test_allreduce_replayed_from_a_cuda_graph():
         torch.cuda.synchronize()
         assert np.array_equal(np_of(b), want)
     ok_status()
+
+
+def test_l2_rate_probe_copies_and_adds_exactly():
+    """The measurement hook runs the ring's own copy and f32 add loops; after
+    any number of passes dst holds a copy of a, or the f32 sum a + b."""
+    n = (3 << 20) // 4 + 64 * 5          # not a multiple of the per-block share
+    a = torch.randn(n, device=DEV)
+    b = torch.randn(n, device=DEV)
+    d = torch.empty(n, device=DEV)
+    rc.ring_debug_l2_rate(d, a, None, reps=3)
+    torch.cuda.synchronize()
+    assert torch.equal(d, a)
+    rc.ring_debug_l2_rate(d, a, b, reps=2)
+    torch.cuda.synchronize()
+    want = (a.cpu().numpy() + b.cpu().numpy()).astype(np.float32)
+    assert np.array_equal(d.cpu().numpy(), want)
+    with pytest.raises(rc.RingError):
+        rc.ring_debug_l2_rate(d[1:], a[1:], None)    # not 256-byte aligned
