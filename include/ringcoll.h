@@ -325,20 +325,26 @@ int ring_set_slices(int slices);
  * notify that rank `rank` would send after global step `step`, in every
  * slice.  Its neighbour's bounded wait then runs out and ring_status() (or
  * ring_status_ex() for a caller's workspace) reports RC_ERR_TIMEOUT; no
- * fault is raised and the device stays usable.  (-1, -1) cancels a pending
- * skip.
+ * fault is raised and the device stays usable.  Where two ranks share a
+ * thread block (the all-reduce and reduce-scatter at even P), the hop
+ * between them needs no signal, so a skip aimed at either of them skips the
+ * block's notify to the next block.  (-1, -1) cancels a pending skip.
  */
 int ring_debug_skip_notify(int rank, int step);
 
 /*
  * Tracing hook: while dev_buf is set (a device buffer of `bytes` bytes), every
- * ring launch (the entry points listed for ring_debug_skip_notify) has
- * thread 0 of block b (rank b / slices, slice b % slices) write three
- * %globaltimer stamps (ns) per global step g at word (b*steps + g)*3: the
- * start of the wait on the left neighbour, its end, and the end of the step
- * (after the notify).  steps = 2(P-1) for the all-reduce, P-1 otherwise.
- * Blocks whose stamps would not fit write none.  NULL turns tracing off.
- * The caller owns the buffer and must keep it alive while launches use it.
+ * ring launch (the entry points listed for ring_debug_skip_notify) writes
+ * three %globaltimer stamps (ns) per rank, slice and global step g, at word
+ * (b*steps + g)*3 with b = (h*P + r)*slices + j for rank r, slice j and half
+ * h (h = 0 except in the bidirectional reduce-scatter): the start of the
+ * wait on the left neighbour, its end, and the end of the step (after the
+ * notify).  steps = 2(P-1) for the all-reduce, P-1 otherwise.  Where two
+ * ranks share a thread block (the all-reduce and reduce-scatter at even P),
+ * the second rank's step waits on no other block: its wait starts and ends
+ * when its step starts.  Rows whose stamps would not fit are not written.
+ * NULL turns tracing off.  The caller owns the buffer and must keep it alive
+ * while launches use it.
  */
 int ring_debug_set_trace(void *dev_buf, size_t bytes);
 

@@ -120,6 +120,26 @@ int ag_bulk_for(int mode)
     const int v = ag_bulk_setting();
     return v >= 0 ? v : (mode == rc::MODE_ALL_GATHER ? 1 : 0);
 }
+// Two logical ranks per thread block (k_ring_pair) for the all-reduce and the
+// reduce-scatter at even P; the hop inside a block hands the head of every
+// slice over in shared memory.  Knobs, read once: RC_RING_PAIR=0 keeps k_ring
+// (one rank per block) everywhere; RC_PAIR_SMEM = bytes handed over per block
+// (a multiple of 1024; unset or malformed = the default below).
+constexpr int kDefaultPairSmem = 44 << 10;
+int pair_enabled()
+{
+    static const int v = env_uint("RC_RING_PAIR", 1) != 0;
+    return v;
+}
+int pair_smem_bytes()
+{
+    static const int v = [] {
+        const unsigned x = env_uint("RC_PAIR_SMEM", (unsigned)kDefaultPairSmem);
+        return (x % 1024 == 0 && x <= (160u << 10)) ? (int)x : kDefaultPairSmem;
+    }();
+    return v;
+}
+
 // Debug knob, read once from the environment: RC_DEBUG_SERIAL=1 makes every
 // step of a ring launch also wait for all blocks of the launch (a bounded
 // grid barrier), ruling fine-grained synchronisation in or out as the cause
@@ -137,6 +157,7 @@ struct DeviceState {
     int supported = 0;  // 1 if sm_103 and cooperative launch are available
     int sm_count = 0;
     int max_blocks[3] = {0, 0, 0}; // co-resident ring blocks per dtype
+    int pair_blocks[3] = {0, 0, 0}; // co-resident k_ring_pair blocks per dtype (0: pair kernel unavailable)
     void *ws = nullptr;  // WsHeader followed by the signal words
     size_t ws_bytes = 0;
     uint64_t launches = 0;
@@ -203,6 +224,10 @@ int current_device(int *dev_out, DeviceState **st_out)
             for (int dt = 0; dt < 3; ++dt) {
                 e = rc::ring_max_coresident(dt, rc::kRingThreads, dev, &st.max_blocks[dt]);
                 if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+                if (pair_enabled()) {
+                    e = rc::ring_pair_max_coresident(dt, dev, pair_smem_bytes(), &st.pair_blocks[dt]);
+                    if (e != cudaSuccess) return cuda_fail(e, "occupancy query (pair kernel)");
+                }
             }
         }
         st.probed = true;
@@ -252,12 +277,13 @@ int ensure_workspace(DeviceState &st, size_t sig_bytes)
 }
 
 // Slices per rank for a chunk of chunk_bytes (see ring_set_slices).
-int choose_slices(const DeviceState &st, int dtype, int P, size_t chunk_elems, size_t chunk_bytes, int *S_out)
+// blocks: co-resident blocks of the kernel; per_slice: its blocks per slice ring.
+int choose_slices(int blocks, int per_slice, size_t chunk_elems, size_t chunk_bytes, int *S_out)
 {
-    const int cap = st.max_blocks[dtype] / P;
+    const int cap = blocks / per_slice;
     if (cap < 1)
-        return fail(RC_ERR_UNSUPPORTED, "P=%d ranks exceed the %d co-resident blocks of this device", P,
-                    st.max_blocks[dtype]);
+        return fail(RC_ERR_UNSUPPORTED, "%d blocks per slice exceed the %d co-resident blocks of this device",
+                    per_slice, blocks);
     long S;
     const int user = g_slices.load();
     if (user > 0) {
@@ -275,15 +301,35 @@ int choose_slices(const DeviceState &st, int dtype, int P, size_t chunk_elems, s
     return RC_OK;
 }
 
-// Chooses slices and segments of a ring launch (the same for every workspace).
+// k_ring_pair takes the all-reduce and the reduce-scatter at even P when
+// every slice starts on a 32-byte boundary (slot bases, strides and chunk
+// starts multiples of 32 bytes) and the all-gather steps use vector copies.
+bool pair_fits(const rc::RingParams &p, const DeviceState &st, int dtype, size_t es)
+{
+    if (!pair_enabled() || st.pair_blocks[dtype] < 1) return false;
+    if (p.mode != rc::MODE_ALLREDUCE && p.mode != rc::MODE_REDUCE_SCATTER) return false;
+    if (p.P < 2 || (p.P & 1) || p.ag_bulk) return false;
+    const size_t cs = p.chunk_stride ? p.chunk_stride : p.chunk;
+    if (((uintptr_t)p.data | p.data_stride | (cs * es)) & 31u) return false;
+    if (p.mode == rc::MODE_REDUCE_SCATTER && (((uintptr_t)p.out | p.out_stride) & 31u)) return false;
+    return true;
+}
+
+// Chooses the kernel, slices and segments of a ring launch (the same for every workspace).
 int plan_ring(rc::RingParams &p, int dtype, DeviceState *st)
 {
     int rc_ = RC_OK;
     const size_t es = elem_size(dtype);
+    p.ag_bulk = ag_bulk_for(p.mode);
+    p.pair = pair_fits(p, *st, dtype, es) ? 1 : 0;
+    p.hand_bytes = p.pair ? pair_smem_bytes() : 0;
     // The bidirectional reduce-scatter runs two rings (top and bottom halves) per slice.
     const int rings = p.mode == rc::MODE_RS_BIDIR ? 2 : 1;
     const size_t ring_elems = p.chunk / (size_t)rings;
-    rc_ = choose_slices(*st, dtype, p.P * rings, ring_elems, ring_elems * es, &p.S);
+    if (p.pair)
+        rc_ = choose_slices(st->pair_blocks[dtype], p.P / 2, ring_elems, ring_elems * es, &p.S);
+    else
+        rc_ = choose_slices(st->max_blocks[dtype], p.P * rings, ring_elems, ring_elems * es, &p.S);
     if (rc_) return rc_;
     {
         const size_t live = (size_t)p.P * p.chunk * es, budget = l2_live_bytes();
@@ -295,7 +341,6 @@ int plan_ring(rc::RingParams &p, int dtype, DeviceState *st)
         if (G < 1) G = 1;
         p.segments = (int)G;
     }
-    p.ag_bulk = ag_bulk_for(p.mode);
     if (p.chunk_stride == 0) p.chunk_stride = p.chunk;
     set_stagger(p, es);
     return rc_;
@@ -335,7 +380,7 @@ int run_ring(rc::RingParams &p, int dtype, cudaStream_t st_cuda, void *ext_ws = 
     p.trace = g_trace.load();
     p.trace_words = g_trace_words.load();
     p.debug_serial = debug_serial();
-    cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, st_cuda);
+    cudaError_t e = p.pair ? rc::launch_ring_pair(p, dtype, st_cuda) : rc::launch_ring(p, dtype, rc::kRingThreads, st_cuda);
     if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
     if (!ext_ws) st->launches += (uint64_t)p.segments; // the launch advances the epoch by its segment count
     return RC_OK;
@@ -926,7 +971,7 @@ int ring_allreduce_noalloc(void *bufs_base, size_t stride, int P, size_t N, int 
     p.trace = g_trace.load();
     p.trace_words = g_trace_words.load();
     p.debug_serial = debug_serial();
-    cudaError_t e = rc::launch_ring(p, dtype, rc::kRingThreads, s);
+    cudaError_t e = p.pair ? rc::launch_ring_pair(p, dtype, s) : rc::launch_ring(p, dtype, rc::kRingThreads, s);
     if (e != cudaSuccess) return cuda_fail(e, "ring kernel launch");
     na.launches += (uint64_t)p.segments; // the launch advances the epoch by its segment count
     return RC_OK;

@@ -105,6 +105,17 @@ __device__ __forceinline__ void ld8_ef(const void *p, uint4 &a, uint4 &b)
                  : "memory");
 }
 
+// ld8_ef issued only when `valid` is non-zero (a PTX predicate); otherwise a
+// and b are left as they were.
+__device__ __forceinline__ void ld8_ef_if(const void *p, uint32_t valid, uint4 &a, uint4 &b)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %9, 0;\n\t"
+                 "@q ld.global.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t}"
+                 : "+r"(a.x), "+r"(a.y), "+r"(a.z), "+r"(a.w), "+r"(b.x), "+r"(b.y), "+r"(b.z), "+r"(b.w)
+                 : "l"(p), "r"(valid)
+                 : "memory");
+}
+
 // Store policies: kStNormal (output read by a neighbour next step), kStEvictFirst
 // (nothing reads it again in this launch), kStEvictLast (a reduce-scatter
 // partial: it must survive in L2 until the right neighbour reads it, which then

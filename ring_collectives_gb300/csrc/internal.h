@@ -42,6 +42,8 @@ struct RingParams {
     int stagger_groups;  // > 1: slice j starts (j % stagger_groups) * stagger_ns later (phase-shifted rings)
     unsigned stagger_ns;
     int skip_rank, skip_step; // test hook: this rank skips its notify after this step (-1: none)
+    int pair;            // 1: k_ring_pair (two ranks per thread block), else k_ring
+    int hand_bytes;      // k_ring_pair: shared-memory bytes per block handed from rank r0 to r1 (multiple of 1024)
     unsigned long long timeout_ns;
     unsigned long long *trace; // optional step stamps (see ring_debug_set_trace); null: off
     size_t trace_words;
@@ -50,6 +52,9 @@ struct RingParams {
 // Launch helpers implemented in ring_kernels.cu.  They return a cudaError_t.
 cudaError_t launch_ring(const RingParams &p, int dtype, int threads, cudaStream_t st);
 cudaError_t ring_max_coresident(int dtype, int threads, int device, int *blocks);
+// ring_pair.cu: the same engine with two logical ranks per thread block.
+cudaError_t launch_ring_pair(const RingParams &p, int dtype, cudaStream_t st);
+cudaError_t ring_pair_max_coresident(int dtype, int device, int hand_bytes, int *blocks);
 // fold_kernels.cu: order 0 = ring order (fused single-pass all-reduce), 1 = psum order.
 cudaError_t launch_fold(char *data, size_t stride, int P, size_t N, size_t chunk, int dtype, int order, int sm_count,
                         cudaStream_t st);
@@ -99,6 +104,15 @@ int prepare_workspace(size_t sig_words, WsHeader **hdr, uint32_t **sig, int *sm_
 #define RC_PPERMUTE_BLOCKS_PER_SM 8
 #endif
 constexpr int kRingThreads = RC_RING_THREADS;
+// Threads per block and blocks per SM of k_ring_pair (two ranks per block,
+// so the same thread count per SM as k_ring's 8 x 128).
+#ifndef RC_PAIR_THREADS
+#define RC_PAIR_THREADS 256
+#endif
+#ifndef RC_PAIR_MIN_BLOCKS
+#define RC_PAIR_MIN_BLOCKS 4
+#endif
+constexpr int kPairThreads = RC_PAIR_THREADS;
 // Slices start on multiples of this many elements (keeps 16-byte vectors aligned).
 constexpr size_t kSliceGranule = 64;
 // Bulk-copy staging of the ring's all-gather copies: stages x bytes of

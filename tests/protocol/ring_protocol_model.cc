@@ -17,6 +17,12 @@
 // section 4 (top halves travel left, bottom halves right, P-1 steps; the
 // last add stores the finished half straight into its owner's output).
 //
+// Modes allreduce_pair and reduce_scatter_pair model the variant with two
+// ranks per thread block (k_ring_pair): thread m plays ranks 2m and 2m+1,
+// does rank 2m+1's step before waiting on thread m-1, hands the head of
+// every slice from rank 2m to rank 2m+1 in thread-private memory (the
+// kernel's shared memory), and signals only between threads.
+//
 // Integer adds make every order give the same sum, so the model also checks
 // its results against plain sums.  Variant "early_notify" signals before the
 // step's stores (a planted protocol error that ThreadSanitizer must report);
@@ -24,7 +30,7 @@
 // kernel's phase-shifted slice rings.
 //
 // Usage: ring_protocol_model MODE P S SEGMENTS LAUNCHES N_PER_RANK [early_notify|stagger]
-//   MODE: allreduce | reduce_scatter | all_gather | rs_bidir
+//   MODE: allreduce | reduce_scatter | all_gather | rs_bidir | allreduce_pair | reduce_scatter_pair
 // Exit status 0 with "ok" when every launch produced the expected result.
 #include <atomic>
 #include <chrono>
@@ -42,6 +48,7 @@ enum Mode { ALLREDUCE, REDUCE_SCATTER, ALL_GATHER, RS_BIDIR };
 
 struct Launch {
     Mode mode;
+    bool pair;
     int P, S, segments, rows, nsteps;
     size_t chunk;                       // elements per chunk (all-gather: shard length)
     uint32_t *data;                     // P slots (all-gather: the outputs)
@@ -130,6 +137,86 @@ void block(const Launch &L, int h, int r, int j)
     }
 }
 
+void pair_block(const Launch &L, int m, int j)
+{
+    const int P = L.P, S = L.S;
+    const int r0 = 2 * m, r1 = 2 * m + 1, lrank = (r0 - 1 + P) % P, rrank = (r1 + 1) % P;
+    const uint32_t E0 = L.epoch->load(std::memory_order_relaxed);
+    if (L.stagger && j % 3) std::this_thread::sleep_for(std::chrono::microseconds(50 * (j % 3)));
+    std::atomic<uint32_t> *my_rows = L.sig + ((size_t)j * P + r0) * L.rows * P;
+    std::atomic<uint32_t> *to_rows = L.sig + ((size_t)j * P + rrank) * L.rows * P;
+    const size_t c = L.chunk;
+    uint32_t *s0 = L.data + (size_t)r0 * L.stride, *s1 = L.data + (size_t)r1 * L.stride;
+    const uint32_t *sl = L.data + (size_t)lrank * L.stride;
+    std::vector<uint32_t> hand;
+    for (int q = 0; q < L.segments; ++q) {
+        const size_t seg_lo = part_begin(c, q, L.segments);
+        const size_t seg_n = part_begin(c, q + 1, L.segments) - seg_lo;
+        const size_t lo = seg_lo + part_begin(seg_n, j, S);
+        const size_t n = seg_lo + part_begin(seg_n, j + 1, S) - lo;
+        const uint32_t V = E0 + 1u + (uint32_t)q;
+        const size_t h = n / 2;   // head of the slice handed from rank r0 to r1 in private memory
+        hand.assign(h, 0u);
+        auto notify = [&](int row) { to_rows[(size_t)row * P + r1].store(V, std::memory_order_release); };
+        for (int g = 0; g < L.nsteps; ++g) {
+            const bool notify_next = g + 1 < L.nsteps;
+            const bool last = g == L.nsteps - 1;
+            if (L.early_notify && notify_next) notify(g + 1);
+            // rank r1: needs only rank r0's previous step (this thread)
+            if (g < P - 1) {
+                const int k = (r1 - g - 2 + 2 * P) % P;
+                uint32_t *dst = (L.mode == REDUCE_SCATTER && g == P - 2) ? L.out + (size_t)r1 * c : s1 + (size_t)k * c;
+                for (size_t i = 0; i < n; ++i) {
+                    const uint32_t a = (i < h && g >= 1) ? hand[i] : s0[(size_t)k * c + lo + i];
+                    dst[lo + i] = a + s1[(size_t)k * c + lo + i];
+                }
+            } else {
+                const int k = (r1 - 1 - (g - (P - 1)) + 2 * P) % P;
+                for (size_t i = 0; i < n; ++i) s1[(size_t)k * c + lo + i] = i < h ? hand[i] : s0[(size_t)k * c + lo + i];
+            }
+            if (!L.early_notify && notify_next) notify(g + 1);
+            // rank r0: waits for thread m-1 (rank r0's left neighbour)
+            if (g > 0) {
+                std::atomic<uint32_t> &f = my_rows[(size_t)g * P + lrank];
+                for (long spins = 0; !reached(f.load(std::memory_order_acquire), V); ++spins) {
+                    if (spins > 400000000L) {
+                        std::fprintf(stderr, "wait gave up: pair %d step %d slice %d\n", m, g, j);
+                        std::exit(3);
+                    }
+                    std::this_thread::yield();
+                }
+            }
+            if (g < P - 1) {
+                const int k = (r0 - g - 2 + 2 * P) % P;
+                for (size_t i = 0; i < n; ++i) {
+                    const uint32_t v = sl[(size_t)k * c + lo + i] + s0[(size_t)k * c + lo + i];
+                    if (L.mode == REDUCE_SCATTER && g == P - 2) {
+                        L.out[(size_t)r0 * c + lo + i] = v;
+                    } else if (g == P - 2) {
+                        s0[(size_t)k * c + lo + i] = v;
+                        if (i < h) hand[i] = v;
+                    } else if (i < h) {
+                        hand[i] = v;
+                    } else {
+                        s0[(size_t)k * c + lo + i] = v;
+                    }
+                }
+            } else {
+                const int k = (r0 - 1 - (g - (P - 1)) + 2 * P) % P;
+                for (size_t i = 0; i < n; ++i) {
+                    const uint32_t v = sl[(size_t)k * c + lo + i];
+                    s0[(size_t)k * c + lo + i] = v;
+                    if (i < h && !last) hand[i] = v;
+                }
+            }
+        }
+    }
+    if (L.done->fetch_add(1, std::memory_order_acq_rel) == (uint32_t)L.total_threads - 1) {
+        L.done->store(0, std::memory_order_relaxed);
+        L.epoch->store(E0 + (uint32_t)L.segments, std::memory_order_release);
+    }
+}
+
 } // namespace
 
 int main(int argc, char **argv)
@@ -139,13 +226,16 @@ int main(int argc, char **argv)
         return 2;
     }
     const std::string ms = argv[1];
-    const Mode mode = ms == "allreduce" ? ALLREDUCE : ms == "reduce_scatter" ? REDUCE_SCATTER
+    const bool pair = ms == "allreduce_pair" || ms == "reduce_scatter_pair";
+    const Mode mode = (ms == "allreduce" || ms == "allreduce_pair") ? ALLREDUCE
+                      : (ms == "reduce_scatter" || ms == "reduce_scatter_pair") ? REDUCE_SCATTER
                       : ms == "all_gather" ? ALL_GATHER : RS_BIDIR;
     const int P = std::atoi(argv[2]), S = std::atoi(argv[3]), G = std::atoi(argv[4]), launches = std::atoi(argv[5]);
     const size_t npr = (size_t)std::atoll(argv[6]);
     const bool early = argc > 7 && std::string(argv[7]) == "early_notify";
     const bool stagger = argc > 7 && std::string(argv[7]) == "stagger";
     if (P < 2 || S < 1 || G < 1 || launches < 1 || (mode != ALL_GATHER && npr % (size_t)P)) return 2;
+    if (pair && (P & 1)) return 2;
     const size_t chunk = mode == ALL_GATHER ? npr : npr / (size_t)P;
     const size_t slot = mode == ALL_GATHER ? (size_t)P * npr : npr;
     const int halves = mode == RS_BIDIR ? 2 : 1;
@@ -171,12 +261,17 @@ int main(int argc, char **argv)
         } else {
             data = x;
         }
-        Launch L{mode, P, S, G, rows, nsteps, chunk, data.data(), slot, in.data(), out.data(), sig.data(),
-                 &epoch, &done, P * S * halves, early, stagger};
+        Launch L{mode, pair, P, S, G, rows, nsteps, chunk, data.data(), slot, in.data(), out.data(), sig.data(),
+                 &epoch, &done, pair ? P / 2 * S : P * S * halves, early, stagger};
         std::vector<std::thread> th;
-        for (int h = 0; h < halves; ++h)
-            for (int r = 0; r < P; ++r)
-                for (int j = 0; j < S; ++j) th.emplace_back(block, std::cref(L), h, r, j);
+        if (pair) {
+            for (int m = 0; m < P / 2; ++m)
+                for (int j = 0; j < S; ++j) th.emplace_back(pair_block, std::cref(L), m, j);
+        } else {
+            for (int h = 0; h < halves; ++h)
+                for (int r = 0; r < P; ++r)
+                    for (int j = 0; j < S; ++j) th.emplace_back(block, std::cref(L), h, r, j);
+        }
         for (auto &t : th) t.join();
         // expected results: plain sums / copies
         for (size_t i = 0; i < (mode == ALL_GATHER ? 0 : npr); ++i) {
