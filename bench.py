@@ -44,7 +44,8 @@ if ROOT not in sys.path:
 from ring_collectives_gb300 import synthetic  # noqa: E402
 
 ES = {"f32": 4, "bf16": 2}
-KERNEL_SOURCES = ["ring_collectives_gb300/csrc/ring_kernels.cu", "ring_collectives_gb300/csrc/dev.cuh",
+KERNEL_SOURCES = ["ring_collectives_gb300/csrc/ring_kernels.cu", "ring_collectives_gb300/csrc/ring_pair.cu",
+                  "ring_collectives_gb300/csrc/ring_common.cuh", "ring_collectives_gb300/csrc/dev.cuh",
                   "ring_collectives_gb300/csrc/internal.h", "ring_collectives_gb300/csrc/api.cu",
                   "ring_collectives_gb300/csrc/tc.cuh"]
 FOLD_SOURCES = ["ring_collectives_gb300/csrc/fold_kernels.cu", "ring_collectives_gb300/csrc/dev.cuh",
