@@ -30,7 +30,11 @@
  *     demand and released by ring_finalize().  Make the first call (at the
  *     largest P used) before capturing calls into a CUDA graph.  Calls that
  *     share a device's workspace must not run concurrently: issue them on one
- *     stream, or order the streams.
+ *     stream, or order the streams.  Every collective that signals also has
+ *     an _ex variant taking a caller-owned workspace instead (sized by its
+ *     *_workspace_bytes function, zeroed once before first use); calls with
+ *     different workspaces may run concurrently on different streams, and a
+ *     device timeout of such a call is read with ring_status_ex().
  *   - Return values are rc_status codes; ring_last_error() describes the most
  *     recent failure of the calling thread.
  *   - NaN.  The floating-point collectives are bit-identical to the fold
@@ -91,6 +95,23 @@ int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_
                     int P, size_t n, int dtype, void *stream);
 
 /*
+ * ring_all_gather_ex -- ring_all_gather with a caller-owned signal workspace:
+ * DEVICE memory of ws_bytes bytes, 16-byte aligned, zeroed once before its
+ * first use and otherwise left to the library; calls sharing one must be
+ * stream-ordered, calls with different workspaces may run concurrently
+ * (re-zero it, with no call in flight, before about 2^30 calls).  ws_bytes
+ * below ring_all_gather_workspace_bytes(P, n, dtype) gives RC_ERR_INVALID;
+ * device timeouts are read with ring_status_ex(workspace, stream).
+ * Arguments, validation and result as ring_all_gather.
+ */
+int ring_all_gather_ex(const void *in_base, size_t in_stride, void *out_base, size_t out_stride, int P, size_t n,
+                       int dtype, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes ring_all_gather_ex needs for (P, n, dtype) on the current
+ * device; 0 for invalid arguments or when no sm_103 device is current. */
+size_t ring_all_gather_workspace_bytes(int P, size_t n, int dtype);
+
+/*
  * ring_reduce_scatter -- rank r ends with the sum over ranks of chunk r.
  * "TPU 与分布式通信原语", section "reduce-scatter 与 all-gather" (the ring
  * reduce-scatter kernel, whose last step writes out_ref), with the round
@@ -112,6 +133,19 @@ int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_
  */
 int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride,
                         int P, size_t N, int dtype, void *stream);
+
+/*
+ * ring_reduce_scatter_ex -- ring_reduce_scatter with a caller-owned signal
+ * workspace (rules as for ring_all_gather_ex; size from
+ * ring_reduce_scatter_workspace_bytes).  Arguments, validation and result as
+ * ring_reduce_scatter.
+ */
+int ring_reduce_scatter_ex(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P, size_t N,
+                           int dtype, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes ring_reduce_scatter_ex needs for (P, N, dtype) on the
+ * current device; 0 for invalid arguments or no sm_103 device. */
+size_t ring_reduce_scatter_workspace_bytes(int P, size_t N, int dtype);
 
 /*
  * ring_reduce_scatter_bidir -- bidirectional reduce-scatter of "Pallas TPU
@@ -136,6 +170,18 @@ int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, siz
  */
 int ring_reduce_scatter_bidir(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P,
                               size_t N, int dtype, void *stream);
+
+/*
+ * ring_reduce_scatter_bidir_ex -- ring_reduce_scatter_bidir with a
+ * caller-owned signal workspace (rules as for ring_all_gather_ex; size from
+ * ring_reduce_scatter_bidir_workspace_bytes).
+ */
+int ring_reduce_scatter_bidir_ex(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P,
+                                 size_t N, int dtype, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes ring_reduce_scatter_bidir_ex needs; 0 for invalid
+ * arguments or no sm_103 device. */
+size_t ring_reduce_scatter_bidir_workspace_bytes(int P, size_t N, int dtype);
 
 /*
  * ring_allreduce -- in-place ring all-reduce: reduce-scatter (P-1 rounds)
@@ -248,6 +294,21 @@ int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, const void 
             int P, int rank, int M_r, int N, int K, void *stream);
 
 /*
+ * ag_gemm_ex -- ag_gemm with a caller-owned workspace holding the launch
+ * epoch, the status header and one ready flag per 16 gathered rows (rules as
+ * for ring_all_gather_ex; size from ag_gemm_workspace_bytes(P, M_r)).  With
+ * different workspaces, ag_gemm_ex calls may be issued on different streams;
+ * each launch fills the GPU, so concurrent calls mostly run one after the
+ * other.  Arguments, validation and result as ag_gemm.
+ */
+int ag_gemm_ex(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P, int rank,
+               int M_r, int N, int K, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes ag_gemm_ex needs: 128 + 4 * P * M_r / 16; 0 when P or M_r
+ * is invalid (M_r must be a multiple of 128). */
+size_t ag_gemm_workspace_bytes(int P, int M_r);
+
+/*
  * gemm_rs -- matmul followed by a ring reduce-scatter over output columns.
  * "TPU 与分布式通信原语", section "collective matmul" (matmul-reduce-scatter:
  * each rank's partial product is cast to bf16, laid out chunk-major by output
@@ -272,6 +333,18 @@ int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_stride, void
             int P, int M, int N, int K, void *stream);
 
 /*
+ * gemm_rs_ex -- gemm_rs with a caller-owned workspace, which holds only the
+ * launch's status header (rules as for ring_all_gather_ex; size from
+ * gemm_rs_workspace_bytes).  Arguments, validation and result as gemm_rs.
+ */
+int gemm_rs_ex(const void *A, size_t a_stride, const void *B, size_t b_stride, void *out, size_t out_stride, int P,
+               int M, int N, int K, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes gemm_rs_ex needs (the 128-byte header); 0 for invalid
+ * arguments. */
+size_t gemm_rs_workspace_bytes(int P, int M, int N, int K);
+
+/*
  * ring_status -- waits for `stream`, then returns and clears the device
  * status of the library's own signal areas on the calling device: the
  * workspace of the regular entry points and the fixed array of
@@ -286,7 +359,7 @@ int ring_status(void *stream);
 
 /*
  * ring_status_ex -- ring_status for a caller-owned workspace (the one given
- * to ring_allreduce_ex): waits for `stream`, then returns and clears the
+ * to an _ex entry point): waits for `stream`, then returns and clears the
  * status recorded in `workspace` (DEVICE pointer, 16-byte aligned; null or
  * misaligned gives RC_ERR_INVALID).  RC_OK or RC_ERR_TIMEOUT as above.
  */

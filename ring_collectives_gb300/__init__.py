@@ -26,7 +26,9 @@ __all__ = [
     "RingError", "ring_ppermute_right", "ring_all_gather", "ring_reduce_scatter", "ring_reduce_scatter_bidir",
     "ring_allreduce", "ring_allreduce_ex", "ring_allreduce_workspace_bytes", "ring_allreduce_host",
     "ring_allreduce_fused", "ring_psum", "ring_allreduce_noalloc", "ag_gemm", "gemm_rs", "ring_status",
-    "ring_status_ex",
+    "ring_status_ex", "ring_all_gather_ex", "ring_all_gather_workspace_bytes", "ring_reduce_scatter_ex",
+    "ring_reduce_scatter_workspace_bytes", "ring_reduce_scatter_bidir_ex", "ring_reduce_scatter_bidir_workspace_bytes",
+    "ag_gemm_ex", "ag_gemm_workspace_bytes", "gemm_rs_ex", "gemm_rs_workspace_bytes",
     "ring_last_error", "ring_set_timeout_ms", "ring_set_slices", "ring_debug_skip_notify",
     "ring_debug_set_trace", "ring_debug_l2_rate", "ring_finalize", "library_path", "load",
 ]
@@ -42,6 +44,16 @@ _vp, _sz, _i, _u = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint
 _SIGNATURES = {
     "ring_ppermute_right": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp], _i),
     "ring_all_gather": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp], _i),
+    "ring_all_gather_ex": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp, _sz, _vp], _i),
+    "ring_all_gather_workspace_bytes": ([_i, _sz, _i], _sz),
+    "ring_reduce_scatter_ex": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp, _sz, _vp], _i),
+    "ring_reduce_scatter_workspace_bytes": ([_i, _sz, _i], _sz),
+    "ring_reduce_scatter_bidir_ex": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp, _sz, _vp], _i),
+    "ring_reduce_scatter_bidir_workspace_bytes": ([_i, _sz, _i], _sz),
+    "ag_gemm_ex": ([_vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp], _i),
+    "ag_gemm_workspace_bytes": ([_i, _i], _sz),
+    "gemm_rs_ex": ([_vp, _sz, _vp, _sz, _vp, _sz, _i, _i, _i, _i, _vp, _sz, _vp], _i),
+    "gemm_rs_workspace_bytes": ([_i, _i, _i, _i], _sz),
     "ring_reduce_scatter": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp], _i),
     "ring_reduce_scatter_bidir": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp], _i),
     "ring_allreduce": ([_vp, _sz, _i, _sz, _i, _vp], _i),
@@ -199,6 +211,65 @@ def ring_allreduce_ex(bufs: torch.Tensor, workspace: torch.Tensor, N: int | None
     return bufs
 
 
+def _ws(workspace):
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def ring_all_gather_workspace_bytes(P: int, n: int, dtype=torch.float32) -> int:
+    return int(load().ring_all_gather_workspace_bytes(P, n, _DTYPE[dtype]))
+
+
+def ring_all_gather_ex(inp: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor, n: int | None = None,
+                       stream=None) -> torch.Tensor:
+    """ring_all_gather with a caller-owned workspace (zeroed CUDA tensor of at
+    least ring_all_gather_workspace_bytes bytes)."""
+    ip, is_, dt = _slots(inp, "inp")
+    op, os_, dt2 = _slots(out, "out")
+    if dt != dt2 or inp.size(0) != out.size(0):
+        raise ValueError("inp and out differ in dtype or rank count")
+    n = inp.size(1) if n is None else n
+    if out.size(1) < inp.size(0) * n:
+        raise ValueError("out rows are shorter than P*n")
+    wp, wb = _ws(workspace)
+    with torch.cuda.device(inp.device):
+        _check(load().ring_all_gather_ex(ip, is_, op, os_, inp.size(0), n, dt, wp, wb, _stream(stream, inp.device)))
+    return out
+
+
+def ring_reduce_scatter_workspace_bytes(P: int, N: int, dtype=torch.float32) -> int:
+    return int(load().ring_reduce_scatter_workspace_bytes(P, N, _DTYPE[dtype]))
+
+
+def ring_reduce_scatter_bidir_workspace_bytes(P: int, N: int, dtype=torch.float32) -> int:
+    return int(load().ring_reduce_scatter_bidir_workspace_bytes(P, N, _DTYPE[dtype]))
+
+
+def _rs_ex(fn, bufs, out, workspace, N, stream):
+    bp, bs, dt = _slots(bufs, "bufs")
+    op, os_, dt2 = _slots(out, "out")
+    if dt != dt2 or bufs.size(0) != out.size(0):
+        raise ValueError("bufs and out differ in dtype or rank count")
+    N = bufs.size(1) if N is None else N
+    wp, wb = _ws(workspace)
+    with torch.cuda.device(bufs.device):
+        _check(fn(bp, bs, op, os_, bufs.size(0), N, dt, wp, wb, _stream(stream, bufs.device)))
+    return out
+
+
+def ring_reduce_scatter_ex(bufs: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor, N: int | None = None,
+                           stream=None) -> torch.Tensor:
+    """ring_reduce_scatter with a caller-owned workspace; ``bufs`` is clobbered."""
+    return _rs_ex(load().ring_reduce_scatter_ex, bufs, out, workspace, N, stream)
+
+
+def ring_reduce_scatter_bidir_ex(bufs: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                                 N: int | None = None, stream=None) -> torch.Tensor:
+    """ring_reduce_scatter_bidir with a caller-owned workspace; ``bufs`` is clobbered."""
+    return _rs_ex(load().ring_reduce_scatter_bidir_ex, bufs, out, workspace, N, stream)
+
+
 def ring_allreduce_fused(bufs: torch.Tensor, N: int | None = None, stream=None) -> torch.Tensor:
     """Single-pass all-reduce with the ring's result (bit-identical to ring_allreduce)."""
     fn = load().ring_allreduce_fused
@@ -260,6 +331,56 @@ def ag_gemm(a_shards: torch.Tensor, a_gathered: torch.Tensor, B: torch.Tensor, C
         _check(load().ag_gemm(a_shards.data_ptr(), a_shards.stride(0) * 2, a_gathered.data_ptr(), B.data_ptr(),
                               C.data_ptr(), P, rank, M_r, N, K, _stream(stream, a_shards.device)))
     return C
+
+
+def ag_gemm_workspace_bytes(P: int, M_r: int) -> int:
+    return int(load().ag_gemm_workspace_bytes(P, M_r))
+
+
+def ag_gemm_ex(a_shards: torch.Tensor, a_gathered: torch.Tensor, B: torch.Tensor, C: torch.Tensor, rank: int,
+               workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """ag_gemm with a caller-owned workspace (zeroed CUDA tensor of at least
+    ag_gemm_workspace_bytes(P, M_r) bytes)."""
+    for name, t in (("a_shards", a_shards), ("a_gathered", a_gathered), ("B", B), ("C", C)):
+        if not t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+    if a_shards.dim() != 3 or a_shards.stride(2) != 1 or a_shards.stride(1) != a_shards.size(2):
+        raise ValueError("a_shards must be [P, M_r, K] with row-major shards")
+    P, M_r, K = a_shards.shape
+    N = B.size(0)
+    if tuple(a_gathered.shape) != (P * M_r, K) or not a_gathered.is_contiguous():
+        raise ValueError("a_gathered must be contiguous [P*M_r, K]")
+    if tuple(B.shape) != (N, K) or not B.is_contiguous():
+        raise ValueError("B must be contiguous [N, K]")
+    if tuple(C.shape) != (P * M_r, N) or not C.is_contiguous():
+        raise ValueError("C must be contiguous [P*M_r, N]")
+    wp, wb = _ws(workspace)
+    with torch.cuda.device(a_shards.device):
+        _check(load().ag_gemm_ex(a_shards.data_ptr(), a_shards.stride(0) * 2, a_gathered.data_ptr(), B.data_ptr(),
+                                 C.data_ptr(), P, rank, M_r, N, K, wp, wb, _stream(stream, a_shards.device)))
+    return C
+
+
+def gemm_rs_workspace_bytes(P: int, M: int, N: int, K: int) -> int:
+    return int(load().gemm_rs_workspace_bytes(P, M, N, K))
+
+
+def gemm_rs_ex(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+               stream=None) -> torch.Tensor:
+    """gemm_rs with a caller-owned workspace (zeroed CUDA tensor of at least
+    gemm_rs_workspace_bytes bytes)."""
+    for name, t in (("A", A), ("B", B), ("out", out)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous 3-D bf16 CUDA tensor")
+    P, M, K = A.shape
+    N = B.size(1)
+    if B.size(0) != P or B.size(2) != K or tuple(out.shape) != (P, M, N // P):
+        raise ValueError("shapes must be A [P,M,K], B [P,N,K], out [P,M,N/P]")
+    wp, wb = _ws(workspace)
+    with torch.cuda.device(A.device):
+        _check(load().gemm_rs_ex(A.data_ptr(), A.stride(0) * 2, B.data_ptr(), B.stride(0) * 2, out.data_ptr(),
+                                 out.stride(0) * 2, P, M, N, K, wp, wb, _stream(stream, A.device)))
+    return out
 
 
 def gemm_rs(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:

@@ -682,8 +682,8 @@ static bool overlap(const void *a, size_t an, const void *b, size_t bn)
 } // namespace ag
 } // namespace rc
 
-extern "C" int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P,
-                       int rank, int M_r, int N, int K, void *stream)
+static int ag_gemm_run(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P,
+                       int rank, int M_r, int N, int K, void *ws, size_t ws_bytes, void *stream)
 {
     using namespace rc;
     using namespace rc::ag;
@@ -721,7 +721,7 @@ extern "C" int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, 
     p.units = p.g_total_m * (BM / PIECE_ROWS);
     p.st32 = (((uintptr_t)C | (size_t)N * 2) & 31u) == 0;
     int sm_count = 0;
-    int rc_ = prepare_workspace((size_t)p.units, &p.hdr, &p.flags, &sm_count, &p.timeout_ns);
+    int rc_ = prepare_workspace_ext(ws, ws_bytes, (size_t)p.units, &p.hdr, &p.flags, &sm_count, &p.timeout_ns);
     if (rc_) return rc_;
     const bool pairs = M_r % PM == 0 && K % BK2 == 0 && sm_count >= 2 && pair_tiles_enabled();
     const size_t sh_stride = P > 1 ? a_stride : shard_bytes;
@@ -813,4 +813,26 @@ extern "C" int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, 
     }
     if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "ag_gemm launch: %s", cudaGetErrorString(e));
     return RC_OK;
+}
+
+extern "C" int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P,
+                       int rank, int M_r, int N, int K, void *stream)
+{
+    return ag_gemm_run(a_shards, a_stride, a_gathered, B, C, P, rank, M_r, N, K, nullptr, 0, stream);
+}
+
+extern "C" int ag_gemm_ex(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P,
+                          int rank, int M_r, int N, int K, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!workspace) return rc::set_error(RC_ERR_INVALID, "null workspace");
+    return ag_gemm_run(a_shards, a_stride, a_gathered, B, C, P, rank, M_r, N, K, workspace, ws_bytes, stream);
+}
+
+// Header + one ready flag per gather unit (PIECE_ROWS rows of A_g).
+extern "C" size_t ag_gemm_workspace_bytes(int P, int M_r)
+{
+    using namespace rc::ag;
+    if (P < 1 || P > RC_MAX_P || M_r <= 0 || M_r % BM) return 0;
+    const size_t units = (size_t)P * (size_t)(M_r / BM) * (BM / PIECE_ROWS);
+    return sizeof(rc::WsHeader) + units * 4;
 }

@@ -315,13 +315,14 @@ bool pair_fits(const rc::RingParams &p, const DeviceState &st, int dtype, size_t
     return true;
 }
 
-// Chooses the kernel, slices and segments of a ring launch (the same for every workspace).
-int plan_ring(rc::RingParams &p, int dtype, DeviceState *st)
+// Chooses the kernel, slices and segments of a ring launch (the same for every
+// workspace).  allow_pair = 0 plans k_ring even where k_ring_pair would run.
+int plan_ring(rc::RingParams &p, int dtype, DeviceState *st, int allow_pair = 1)
 {
     int rc_ = RC_OK;
     const size_t es = elem_size(dtype);
     p.ag_bulk = ag_bulk_for(p.mode);
-    p.pair = pair_fits(p, *st, dtype, es) ? 1 : 0;
+    p.pair = allow_pair && pair_fits(p, *st, dtype, es) ? 1 : 0;
     p.hand_bytes = p.pair ? pair_smem_bytes() : 0;
     // The bidirectional reduce-scatter runs two rings (top and bottom halves) per slice.
     const int rings = p.mode == rc::MODE_RS_BIDIR ? 2 : 1;
@@ -347,6 +348,25 @@ int plan_ring(rc::RingParams &p, int dtype, DeviceState *st)
 }
 
 size_t ring_sig_bytes(const rc::RingParams &p) { return (size_t)p.S * p.P * (size_t)p.rows * p.P * 4; }
+
+// Workspace bytes a caller must provide for a ring launch of these
+// parameters: the larger of the two kernels' signal rows (which kernel runs
+// depends on the caller's slot alignment), plus the header; 0 when no
+// supported device is current.
+size_t ring_ws_bytes_for(rc::RingParams p, int dtype)
+{
+    int dev;
+    DeviceState *st = nullptr;
+    if (current_device(&dev, &st)) return 0;
+    // placeholder slots on 32-byte boundaries, so the pair kernel is planned
+    // wherever the caller's layout could let it run
+    p.data_stride = (p.data_stride + 31) & ~(size_t)31;
+    p.out_stride = (p.out_stride + 31) & ~(size_t)31;
+    rc::RingParams a = p, b = p;
+    if (plan_ring(a, dtype, st, 1) || plan_ring(b, dtype, st, 0)) return 0;
+    const size_t x = ring_sig_bytes(a), y = ring_sig_bytes(b);
+    return sizeof(rc::WsHeader) + (x > y ? x : y);
+}
 
 // Launches a planned ring collective.  ext_ws == nullptr: the device's own
 // workspace; otherwise the caller's (ext_bytes long, zeroed before first use).
@@ -433,6 +453,25 @@ int prepare_workspace(size_t sig_words, WsHeader **hdr, uint32_t **sig, int *sm_
     return RC_OK;
 }
 
+int prepare_workspace_ext(void *ext, size_t ext_bytes, size_t sig_words, WsHeader **hdr, uint32_t **sig,
+                          int *sm_count, unsigned long long *timeout_ns)
+{
+    if (!ext) return prepare_workspace(sig_words, hdr, sig, sm_count, timeout_ns);
+    int dev;
+    DeviceState *st = nullptr;
+    int rc_ = current_device(&dev, &st);
+    if (rc_) return rc_;
+    const size_t need = sizeof(WsHeader) + sig_words * 4;
+    if ((uintptr_t)ext & 15u) return fail(RC_ERR_INVALID, "workspace must be 16-byte aligned");
+    if (ext_bytes < need)
+        return fail(RC_ERR_INVALID, "workspace of %zu bytes is below the %zu this call needs", ext_bytes, need);
+    *hdr = (WsHeader *)ext;
+    *sig = (uint32_t *)((char *)ext + sizeof(WsHeader));
+    *sm_count = st->sm_count;
+    *timeout_ns = (unsigned long long)g_timeout_ms.load() * 1000000ull;
+    return RC_OK;
+}
+
 } // namespace rc
 
 extern "C" {
@@ -505,13 +544,18 @@ int ring_ppermute_right(const void *src_base, size_t src_stride, void *dst_base,
     return run_copy(src_base, src_stride, dst_base, dst_stride, P, n, dtype, (cudaStream_t)stream);
 }
 
-int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_t out_stride, int P, size_t n,
-                    int dtype, void *stream)
+// Validation and launch parameters of the ring collectives.  Results:
+// RC_OK (p filled), kNothing (no work), kCopy (P = 1: a plain copy), or an
+// error code (message set).
+constexpr int kNothing = -1, kCopy = -2;
+
+static int ag_params(const void *in_base, size_t in_stride, void *out_base, size_t out_stride, int P, size_t n,
+                     int dtype, rc::RingParams &p)
 {
     const size_t es = elem_size(dtype);
     if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
     if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
-    if (n == 0) return RC_OK;
+    if (n == 0) return kNothing;
     if (!in_base || !out_base) return fail(RC_ERR_INVALID, "null slot base");
     if (P > 1 && (in_stride < n * es || out_stride < (size_t)P * n * es))
         return fail(RC_ERR_INVALID, "stride below a slot's bytes (in %zu, out %zu)", n * es, (size_t)P * n * es);
@@ -519,8 +563,8 @@ int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_
         return fail(RC_ERR_INVALID, "in and out slots overlap");
     if (!elem_aligned(in_base, in_stride, es) || !elem_aligned(out_base, out_stride, es))
         return fail(RC_ERR_INVALID, "slot bases and strides must be multiples of the %zu-byte element", es);
-    if (P == 1) return run_copy(in_base, in_stride, out_base, out_stride, 1, n, dtype, (cudaStream_t)stream);
-    rc::RingParams p{};
+    if (P == 1) return kCopy;
+    p = rc::RingParams{};
     p.data = (char *)out_base;
     p.data_stride = out_stride;
     p.in = (const char *)in_base;
@@ -530,67 +574,134 @@ int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_
     p.rows = P - 1;
     p.mode = rc::MODE_ALL_GATHER;
     p.discard = 0;
-    return run_ring(p, dtype, (cudaStream_t)stream);
+    return RC_OK;
+}
+
+static int all_gather_run(const void *in_base, size_t in_stride, void *out_base, size_t out_stride, int P, size_t n,
+                          int dtype, void *ws, size_t ws_bytes, void *stream)
+{
+    rc::RingParams p;
+    const int v = ag_params(in_base, in_stride, out_base, out_stride, P, n, dtype, p);
+    if (v == kNothing) return RC_OK;
+    if (v == kCopy) return run_copy(in_base, in_stride, out_base, out_stride, 1, n, dtype, (cudaStream_t)stream);
+    if (v) return v;
+    return run_ring(p, dtype, (cudaStream_t)stream, ws, ws_bytes);
+}
+
+int ring_all_gather(const void *in_base, size_t in_stride, void *out_base, size_t out_stride, int P, size_t n,
+                    int dtype, void *stream)
+{
+    return all_gather_run(in_base, in_stride, out_base, out_stride, P, n, dtype, nullptr, 0, stream);
+}
+
+int ring_all_gather_ex(const void *in_base, size_t in_stride, void *out_base, size_t out_stride, int P, size_t n,
+                       int dtype, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!workspace) return fail(RC_ERR_INVALID, "null workspace");
+    return all_gather_run(in_base, in_stride, out_base, out_stride, P, n, dtype, workspace, ws_bytes, stream);
+}
+
+size_t ring_all_gather_workspace_bytes(int P, size_t n, int dtype)
+{
+    rc::RingParams p;
+    const size_t es = elem_size(dtype);
+    const int v = ag_params((const void *)(uintptr_t)4096, n * es, (void *)((uintptr_t)1 << 40), (size_t)P * n * es,
+                            P, n, dtype, p);
+    if (v == kNothing || v == kCopy) return sizeof(rc::WsHeader);
+    if (v) return 0;
+    return ring_ws_bytes_for(p, dtype);
+}
+
+// mode: MODE_REDUCE_SCATTER or MODE_RS_BIDIR.
+static int rs_params(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P, size_t N,
+                     int dtype, int mode, rc::RingParams &p)
+{
+    const size_t es = elem_size(dtype);
+    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
+    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
+    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
+    if (N == 0) return kNothing;
+    if (!bufs_base || !out_base) return fail(RC_ERR_INVALID, "null slot base");
+    const size_t c = N / (size_t)P;
+    if (P > 1 && (bufs_stride < N * es || out_stride < c * es))
+        return fail(RC_ERR_INVALID, "stride below a slot's bytes (bufs %zu, out %zu)", N * es, c * es);
+    if (regions_overlap(bufs_base, bufs_stride, N * es, out_base, out_stride, c * es, P))
+        return fail(RC_ERR_INVALID, "bufs and out slots overlap");
+    if (!elem_aligned(bufs_base, bufs_stride, es) || !elem_aligned(out_base, out_stride, es))
+        return fail(RC_ERR_INVALID, "slot bases and strides must be multiples of the %zu-byte element", es);
+    if (P == 1) return kCopy;
+    p = rc::RingParams{};
+    p.data = (char *)bufs_base;
+    p.data_stride = bufs_stride;
+    p.out = (char *)out_base;
+    p.out_stride = out_stride;
+    p.chunk = c;
+    p.P = P;
+    p.rows = mode == rc::MODE_RS_BIDIR ? 2 * (P - 1) : P - 1;   // bidirectional: P-1 steps per half
+    p.mode = mode;
+    p.discard = 1;
+    return RC_OK;
+}
+
+static int rs_run(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P, size_t N, int dtype,
+                  int mode, void *ws, size_t ws_bytes, void *stream)
+{
+    rc::RingParams p;
+    const int v = rs_params(bufs_base, bufs_stride, out_base, out_stride, P, N, dtype, mode, p);
+    if (v == kNothing) return RC_OK;
+    if (v == kCopy) return run_copy(bufs_base, bufs_stride, out_base, out_stride, 1, N, dtype, (cudaStream_t)stream);
+    if (v) return v;
+    return run_ring(p, dtype, (cudaStream_t)stream, ws, ws_bytes);
+}
+
+static size_t rs_ws_bytes(int P, size_t N, int dtype, int mode)
+{
+    rc::RingParams p;
+    const size_t es = elem_size(dtype);
+    const int v = rs_params((void *)(uintptr_t)4096, N * es, (void *)((uintptr_t)1 << 40), (P > 0 ? N / (size_t)P : 0) * es,
+                            P, N, dtype, mode, p);
+    if (v == kNothing || v == kCopy) return sizeof(rc::WsHeader);
+    if (v) return 0;
+    return ring_ws_bytes_for(p, dtype);
 }
 
 int ring_reduce_scatter(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P, size_t N,
                         int dtype, void *stream)
 {
-    const size_t es = elem_size(dtype);
-    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
-    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
-    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
-    if (N == 0) return RC_OK;
-    if (!bufs_base || !out_base) return fail(RC_ERR_INVALID, "null slot base");
-    const size_t c = N / (size_t)P;
-    if (P > 1 && (bufs_stride < N * es || out_stride < c * es))
-        return fail(RC_ERR_INVALID, "stride below a slot's bytes (bufs %zu, out %zu)", N * es, c * es);
-    if (regions_overlap(bufs_base, bufs_stride, N * es, out_base, out_stride, c * es, P))
-        return fail(RC_ERR_INVALID, "bufs and out slots overlap");
-    if (!elem_aligned(bufs_base, bufs_stride, es) || !elem_aligned(out_base, out_stride, es))
-        return fail(RC_ERR_INVALID, "slot bases and strides must be multiples of the %zu-byte element", es);
-    if (P == 1) return run_copy(bufs_base, bufs_stride, out_base, out_stride, 1, c, dtype, (cudaStream_t)stream);
-    rc::RingParams p{};
-    p.data = (char *)bufs_base;
-    p.data_stride = bufs_stride;
-    p.out = (char *)out_base;
-    p.out_stride = out_stride;
-    p.chunk = c;
-    p.P = P;
-    p.rows = P - 1;
-    p.mode = rc::MODE_REDUCE_SCATTER;
-    p.discard = 1;
-    return run_ring(p, dtype, (cudaStream_t)stream);
+    return rs_run(bufs_base, bufs_stride, out_base, out_stride, P, N, dtype, rc::MODE_REDUCE_SCATTER, nullptr, 0,
+                  stream);
+}
+
+int ring_reduce_scatter_ex(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P, size_t N,
+                           int dtype, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!workspace) return fail(RC_ERR_INVALID, "null workspace");
+    return rs_run(bufs_base, bufs_stride, out_base, out_stride, P, N, dtype, rc::MODE_REDUCE_SCATTER, workspace,
+                  ws_bytes, stream);
+}
+
+size_t ring_reduce_scatter_workspace_bytes(int P, size_t N, int dtype)
+{
+    return rs_ws_bytes(P, N, dtype, rc::MODE_REDUCE_SCATTER);
 }
 
 int ring_reduce_scatter_bidir(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P,
                               size_t N, int dtype, void *stream)
 {
-    const size_t es = elem_size(dtype);
-    if (!es) return fail(RC_ERR_INVALID, "unknown dtype %d", dtype);
-    if (P < 1 || P > RC_MAX_P) return fail(RC_ERR_INVALID, "P=%d outside 1..%d", P, RC_MAX_P);
-    if (N % (size_t)P) return fail(RC_ERR_INVALID, "N=%zu is not a multiple of P=%d", N, P);
-    if (N == 0) return RC_OK;
-    if (!bufs_base || !out_base) return fail(RC_ERR_INVALID, "null slot base");
-    const size_t c = N / (size_t)P;
-    if (P > 1 && (bufs_stride < N * es || out_stride < c * es))
-        return fail(RC_ERR_INVALID, "stride below a slot's bytes (bufs %zu, out %zu)", N * es, c * es);
-    if (regions_overlap(bufs_base, bufs_stride, N * es, out_base, out_stride, c * es, P))
-        return fail(RC_ERR_INVALID, "bufs and out slots overlap");
-    if (!elem_aligned(bufs_base, bufs_stride, es) || !elem_aligned(out_base, out_stride, es))
-        return fail(RC_ERR_INVALID, "slot bases and strides must be multiples of the %zu-byte element", es);
-    if (P == 1) return run_copy(bufs_base, bufs_stride, out_base, out_stride, 1, c, dtype, (cudaStream_t)stream);
-    rc::RingParams p{};
-    p.data = (char *)bufs_base;
-    p.data_stride = bufs_stride;
-    p.out = (char *)out_base;
-    p.out_stride = out_stride;
-    p.chunk = c;
-    p.P = P;
-    p.rows = 2 * (P - 1);   // P-1 steps for each of the two halves
-    p.mode = rc::MODE_RS_BIDIR;
-    p.discard = 1;
-    return run_ring(p, dtype, (cudaStream_t)stream);
+    return rs_run(bufs_base, bufs_stride, out_base, out_stride, P, N, dtype, rc::MODE_RS_BIDIR, nullptr, 0, stream);
+}
+
+int ring_reduce_scatter_bidir_ex(void *bufs_base, size_t bufs_stride, void *out_base, size_t out_stride, int P,
+                                 size_t N, int dtype, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!workspace) return fail(RC_ERR_INVALID, "null workspace");
+    return rs_run(bufs_base, bufs_stride, out_base, out_stride, P, N, dtype, rc::MODE_RS_BIDIR, workspace, ws_bytes,
+                  stream);
+}
+
+size_t ring_reduce_scatter_bidir_workspace_bytes(int P, size_t N, int dtype)
+{
+    return rs_ws_bytes(P, N, dtype, rc::MODE_RS_BIDIR);
 }
 
 int ring_allreduce(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *stream)
@@ -676,10 +787,7 @@ size_t ring_allreduce_workspace_bytes(int P, size_t N, int dtype)
     int v = allreduce_params((void *)(uintptr_t)4096, N * elem_size(dtype), P, N, dtype, p);
     if (v < 0) return sizeof(rc::WsHeader);
     if (v) return 0;
-    int dev;
-    DeviceState *st = nullptr;
-    if (current_device(&dev, &st) || plan_ring(p, dtype, st)) return 0;
-    return sizeof(rc::WsHeader) + ring_sig_bytes(p);
+    return ring_ws_bytes_for(p, dtype);
 }
 
 int ring_allreduce_ex(void *bufs_base, size_t stride, int P, size_t N, int dtype, void *workspace, size_t ws_bytes,

@@ -627,8 +627,8 @@ static bool overlap(const void *a, size_t an, const void *b, size_t bn)
 } // namespace grs
 } // namespace rc
 
-extern "C" int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_stride, void *out, size_t out_stride,
-                       int P, int M, int N, int K, void *stream)
+static int gemm_rs_run(const void *A, size_t a_stride, const void *B, size_t b_stride, void *out, size_t out_stride,
+                       int P, int M, int N, int K, void *ws, size_t ws_bytes, void *stream)
 {
     using namespace rc;
     using namespace rc::grs;
@@ -659,7 +659,7 @@ extern "C" int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_s
     p.st32 = (((uintptr_t)out | p.out_stride | n_chunk * 2) & 31u) == 0;
     int sm_count = 0;
     uint32_t *unused = nullptr;
-    int rc_ = prepare_workspace(0, &p.hdr, &unused, &sm_count, &p.timeout_ns);
+    int rc_ = prepare_workspace_ext(ws, ws_bytes, 0, &p.hdr, &unused, &sm_count, &p.timeout_ns);
     if (rc_) return rc_;
     const bool pairs = M % PM == 0 && K % BK2 == 0 && sm_count >= 2 && pair_tiles_enabled();
     CUtensorMap map_a, map_b;
@@ -698,4 +698,24 @@ extern "C" int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_s
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(RC_ERR_CUDA, "gemm_rs launch: %s", cudaGetErrorString(e));
     return RC_OK;
+}
+
+extern "C" int gemm_rs(const void *A, size_t a_stride, const void *B, size_t b_stride, void *out, size_t out_stride,
+                       int P, int M, int N, int K, void *stream)
+{
+    return gemm_rs_run(A, a_stride, B, b_stride, out, out_stride, P, M, N, K, nullptr, 0, stream);
+}
+
+extern "C" int gemm_rs_ex(const void *A, size_t a_stride, const void *B, size_t b_stride, void *out,
+                          size_t out_stride, int P, int M, int N, int K, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!workspace) return rc::set_error(RC_ERR_INVALID, "null workspace");
+    return gemm_rs_run(A, a_stride, B, b_stride, out, out_stride, P, M, N, K, workspace, ws_bytes, stream);
+}
+
+// The launch keeps only its status header in the workspace.
+extern "C" size_t gemm_rs_workspace_bytes(int P, int M, int N, int K)
+{
+    if (P < 1 || P > RC_MAX_P || M <= 0 || N <= 0 || K <= 0) return 0;
+    return sizeof(rc::WsHeader);
 }

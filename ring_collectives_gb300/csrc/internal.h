@@ -73,6 +73,11 @@ int set_error(int code, const char *fmt, ...);
 // epoch in the header is shared by every launch that uses the workspace.
 int prepare_workspace(size_t sig_words, WsHeader **hdr, uint32_t **sig, int *sm_count,
                       unsigned long long *timeout_ns);
+// prepare_workspace_ext: the same with a caller-owned workspace (ext, ext_bytes
+// bytes, 16-byte aligned, zeroed before first use); ext == nullptr takes the
+// device's own.
+int prepare_workspace_ext(void *ext, size_t ext_bytes, size_t sig_words, WsHeader **hdr, uint32_t **sig,
+                          int *sm_count, unsigned long long *timeout_ns);
 
 // Threads per block of the ring kernel, and the blocks per SM its register
 // budget is sized for (build-time tuning knobs).

@@ -108,3 +108,21 @@ def test_binding_declares_every_header_function_with_its_result_type():
     L = rc.load()
     for name, ret in decls.items():
         assert getattr(L, name).restype is want[ret], name
+
+
+def test_ex_variants_validate_and_size_without_a_gpu(lib):
+    """The caller-workspace variants reject a null workspace before any CUDA
+    call; the GEMM sizing functions need no device."""
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    fake = vp(0x10000)
+    assert _call(lib, "ring_reduce_scatter_ex", fake, sz(4096), vp(0x20000), sz(1024), 4, sz(16), 0, vp(0), sz(0),
+                 vp(0)) == RC_ERR_INVALID
+    assert _call(lib, "ring_all_gather_ex", fake, sz(64), vp(0x20000), sz(256), 4, sz(16), 0, vp(0), sz(0),
+                 vp(0)) == RC_ERR_INVALID
+    assert _call(lib, "ring_status_ex", vp(0), vp(0)) == RC_ERR_INVALID
+    assert _call(lib, "ring_status_ex", vp(0x10004), vp(0)) == RC_ERR_INVALID   # not 16-byte aligned
+    lib.ag_gemm_workspace_bytes.restype = ctypes.c_size_t
+    lib.gemm_rs_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.ag_gemm_workspace_bytes(8, 1024) == 128 + 4 * 8 * 1024 // 16
+    assert lib.ag_gemm_workspace_bytes(8, 100) == 0
+    assert lib.gemm_rs_workspace_bytes(8, 8192, 4096, 512) == 128
