@@ -466,11 +466,28 @@ def ag_gemm_secondary(rc, dev, stream, args):
     cb = cublas_same_shape(ag, bd, stream, args)
     own = plain_gemm_same_kernel(rc, ag, bd, stream, args)
     own["frac_of_cublas_same_shape"] = round(own["TFLOP/s"] / cb["TFLOP/s"], 4)
+    # the same workload with the weight stored [K][N] (x @ W): MN-major B operand
+    bkn = bd.t().contiguous()
+    for _ in range(args.warmup):
+        rc.ag_gemm_kn(ad, ag, bkn, C, 3, stream=stream)
+    torch.cuda.synchronize()
+    evk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for x, y in evk:
+        x.record(stream)
+        rc.ag_gemm_kn(ad, ag, bkn, C, 3, stream=stream)
+        y.record(stream)
+    torch.cuda.synchronize()
+    if rc.ring_status(stream) != 0:
+        raise RuntimeError(rc.ring_last_error())
+    ms_kn = statistics.mean(x.elapsed_time(y) for x, y in evk)
+    tf_kn = flop / (ms_kn * 1e-3) / 1e12
+    kn = {"ms": round(ms_kn, 4), "TFLOP/s": round(tf_kn, 1), "frac_bf16_peak": round(tf_kn / peak, 4),
+          "frac_of_nk_layout": round(tf_kn / tf, 4), "call": "ag_gemm_kn (B [K][N], MN-major operand)"}
     return {"ag_gemm_p8_8192x4096x4096": {
         "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peak, 4),
         "peak": peak, "peak_kind": kind, "flop_per_call": flop,
         "cublas_same_shape": cb, "frac_of_cublas_same_shape": round(tf / cb["TFLOP/s"], 4),
-        "plain_gemm_same_kernel": own,
+        "plain_gemm_same_kernel": own, "weight_kn_layout": kn,
         "note": "gather of the 8 shards (64 MiB) + C = A_g.B^T, one tcgen05 launch"}}
 
 

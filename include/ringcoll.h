@@ -67,6 +67,11 @@ typedef enum {
 
 #define RC_MAX_P 64 /* largest number of logical ranks */
 
+/* Layout of the weight B of ag_gemm: [N][K] (one output feature per row, the
+ * nn.Linear layout) or [K][N] (the x @ W layout of "TPU 与分布式通信原语",
+ * section "collective matmul"). */
+typedef enum { RC_B_NK = 0, RC_B_KN = 1 } rc_b_layout;
+
 /*
  * ring_ppermute_right -- right shift by one rank.
  * "Pallas TPU Distributed Collectives 复习文档", section 1 (lax.ppermute):
@@ -294,15 +299,28 @@ int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, const void 
             int P, int rank, int M_r, int N, int K, void *stream);
 
 /*
- * ag_gemm_ex -- ag_gemm with a caller-owned workspace holding the launch
- * epoch, the status header and one ready flag per 16 gathered rows (rules as
- * for ring_all_gather_ex; size from ag_gemm_workspace_bytes(P, M_r)).  With
- * different workspaces, ag_gemm_ex calls may be issued on different streams;
- * each launch fills the GPU, so concurrent calls mostly run one after the
- * other.  Arguments, validation and result as ag_gemm.
+ * ag_gemm_kn -- ag_gemm with the weight stored [K][N] row-major (B[k][n] at
+ * B + (k*N + n)*2 bytes), the layout of the page's x @ W1: C = A_g . B.  The
+ * tensor cores read B as an MN-major operand straight from this layout (no
+ * transpose pass).  Same requirements, result and rounding as ag_gemm; the
+ * products are the same, so C is the same bit for bit as ag_gemm with the
+ * transposed weight.
  */
-int ag_gemm_ex(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P, int rank,
-               int M_r, int N, int K, void *workspace, size_t ws_bytes, void *stream);
+int ag_gemm_kn(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C,
+               int P, int rank, int M_r, int N, int K, void *stream);
+
+/*
+ * ag_gemm_ex -- ag_gemm with the weight layout as an argument (b_layout: an
+ * rc_b_layout value; RC_ERR_INVALID otherwise) and a caller-owned workspace
+ * holding the launch epoch, the status header and one ready flag per 16
+ * gathered rows (rules as for ring_all_gather_ex; size from
+ * ag_gemm_workspace_bytes(P, M_r)).  With different workspaces, ag_gemm_ex
+ * calls may be issued on different streams; each launch fills the GPU, so
+ * concurrent calls mostly run one after the other.  Arguments, validation and
+ * result as ag_gemm (RC_B_NK) or ag_gemm_kn (RC_B_KN).
+ */
+int ag_gemm_ex(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, int b_layout, void *C, int P,
+               int rank, int M_r, int N, int K, void *workspace, size_t ws_bytes, void *stream);
 
 /* Workspace bytes ag_gemm_ex needs: 128 + 4 * P * M_r / 16; 0 when P or M_r
  * is invalid (M_r must be a multiple of 128). */

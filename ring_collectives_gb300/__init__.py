@@ -28,7 +28,7 @@ __all__ = [
     "ring_allreduce_fused", "ring_psum", "ring_allreduce_noalloc", "ag_gemm", "gemm_rs", "ring_status",
     "ring_status_ex", "ring_all_gather_ex", "ring_all_gather_workspace_bytes", "ring_reduce_scatter_ex",
     "ring_reduce_scatter_workspace_bytes", "ring_reduce_scatter_bidir_ex", "ring_reduce_scatter_bidir_workspace_bytes",
-    "ag_gemm_ex", "ag_gemm_workspace_bytes", "gemm_rs_ex", "gemm_rs_workspace_bytes",
+    "ag_gemm_ex", "ag_gemm_kn", "ag_gemm_workspace_bytes", "RC_B_NK", "RC_B_KN", "gemm_rs_ex", "gemm_rs_workspace_bytes",
     "ring_last_error", "ring_set_timeout_ms", "ring_set_slices", "ring_debug_skip_notify",
     "ring_debug_set_trace", "ring_debug_l2_rate", "ring_finalize", "library_path", "load",
 ]
@@ -37,6 +37,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libringcoll.so")
 
 RC_OK, RC_ERR_INVALID, RC_ERR_CUDA, RC_ERR_TIMEOUT, RC_ERR_UNSUPPORTED, RC_ERR_NOMEM = range(6)
+RC_B_NK, RC_B_KN = 0, 1   # ag_gemm weight layouts: [N][K] (nn.Linear) or [K][N] (x @ W)
 _DTYPE = {torch.float32: 0, torch.bfloat16: 1, torch.int32: 2}
 
 _vp, _sz, _i, _u = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint
@@ -50,7 +51,8 @@ _SIGNATURES = {
     "ring_reduce_scatter_workspace_bytes": ([_i, _sz, _i], _sz),
     "ring_reduce_scatter_bidir_ex": ([_vp, _sz, _vp, _sz, _i, _sz, _i, _vp, _sz, _vp], _i),
     "ring_reduce_scatter_bidir_workspace_bytes": ([_i, _sz, _i], _sz),
-    "ag_gemm_ex": ([_vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp], _i),
+    "ag_gemm_ex": ([_vp, _sz, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp], _i),
+    "ag_gemm_kn": ([_vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp], _i),
     "ag_gemm_workspace_bytes": ([_i, _i], _sz),
     "gemm_rs_ex": ([_vp, _sz, _vp, _sz, _vp, _sz, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "gemm_rs_workspace_bytes": ([_i, _i, _i, _i], _sz),
@@ -310,26 +312,42 @@ def ring_allreduce_host(h_in: torch.Tensor, h_out: torch.Tensor, d_bufs: torch.T
     return h_out
 
 
-def ag_gemm(a_shards: torch.Tensor, a_gathered: torch.Tensor, B: torch.Tensor, C: torch.Tensor, rank: int,
-            stream=None) -> torch.Tensor:
-    """a_shards [P, M_r, K], a_gathered [P*M_r, K], B [N, K], C [P*M_r, N], all bf16:
-    gathers the shards and computes C = A_g . B^T (fp32 accumulate, bf16 out)."""
+def _ag_gemm_args(a_shards, a_gathered, B, C, b_layout):
     for name, t in (("a_shards", a_shards), ("a_gathered", a_gathered), ("B", B), ("C", C)):
         if not t.is_cuda or t.dtype != torch.bfloat16:
             raise TypeError(f"{name} must be a bf16 CUDA tensor")
     if a_shards.dim() != 3 or a_shards.stride(2) != 1 or a_shards.stride(1) != a_shards.size(2):
         raise ValueError("a_shards must be [P, M_r, K] with row-major shards")
     P, M_r, K = a_shards.shape
-    N = B.size(0)
+    N = B.size(0) if b_layout == RC_B_NK else B.size(1)
     if tuple(a_gathered.shape) != (P * M_r, K) or not a_gathered.is_contiguous():
         raise ValueError("a_gathered must be contiguous [P*M_r, K]")
-    if tuple(B.shape) != (N, K) or not B.is_contiguous():
-        raise ValueError("B must be contiguous [N, K]")
+    want_b = (N, K) if b_layout == RC_B_NK else (K, N)
+    if tuple(B.shape) != want_b or not B.is_contiguous():
+        raise ValueError(f"B must be contiguous {list(want_b)}")
     if tuple(C.shape) != (P * M_r, N) or not C.is_contiguous():
         raise ValueError("C must be contiguous [P*M_r, N]")
+    return P, M_r, N, K
+
+
+def ag_gemm(a_shards: torch.Tensor, a_gathered: torch.Tensor, B: torch.Tensor, C: torch.Tensor, rank: int,
+            stream=None) -> torch.Tensor:
+    """a_shards [P, M_r, K], a_gathered [P*M_r, K], B [N, K], C [P*M_r, N], all bf16:
+    gathers the shards and computes C = A_g . B^T (fp32 accumulate, bf16 out)."""
+    P, M_r, N, K = _ag_gemm_args(a_shards, a_gathered, B, C, RC_B_NK)
     with torch.cuda.device(a_shards.device):
         _check(load().ag_gemm(a_shards.data_ptr(), a_shards.stride(0) * 2, a_gathered.data_ptr(), B.data_ptr(),
                               C.data_ptr(), P, rank, M_r, N, K, _stream(stream, a_shards.device)))
+    return C
+
+
+def ag_gemm_kn(a_shards: torch.Tensor, a_gathered: torch.Tensor, B: torch.Tensor, C: torch.Tensor, rank: int,
+               stream=None) -> torch.Tensor:
+    """As ag_gemm with the weight stored [K, N] (the x @ W layout): C = A_g . B."""
+    P, M_r, N, K = _ag_gemm_args(a_shards, a_gathered, B, C, RC_B_KN)
+    with torch.cuda.device(a_shards.device):
+        _check(load().ag_gemm_kn(a_shards.data_ptr(), a_shards.stride(0) * 2, a_gathered.data_ptr(), B.data_ptr(),
+                                 C.data_ptr(), P, rank, M_r, N, K, _stream(stream, a_shards.device)))
     return C
 
 
@@ -338,26 +356,15 @@ def ag_gemm_workspace_bytes(P: int, M_r: int) -> int:
 
 
 def ag_gemm_ex(a_shards: torch.Tensor, a_gathered: torch.Tensor, B: torch.Tensor, C: torch.Tensor, rank: int,
-               workspace: torch.Tensor, stream=None) -> torch.Tensor:
-    """ag_gemm with a caller-owned workspace (zeroed CUDA tensor of at least
+               workspace: torch.Tensor, b_layout: int = RC_B_NK, stream=None) -> torch.Tensor:
+    """ag_gemm (b_layout RC_B_NK, B [N, K]) or ag_gemm_kn (RC_B_KN, B [K, N])
+    with a caller-owned workspace (zeroed CUDA tensor of at least
     ag_gemm_workspace_bytes(P, M_r) bytes)."""
-    for name, t in (("a_shards", a_shards), ("a_gathered", a_gathered), ("B", B), ("C", C)):
-        if not t.is_cuda or t.dtype != torch.bfloat16:
-            raise TypeError(f"{name} must be a bf16 CUDA tensor")
-    if a_shards.dim() != 3 or a_shards.stride(2) != 1 or a_shards.stride(1) != a_shards.size(2):
-        raise ValueError("a_shards must be [P, M_r, K] with row-major shards")
-    P, M_r, K = a_shards.shape
-    N = B.size(0)
-    if tuple(a_gathered.shape) != (P * M_r, K) or not a_gathered.is_contiguous():
-        raise ValueError("a_gathered must be contiguous [P*M_r, K]")
-    if tuple(B.shape) != (N, K) or not B.is_contiguous():
-        raise ValueError("B must be contiguous [N, K]")
-    if tuple(C.shape) != (P * M_r, N) or not C.is_contiguous():
-        raise ValueError("C must be contiguous [P*M_r, N]")
+    P, M_r, N, K = _ag_gemm_args(a_shards, a_gathered, B, C, b_layout)
     wp, wb = _ws(workspace)
     with torch.cuda.device(a_shards.device):
         _check(load().ag_gemm_ex(a_shards.data_ptr(), a_shards.stride(0) * 2, a_gathered.data_ptr(), B.data_ptr(),
-                                 C.data_ptr(), P, rank, M_r, N, K, wp, wb, _stream(stream, a_shards.device)))
+                                 b_layout, C.data_ptr(), P, rank, M_r, N, K, wp, wb, _stream(stream, a_shards.device)))
     return C
 
 

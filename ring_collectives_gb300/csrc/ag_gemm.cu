@@ -63,6 +63,7 @@ struct Params {
     int total_m, tiles_per_pe, n_tiles, total_tiles, units;  // tile schedule (tile rows: BM, or PM for pairs)
     int g_total_m, g_per_pe;   // gather schedule, in 128-row blocks (8 units of 16 rows each)
     int st32;                  // 1: rows of C start on 32-byte boundaries (full-sector stores)
+    int b_kn;                  // 1: B is stored [K][N] (MN-major operand), 0: [N][K] (K-major)
     unsigned long long timeout_ns;
 };
 
@@ -225,7 +226,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tma_load_3d(sA + stage * A_STAGE, &map_sh, kb * BK, row_in_shard, src_rank, full_bar + 8 * stage);
                 else
                     tma_load_2d(sA + stage * A_STAGE, &map_ag, kb * BK, m * BM, full_bar + 8 * stage);
-                tma_load_2d(sB + stage * B_STAGE, &map_b, kb * BK, n * BN, full_bar + 8 * stage);
+                if (p.b_kn)   // [K][N]: 4 blocks of 64 columns x BK rows of k
+                    tma_load_3d(sB + stage * B_STAGE, &map_b, 0, kb * BK, n * (BN / 64), full_bar + 8 * stage);
+                else
+                    tma_load_2d(sB + stage * B_STAGE, &map_b, kb * BK, n * BN, full_bar + 8 * stage);
                 issued[stage]++;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -258,11 +262,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const uint64_t ad = smem_desc_sw128(sA + stage * A_STAGE);
-                const uint64_t bd = smem_desc_sw128(sB + stage * B_STAGE);
+                const uint64_t bd = p.b_kn ? smem_desc_mn_sw128(sB + stage * B_STAGE, BK * 128)
+                                           : smem_desc_sw128(sB + stage * B_STAGE);
 #pragma unroll
                 for (int k = 0; k < BK / UK; ++k) {
-                    // K advances 16 bf16 = 32 bytes inside the 128-byte swizzle row: +2 in 16-byte units
-                    tc_mma(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc, (kb | k) != 0);
+                    // K advances 16 bf16 = 32 bytes inside the 128-byte swizzle row: +2 in 16-byte units;
+                    // for an MN-major B it advances 16 rows of 128 bytes: +128
+                    tc_mma(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(p.b_kn ? 128 * k : 2 * k),
+                           kIdesc | (p.b_kn ? kIdescBMnMajor : 0u), (kb | k) != 0);
                 }
                 tc_commit(empty_bar + 8 * stage); // frees the smem stage once these MMAs have read it
                 if (++stage == STAGES) {
@@ -473,9 +480,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     else
                         tma_load_3d_pair(sA + stage * A2_STAGE, &map_ag, 0, row0, kb * KSUB2, full_even + 8 * stage);
                 }
-                if (b_producer)
-                    tma_load_3d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * KSUB2,
-                                     full_even + 8 * stage);
+                if (b_producer) {
+                    if (p.b_kn)   // [K][N]: this CTA's 2 blocks of 64 columns x BK2 rows of k
+                        tma_load_3d_pair(sB + stage * B2_STAGE, &map_b, 0, kb * BK2, (n * PN + (int)cta * HN) / 64,
+                                         full_even + 8 * stage);
+                    else
+                        tma_load_3d_pair(sB + stage * B2_STAGE, &map_b, 0, n * PN + (int)cta * HN, kb * KSUB2,
+                                         full_even + 8 * stage);
+                }
                 issued[stage]++;
                 if (++stage == STAGES2) {
                     stage = 0;
@@ -506,11 +518,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
+                const uint64_t bd_mn = smem_desc_mn_sw128(sB + stage * B2_STAGE, BK2 * 128);
 #pragma unroll
                 for (int kk = 0; kk < BK2 / UK; ++kk) {
                     const uint64_t ad = smem_desc_sw128(sA + stage * A2_STAGE + (kk >> 2) * A2_SUB);
-                    const uint64_t bd = smem_desc_sw128(sB + stage * B2_STAGE + (kk >> 2) * B2_SUB);
-                    tc_mma_pair(d, ad + (uint64_t)(2 * (kk & 3)), bd + (uint64_t)(2 * (kk & 3)), kIdesc2,
+                    // K-major B: 16 K-columns of a 64-column sub-tile; MN-major B: 16 rows of k (2048 bytes)
+                    const uint64_t bd = p.b_kn ? bd_mn + (uint64_t)(128 * kk)
+                                               : smem_desc_sw128(sB + stage * B2_STAGE + (kk >> 2) * B2_SUB) +
+                                                     (uint64_t)(2 * (kk & 3));
+                    tc_mma_pair(d, ad + (uint64_t)(2 * (kk & 3)), bd, kIdesc2 | (p.b_kn ? kIdescBMnMajor : 0u),
                                 (kb | kk) != 0);
                 }
                 tc_commit_pair_mc(empty_bar + 8 * stage, 3);
@@ -648,6 +664,21 @@ static int make_map(CUtensorMap *map, const void *ptr, int rank, const cuuint64_
 
 // The same over [..][K/64][rows][64] (dims {64, rows, K/64, ...}): a box of two
 // 64-column K blocks of box_rows rows is one request (the CTA-pair stages).
+// [K][N] weight as a 3-D map (64 columns, k, 64-column block): one box of
+// 64 columns x k_rows rows x blocks blocks, 128-byte swizzled rows of k.
+static int make_map_mn(CUtensorMap *map, const void *ptr, const cuuint64_t *dims, const cuuint64_t *strides,
+                       uint32_t k_rows, uint32_t blocks)
+{
+    auto fn = encode_fn();
+    if (!fn) return set_error(RC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint32_t box[3] = {64, k_rows, blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3u, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(RC_ERR_INVALID, "tensor map encoding failed (CUresult %d)", (int)r);
+    return RC_OK;
+}
 static int make_map_k2(CUtensorMap *map, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
                        uint32_t box_rows)
 {
@@ -682,8 +713,8 @@ static bool overlap(const void *a, size_t an, const void *b, size_t bn)
 } // namespace ag
 } // namespace rc
 
-static int ag_gemm_run(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P,
-                       int rank, int M_r, int N, int K, void *ws, size_t ws_bytes, void *stream)
+static int ag_gemm_run(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, int b_layout, void *C,
+                       int P, int rank, int M_r, int N, int K, void *ws, size_t ws_bytes, void *stream)
 {
     using namespace rc;
     using namespace rc::ag;
@@ -693,6 +724,7 @@ static int ag_gemm_run(const void *a_shards, size_t a_stride, void *a_gathered, 
         return set_error(RC_ERR_INVALID, "need M_r %% %d == 0, N %% %d == 0, K %% %d == 0 (got %d, %d, %d)", BM, BN, BK,
                          M_r, N, K);
     if (!a_shards || !a_gathered || !B || !C) return set_error(RC_ERR_INVALID, "null pointer");
+    if (b_layout != RC_B_NK && b_layout != RC_B_KN) return set_error(RC_ERR_INVALID, "unknown B layout %d", b_layout);
     if (((uintptr_t)a_shards | (uintptr_t)a_gathered | (uintptr_t)B | (uintptr_t)C | a_stride) & 15u)
         return set_error(RC_ERR_INVALID, "pointers and a_stride must be 16-byte aligned");
     const size_t shard_bytes = (size_t)M_r * K * 2;
@@ -720,6 +752,7 @@ static int ag_gemm_run(const void *a_shards, size_t a_stride, void *a_gathered, 
     p.g_per_pe = M_r / BM;
     p.units = p.g_total_m * (BM / PIECE_ROWS);
     p.st32 = (((uintptr_t)C | (size_t)N * 2) & 31u) == 0;
+    p.b_kn = b_layout == RC_B_KN;
     int sm_count = 0;
     int rc_ = prepare_workspace_ext(ws, ws_bytes, (size_t)p.units, &p.hdr, &p.flags, &sm_count, &p.timeout_ns);
     if (rc_) return rc_;
@@ -734,9 +767,15 @@ static int ag_gemm_run(const void *a_shards, size_t a_stride, void *a_gathered, 
         const cuuint64_t dsh[4] = {64, (cuuint64_t)M_r, (cuuint64_t)K / 64, (cuuint64_t)P};
         const cuuint64_t ssh[3] = {(cuuint64_t)K * 2, 128, (cuuint64_t)sh_stride};
         if ((rc_ = make_map_k2(&map_sh, a_shards, 4, dsh, ssh, HM))) return rc_;
-        const cuuint64_t db[3] = {64, (cuuint64_t)N, (cuuint64_t)K / 64};
-        const cuuint64_t sb[2] = {(cuuint64_t)K * 2, 128};
-        if ((rc_ = make_map_k2(&map_b, B, 3, db, sb, HN))) return rc_;
+        if (p.b_kn) {   // [K][N]: (64 columns, k, 64-column block), box 64 x BK2 x 2
+            const cuuint64_t db[3] = {64, (cuuint64_t)K, (cuuint64_t)N / 64};
+            const cuuint64_t sb[2] = {(cuuint64_t)N * 2, 128};
+            if ((rc_ = make_map_mn(&map_b, B, db, sb, BK2, HN / 64))) return rc_;
+        } else {
+            const cuuint64_t db[3] = {64, (cuuint64_t)N, (cuuint64_t)K / 64};
+            const cuuint64_t sb[2] = {(cuuint64_t)K * 2, 128};
+            if ((rc_ = make_map_k2(&map_b, B, 3, db, sb, HN))) return rc_;
+        }
     } else {
         {
             cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
@@ -748,7 +787,11 @@ static int ag_gemm_run(const void *a_shards, size_t a_stride, void *a_gathered, 
             cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)sh_stride};
             if ((rc_ = make_map(&map_sh, a_shards, 3, dims, strides, BM))) return rc_;
         }
-        {
+        if (p.b_kn) {   // [K][N]: (64 columns, k, 64-column block), box 64 x BK x 4
+            const cuuint64_t db[3] = {64, (cuuint64_t)K, (cuuint64_t)N / 64};
+            const cuuint64_t sb[2] = {(cuuint64_t)N * 2, 128};
+            if ((rc_ = make_map_mn(&map_b, B, db, sb, BK, BN / 64))) return rc_;
+        } else {
             cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
             cuuint64_t strides[1] = {(cuuint64_t)K * 2};
             if ((rc_ = make_map(&map_b, B, 2, dims, strides, BN))) return rc_;
@@ -818,14 +861,22 @@ static int ag_gemm_run(const void *a_shards, size_t a_stride, void *a_gathered, 
 extern "C" int ag_gemm(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P,
                        int rank, int M_r, int N, int K, void *stream)
 {
-    return ag_gemm_run(a_shards, a_stride, a_gathered, B, C, P, rank, M_r, N, K, nullptr, 0, stream);
+    return ag_gemm_run(a_shards, a_stride, a_gathered, B, RC_B_NK, C, P, rank, M_r, N, K, nullptr, 0, stream);
 }
 
-extern "C" int ag_gemm_ex(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P,
-                          int rank, int M_r, int N, int K, void *workspace, size_t ws_bytes, void *stream)
+extern "C" int ag_gemm_kn(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, void *C, int P,
+                          int rank, int M_r, int N, int K, void *stream)
+{
+    return ag_gemm_run(a_shards, a_stride, a_gathered, B, RC_B_KN, C, P, rank, M_r, N, K, nullptr, 0, stream);
+}
+
+extern "C" int ag_gemm_ex(const void *a_shards, size_t a_stride, void *a_gathered, const void *B, int b_layout,
+                          void *C, int P, int rank, int M_r, int N, int K, void *workspace, size_t ws_bytes,
+                          void *stream)
 {
     if (!workspace) return rc::set_error(RC_ERR_INVALID, "null workspace");
-    return ag_gemm_run(a_shards, a_stride, a_gathered, B, C, P, rank, M_r, N, K, workspace, ws_bytes, stream);
+    return ag_gemm_run(a_shards, a_stride, a_gathered, B, b_layout, C, P, rank, M_r, N, K, workspace, ws_bytes,
+                       stream);
 }
 
 // Header + one ready flag per gather unit (PIECE_ROWS rows of A_g).

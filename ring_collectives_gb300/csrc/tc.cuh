@@ -229,6 +229,25 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
     return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major tile written by TMA with the
+// 128-byte swizzle: each 128-byte row holds 64 consecutive M (or N) elements
+// of one k, 8 consecutive k rows form one 1024-byte swizzle atom (stride
+// byte offset 1024, the step between 8-row k groups), and the leading byte
+// offset is the step between consecutive 64-element blocks along M/N.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t addr, uint32_t mn_block_bytes)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);                  // start address
+    d |= (uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16;   // leading byte offset
+    d |= (uint64_t)(1024u >> 4) << 32;                         // stride byte offset
+    d |= (uint64_t)1 << 46;                                    // version
+    d |= (uint64_t)2 << 61;                                    // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor bit that marks the B operand MN-major ("transpose B").
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
+
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N>>3 at bits
 // 17-22, M>>4 at bits 24-28.

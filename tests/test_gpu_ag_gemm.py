@@ -134,3 +134,69 @@ def test_ag_gemm_rejects_bad_shapes():
         rc.ag_gemm(a, torch.zeros((200, 64), dtype=torch.bfloat16, device=DEV),
                    torch.zeros((256, 64), dtype=torch.bfloat16, device=DEV),
                    torch.zeros((200, 256), dtype=torch.bfloat16, device=DEV), 0)
+
+
+# ------------------------------------------------------------------ weight stored [K][N] (x @ W)
+@pytest.mark.parametrize("P,M_r,K,N,rank", [(4, 256, 256, 512, 1), (2, 256, 1024, 256, 0), (3, 128, 192, 256, 2),
+                                            (5, 128, 64, 768, 4), (1, 256, 128, 256, 0)])
+def test_ag_gemm_kn_layout_small(P, M_r, K, N, rank):
+    """B given [K][N] (the page's x @ W1) runs the MN-major operand path: C is
+    the same bit for bit as ag_gemm on the transposed [N][K] weight (the
+    same MMA sequence; only the operand's shared-memory layout differs) and
+    within the oracle's bound.  CTA-pair and one-CTA shapes."""
+    a, b_nk = synthetic.ag_gemm_inputs(P=P, M_r=M_r, K=K, N=N, seed=21)
+    b_kn = b_nk.t().contiguous()                 # [K][N]
+    ad = a.to(DEV)
+    ag = torch.full((P * M_r, K), float("nan"), dtype=torch.bfloat16, device=DEV)
+    C_kn = torch.full((P * M_r, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    rc.ag_gemm_kn(ad, ag, b_kn.to(DEV), C_kn, rank)
+    assert rc.ring_status() == 0, rc.ring_last_error()
+    ag2 = torch.empty_like(ag)
+    C_nk = torch.empty_like(C_kn)
+    rc.ag_gemm(ad, ag2, b_nk.to(DEV), C_nk, rank)
+    assert rc.ring_status() == 0, rc.ring_last_error()
+    A_bits = oracle.ag_gather(synthetic.bf16_bits(a))
+    assert np.array_equal(bits(ag), A_bits)
+    assert np.array_equal(bits(C_kn), bits(C_nk))
+    check_c(A_bits, synthetic.bf16_bits(b_nk), bits(C_kn))
+
+
+def test_ag_gemm_kn_full_size_sampled():
+    """The benchmark's shapes (P=8, shards [1024,4096], W [4096,4096] stored
+    [K][N]), rank 5: A_g bit for bit, C on sampled rows and columns within
+    the bound, and the same bits as the [N][K] path on those samples."""
+    P, M_r, K, N = 8, 1024, 4096, 4096
+    a, b_nk = synthetic.ag_gemm_inputs(P=P, M_r=M_r, K=K, N=N)
+    b_kn = b_nk.t().contiguous()
+    ad = a.to(DEV)
+    ag = torch.empty((P * M_r, K), dtype=torch.bfloat16, device=DEV)
+    C = torch.empty((P * M_r, N), dtype=torch.bfloat16, device=DEV)
+    rc.ag_gemm_kn(ad, ag, b_kn.to(DEV), C, 5)
+    assert rc.ring_status() == 0, rc.ring_last_error()
+    assert torch.equal(ag.view(P, M_r, K).cpu(), a)
+    C2 = torch.empty_like(C)
+    rc.ag_gemm(ad, torch.empty_like(ag), b_nk.to(DEV), C2, 5)
+    assert rc.ring_status() == 0, rc.ring_last_error()
+    g = np.random.default_rng(9)
+    rows = np.sort(g.choice(P * M_r, 256, replace=False))
+    cols = np.sort(g.choice(N, 256, replace=False))
+    A_bits = synthetic.bf16_bits(ag.cpu())
+    cb = bits(C)[np.ix_(rows, cols)]
+    assert np.array_equal(cb, bits(C2)[np.ix_(rows, cols)])
+    check_c(A_bits, synthetic.bf16_bits(b_nk), cb, rows=rows, cols=cols)
+
+
+def test_ag_gemm_ex_kn_layout_and_bad_layout():
+    P, M_r, K, N = 2, 256, 256, 256
+    a, b_nk = synthetic.ag_gemm_inputs(P=P, M_r=M_r, K=K, N=N, seed=22)
+    ad, bk = a.to(DEV), b_nk.t().contiguous().to(DEV)
+    ws = torch.zeros(rc.ag_gemm_workspace_bytes(P, M_r), dtype=torch.uint8, device=DEV)
+    ag = torch.empty((P * M_r, K), dtype=torch.bfloat16, device=DEV)
+    C = torch.empty((P * M_r, N), dtype=torch.bfloat16, device=DEV)
+    rc.ag_gemm_ex(ad, ag, bk, C, 1, ws, b_layout=rc.RC_B_KN)
+    assert rc.ring_status_ex(ws) == 0, rc.ring_last_error()
+    check_c(oracle.ag_gather(synthetic.bf16_bits(a)), synthetic.bf16_bits(b_nk), bits(C))
+    L = rc.load()
+    rcode = L.ag_gemm_ex(ad.data_ptr(), ad.stride(0) * 2, ag.data_ptr(), bk.data_ptr(), 7, C.data_ptr(), P, 1, M_r,
+                         N, K, ws.data_ptr(), ws.numel(), None)
+    assert rcode == rc.RC_ERR_INVALID and "layout" in rc.ring_last_error()
