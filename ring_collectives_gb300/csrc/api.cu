@@ -301,17 +301,19 @@ int choose_slices(int blocks, int per_slice, size_t chunk_elems, size_t chunk_by
     return RC_OK;
 }
 
-// k_ring_pair takes the all-reduce and the reduce-scatter at even P when
-// every slice starts on a 32-byte boundary (slot bases, strides and chunk
-// starts multiples of 32 bytes) and the all-gather steps use vector copies.
+// k_ring_pair takes the all-reduce and both reduce-scatters at even P when
+// every slice starts on a 32-byte boundary (slot bases, strides, chunk starts
+// and, for the bidirectional one, the second half of every chunk multiples of
+// 32 bytes) and the all-gather steps use vector copies.
 bool pair_fits(const rc::RingParams &p, const DeviceState &st, int dtype, size_t es)
 {
     if (!pair_enabled() || st.pair_blocks[dtype] < 1) return false;
-    if (p.mode != rc::MODE_ALLREDUCE && p.mode != rc::MODE_REDUCE_SCATTER) return false;
+    if (p.mode == rc::MODE_ALL_GATHER) return false;
     if (p.P < 2 || (p.P & 1) || p.ag_bulk) return false;
     const size_t cs = p.chunk_stride ? p.chunk_stride : p.chunk;
     if (((uintptr_t)p.data | p.data_stride | (cs * es)) & 31u) return false;
-    if (p.mode == rc::MODE_REDUCE_SCATTER && (((uintptr_t)p.out | p.out_stride) & 31u)) return false;
+    if (p.mode != rc::MODE_ALLREDUCE && (((uintptr_t)p.out | p.out_stride) & 31u)) return false;
+    if (p.mode == rc::MODE_RS_BIDIR && ((p.chunk / 2) * es) & 31u) return false;
     return true;
 }
 
@@ -328,7 +330,7 @@ int plan_ring(rc::RingParams &p, int dtype, DeviceState *st, int allow_pair = 1)
     const int rings = p.mode == rc::MODE_RS_BIDIR ? 2 : 1;
     const size_t ring_elems = p.chunk / (size_t)rings;
     if (p.pair)
-        rc_ = choose_slices(st->pair_blocks[dtype], p.P / 2, ring_elems, ring_elems * es, &p.S);
+        rc_ = choose_slices(st->pair_blocks[dtype], p.P / 2 * rings, ring_elems, ring_elems * es, &p.S);
     else
         rc_ = choose_slices(st->max_blocks[dtype], p.P * rings, ring_elems, ring_elems * es, &p.S);
     if (rc_) return rc_;

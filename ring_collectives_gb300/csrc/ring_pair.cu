@@ -186,29 +186,45 @@ __global__ void __launch_bounds__(kPairThreads, RC_PAIR_MIN_BLOCKS) k_ring_pair(
 {
     constexpr size_t ES = DT == 1 ? 2 : 4;
     constexpr int T = kPairThreads;
+    constexpr bool BIDIR = MODE == MODE_RS_BIDIR;
     const int P = p.P, S = p.S;
-    const int m = (int)(blockIdx.x / (unsigned)S), j = (int)(blockIdx.x % (unsigned)S);
+    const int bm = (int)(blockIdx.x / (unsigned)S), j = (int)(blockIdx.x % (unsigned)S);
+    // The bidirectional reduce-scatter runs two rings per slice: half 0 (the
+    // top half of every chunk) towards lower ranks, half 1 towards higher
+    // ranks; every other mode runs one ring towards higher ranks.
+    const int hf = BIDIR ? bm / (P / 2) : 1;
+    const int m = BIDIR ? bm % (P / 2) : bm;
     const int r0 = 2 * m, r1 = 2 * m + 1;
-    const int lrank = (r0 - 1 + P) % P;   // r0's left neighbour: rank r1 of the previous block
-    const int rrank = (r1 + 1) % P;       // r1's right neighbour: rank r0 of the next block
+    const bool rightward = hf == 1;
+    const int rL = rightward ? r1 : r0;                          // fed by its partner in this block
+    const int rR = rightward ? r0 : r1;                          // fed by another block
+    const int up = rightward ? (r0 - 1 + P) % P : (r1 + 1) % P;  // rR's upstream neighbour (another block)
+    const int down = rightward ? (r1 + 1) % P : (r0 - 1 + P) % P; // rL's downstream neighbour (another block)
     uint32_t *abort_word = &p.hdr->pad[0];
     const int nsteps = MODE == MODE_ALLREDUCE ? 2 * (P - 1) : P - 1;
+    const size_t row_h = BIDIR ? (size_t)hf * nsteps : 0;       // first signal row of this ring
+    // Chunk rank r works on in reduce-scatter step s: (r-s-2) in the
+    // one-direction ring; (r-1-s) / (r+1+s) in the bidirectional halves.
+    auto chunk_of = [&](int r, int s_) {
+        return BIDIR ? (rightward ? (r - 1 - s_ + 2 * P) % P : (r + 1 + s_) % P) : (r - s_ - 2 + 2 * P) % P;
+    };
 
     __shared__ uint32_t s_epoch0;
     __shared__ int s_abort;
-    __shared__ const uint32_t *s_my_rows;   // signal rows of (rank r0, slice j)
-    __shared__ uint32_t *s_to_rows;         // signal rows of (rank rrank, slice j)
-    __shared__ unsigned long long *s_stamp0, *s_stamp1;   // step stamps of ranks r0 and r1, or null
+    __shared__ const uint32_t *s_my_rows;   // signal rows of (rank rR, slice j, this ring)
+    __shared__ uint32_t *s_to_rows;         // signal rows of (rank down, slice j, this ring)
+    __shared__ unsigned long long *s_stampR, *s_stampL;   // step stamps of ranks rR and rL, or null
     extern __shared__ __align__(16) unsigned char s_hand[];   // p.hand_bytes: the handed-over head
     if (threadIdx.x == 0) {
         s_epoch0 = ld_relaxed_gpu(&p.hdr->epoch);
         s_abort = 0;
-        s_my_rows = p.sig + ((size_t)j * P + r0) * (size_t)p.rows * P;
-        s_to_rows = p.sig + ((size_t)j * P + rrank) * (size_t)p.rows * P;
-        // stamps keep k_ring's layout, one row per (rank, slice): row r * S + j
-        const size_t row0 = (size_t)r0 * S + j, row1 = (size_t)r1 * S + j;
-        s_stamp0 = (p.trace && (row0 + 1) * nsteps * 3 <= p.trace_words) ? p.trace + row0 * nsteps * 3 : nullptr;
-        s_stamp1 = (p.trace && (row1 + 1) * nsteps * 3 <= p.trace_words) ? p.trace + row1 * nsteps * 3 : nullptr;
+        s_my_rows = p.sig + (((size_t)j * P + rR) * (size_t)p.rows + row_h) * P;
+        s_to_rows = p.sig + (((size_t)j * P + down) * (size_t)p.rows + row_h) * P;
+        // stamps keep k_ring's layout, one row per (half, rank, slice): row (h*P + r) * S + j
+        const size_t hbase = BIDIR ? (size_t)hf * P : 0;
+        const size_t rowR = (hbase + rR) * S + j, rowL = (hbase + rL) * S + j;
+        s_stampR = (p.trace && (rowR + 1) * nsteps * 3 <= p.trace_words) ? p.trace + rowR * nsteps * 3 : nullptr;
+        s_stampL = (p.trace && (rowL + 1) * nsteps * 3 <= p.trace_words) ? p.trace + rowL * nsteps * 3 : nullptr;
     }
     __syncthreads();
     if (p.stagger_groups > 1) {   // phase-shifted slice rings, as in k_ring
@@ -222,17 +238,20 @@ __global__ void __launch_bounds__(kPairThreads, RC_PAIR_MIN_BLOCKS) k_ring_pair(
     const uint32_t E0 = s_epoch0;
     const uint32_t E = E0 + 1u;
     const size_t cs = p.chunk_stride;
-    char *slot0 = p.data + (size_t)r0 * p.data_stride;
-    char *slot1 = p.data + (size_t)r1 * p.data_stride;
-    const char *slotl = p.data + (size_t)lrank * p.data_stride;
+    char *slotR = p.data + (size_t)rR * p.data_stride;
+    char *slotL = p.data + (size_t)rL * p.data_stride;
+    const char *slotU = p.data + (size_t)up * p.data_stride;
     const uint32_t sm = (uint32_t)__cvta_generic_to_shared(s_hand);
     constexpr size_t kGroup = 1024 / ES;            // elements of one 32-vector group
     const size_t hmax = (size_t)p.hand_bytes / ES;  // a multiple of kGroup
     uint32_t meet_round = 0;
 
+    const size_t half = p.chunk / 2;
+    const size_t range_lo = BIDIR ? (hf == 0 ? 0 : half) : 0;   // element range of this ring in every chunk
+    const size_t range_n = BIDIR ? (hf == 0 ? half : p.chunk - half) : p.chunk;
     for (int q = 0; q < p.segments; ++q) {
-        const size_t seg_lo = slice_begin(p.chunk, q, p.segments);
-        const size_t seg_n = slice_begin(p.chunk, q + 1, p.segments) - seg_lo;
+        const size_t seg_lo = range_lo + slice_begin(range_n, q, p.segments);
+        const size_t seg_n = range_lo + slice_begin(range_n, q + 1, p.segments) - seg_lo;
         const size_t lo = seg_lo + slice_begin(seg_n, j, S);
         const size_t n = seg_lo + slice_begin(seg_n, j + 1, S) - lo;
         const uint32_t V = E0 + 1u + (uint32_t)q;
@@ -242,19 +261,19 @@ __global__ void __launch_bounds__(kPairThreads, RC_PAIR_MIN_BLOCKS) k_ring_pair(
         const size_t hb = h * ES;
 
         for (int g = 0; g < nsteps; ++g) {
-            // Step stamps (thread 0, first segment): rank r1 waits on no other
+            // Step stamps (thread 0, first segment): rank rL waits on no other
             // block, so its wait starts and ends when its step starts.
-            if (threadIdx.x == 0 && s_stamp1 && q == 0) s_stamp1[3 * g] = s_stamp1[3 * g + 1] = global_timer_ns();
+            if (threadIdx.x == 0 && s_stampL && q == 0) s_stampL[3 * g] = s_stampL[3 * g + 1] = global_timer_ns();
             const bool last = g == nsteps - 1;
-            // ---- 1. rank r1, step g
+            // ---- 1. rank rL, step g
             if (g < P - 1) {
                 const int s = g;
-                const int k = (r1 - s - 2 + 2 * P) % P;
+                const int k = chunk_of(rL, s);
                 const size_t off = ((size_t)k * cs + lo) * ES;
-                const char *a = slot0 + off;   // r0's output of step s-1 (s = 0: r0's input chunk)
-                char *own = slot1 + off;
-                char *dst = (MODE == MODE_REDUCE_SCATTER && s == P - 2) ? p.out + (size_t)r1 * p.out_stride + lo * ES
-                                                                        : own;
+                const char *a = slotR + off;   // rR's output of step s-1 (s = 0: rR's input chunk)
+                char *own = slotL + off;
+                // the last reduce-scatter step stores the finished chunk k to its owner's out slot
+                char *dst = (MODE != MODE_ALLREDUCE && s == P - 2) ? p.out + (size_t)k * p.out_stride + lo * ES : own;
                 const bool drop = p.discard && s >= 1;
                 if (p.discard && s < P - 2) {   // a partial the next block reads next step: keep it in L2
                     if (s == 0)
@@ -262,7 +281,7 @@ __global__ void __launch_bounds__(kPairThreads, RC_PAIR_MIN_BLOCKS) k_ring_pair(
                     else
                         head_add<DT, T, true, false, true, kStEvictLast>(dst, sm, a, own, hv, false);
                     add_range<DT, T, kStEvictLast>(dst + hb, a + hb, own + hb, n - h, drop);
-                } else if constexpr (MODE == MODE_REDUCE_SCATTER) {   // the output chunk
+                } else if constexpr (MODE != MODE_ALLREDUCE) {   // the output chunk
                     if (s == 0)
                         head_add<DT, T, false, false, true, kStNormal>(dst, sm, a, own, hv, false);
                     else
@@ -277,44 +296,44 @@ __global__ void __launch_bounds__(kPairThreads, RC_PAIR_MIN_BLOCKS) k_ring_pair(
                 }
             } else {
                 const int t = g - (P - 1);
-                const int k = (r1 - 1 - t + 2 * P) % P;
+                const int k = (rL - 1 - t + 2 * P) % P;
                 const size_t off = ((size_t)k * cs + lo) * ES;
                 if (last) {
-                    head_copy<T, true, false, kStEvictFirst>(slot1 + off, sm, slot0 + off, hv);
-                    copy_range<ES, T, kStEvictFirst>(slot1 + off + hb, slot0 + off + hb, n - h);
+                    head_copy<T, true, false, kStEvictFirst>(slotL + off, sm, slotR + off, hv);
+                    copy_range<ES, T, kStEvictFirst>(slotL + off + hb, slotR + off + hb, n - h);
                 } else {
-                    head_copy<T, true, false, kPolReadNext>(slot1 + off, sm, slot0 + off, hv);
-                    copy_range<ES, T, kPolReadNext>(slot1 + off + hb, slot0 + off + hb, n - h);
+                    head_copy<T, true, false, kPolReadNext>(slotL + off, sm, slotR + off, hv);
+                    copy_range<ES, T, kPolReadNext>(slotL + off + hb, slotR + off + hb, n - h);
                 }
             }
             // ---- 2. every thread's stores (and reads of the shared head) precede the notify
             __syncthreads();
             // (test hook: a skip aimed at either rank of the block skips the block's notify)
             if (g + 1 < nsteps && threadIdx.x == 0 && !((r0 == p.skip_rank || r1 == p.skip_rank) && g == p.skip_step))
-                st_release_gpu(&s_to_rows[(size_t)(g + 1) * P + r1], V);
+                st_release_gpu(&s_to_rows[(size_t)(g + 1) * P + rL], V);
             if (threadIdx.x == 0 && q == 0) {
-                const unsigned long long now = (s_stamp0 || s_stamp1) ? global_timer_ns() : 0ull;
-                if (s_stamp1) s_stamp1[3 * g + 2] = now;
-                if (s_stamp0) s_stamp0[3 * g] = now;
+                const unsigned long long now = (s_stampR || s_stampL) ? global_timer_ns() : 0ull;
+                if (s_stampL) s_stampL[3 * g + 2] = now;
+                if (s_stampR) s_stampR[3 * g] = now;
             }
-            // ---- 3. wait for the previous block's rank r1
+            // ---- 3. wait for rR's upstream neighbour, in the neighbouring block
             if (g > 0) {
-                if (threadIdx.x == 0 && !wait_row(&s_my_rows[(size_t)g * P + lrank], V, E, p, r0, g, j, abort_word))
+                if (threadIdx.x == 0 && !wait_row(&s_my_rows[(size_t)g * P + up], V, E, p, rR, g, j, abort_word))
                     s_abort = 1;
                 __syncthreads();
                 if (s_abort) break;
             }
-            if (threadIdx.x == 0 && s_stamp0 && q == 0) s_stamp0[3 * g + 1] = global_timer_ns();
-            // ---- 4. rank r0, step g
+            if (threadIdx.x == 0 && s_stampR && q == 0) s_stampR[3 * g + 1] = global_timer_ns();
+            // ---- 4. rank rR, step g
             if (g < P - 1) {
                 const int s = g;
-                const int k = (r0 - s - 2 + 2 * P) % P;
+                const int k = chunk_of(rR, s);
                 const size_t off = ((size_t)k * cs + lo) * ES;
-                const char *a = slotl + off;
-                char *own = slot0 + off;
+                const char *a = slotU + off;
+                char *own = slotR + off;
                 const bool drop = p.discard && s >= 1;
-                if (MODE == MODE_REDUCE_SCATTER && s == P - 2) {   // the reduced chunk: to the output only
-                    char *dst = p.out + (size_t)r0 * p.out_stride + lo * ES;
+                if (MODE != MODE_ALLREDUCE && s == P - 2) {   // the finished chunk: to its owner's output only
+                    char *dst = p.out + (size_t)k * p.out_stride + lo * ES;
                     head_add<DT, T, false, false, true, kStNormal>(dst, sm, a, own, hv, drop);
                     add_range<DT, T, kStNormal>(dst + hb, a + hb, own + hb, n - h, drop);
                 } else if (s == P - 2) {   // all-reduce: the reduced chunk to the slot, its head also to r1
@@ -329,20 +348,20 @@ __global__ void __launch_bounds__(kPairThreads, RC_PAIR_MIN_BLOCKS) k_ring_pair(
                 }
             } else {
                 const int t = g - (P - 1);
-                const int k = (r0 - 1 - t + 2 * P) % P;
+                const int k = (rR - 1 - t + 2 * P) % P;
                 const size_t off = ((size_t)k * cs + lo) * ES;
                 if (last) {
-                    head_copy<T, false, false, kStEvictFirst>(slot0 + off, sm, slotl + off, hv);
-                    copy_range<ES, T, kStEvictFirst>(slot0 + off + hb, slotl + off + hb, n - h);
+                    head_copy<T, false, false, kStEvictFirst>(slotR + off, sm, slotU + off, hv);
+                    copy_range<ES, T, kStEvictFirst>(slotR + off + hb, slotU + off + hb, n - h);
                 } else {
-                    head_copy<T, false, true, kPolNoReread>(slot0 + off, sm, slotl + off, hv);
-                    copy_range<ES, T, kPolReadNext>(slot0 + off + hb, slotl + off + hb, n - h);
+                    head_copy<T, false, true, kPolNoReread>(slotR + off, sm, slotU + off, hv);
+                    copy_range<ES, T, kPolReadNext>(slotR + off + hb, slotU + off + hb, n - h);
                 }
             }
-            __syncthreads();   // the shared head is complete before rank r1 reads it
-            if (threadIdx.x == 0 && s_stamp0 && q == 0) s_stamp0[3 * g + 2] = global_timer_ns();
+            __syncthreads();   // the shared head is complete before rank rL reads it
+            if (threadIdx.x == 0 && s_stampR && q == 0) s_stampR[3 * g + 2] = global_timer_ns();
             if constexpr (SERIAL) {
-                grid_meet(p, ++meet_round, E, abort_word, r0, g, j, &s_abort);
+                grid_meet(p, ++meet_round, E, abort_word, rR, g, j, &s_abort);
                 if (s_abort) break;
             }
         }
@@ -366,9 +385,11 @@ __global__ void __launch_bounds__(kPairThreads, RC_PAIR_MIN_BLOCKS) k_ring_pair(
 template <int DT, bool SERIAL>
 static const void *pair_fn_mode(int mode)
 {
-    return mode == MODE_ALLREDUCE ? (const void *)k_ring_pair<DT, MODE_ALLREDUCE, SERIAL>
-                                  : (const void *)k_ring_pair<DT, MODE_REDUCE_SCATTER, SERIAL>;
+    return mode == MODE_ALLREDUCE       ? (const void *)k_ring_pair<DT, MODE_ALLREDUCE, SERIAL>
+           : mode == MODE_RS_BIDIR      ? (const void *)k_ring_pair<DT, MODE_RS_BIDIR, SERIAL>
+                                        : (const void *)k_ring_pair<DT, MODE_REDUCE_SCATTER, SERIAL>;
 }
+constexpr int kPairModes[3] = {MODE_ALLREDUCE, MODE_REDUCE_SCATTER, MODE_RS_BIDIR};
 
 static const void *pair_fn(int dtype, int mode, bool serial)
 {
@@ -390,8 +411,8 @@ static const void *pair_fn(int dtype, int mode, bool serial)
 static cudaError_t pair_allow_smem(int hand_bytes)
 {
     for (int dt = 0; dt < 3; ++dt)
-        for (int mode = 0; mode < 4; ++mode) {
-            const void *f = pair_fn(dt, (mode & 1) ? MODE_REDUCE_SCATTER : MODE_ALLREDUCE, mode >= 2);
+        for (int mode = 0; mode < 6; ++mode) {
+            const void *f = pair_fn(dt, kPairModes[mode % 3], mode >= 3);
             cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, hand_bytes);
             if (e != cudaSuccess) return e;
         }
@@ -405,11 +426,10 @@ cudaError_t ring_pair_max_coresident(int dtype, int device, int hand_bytes, int 
     int sms = 0, best = 1 << 30;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
-    for (int mode = 0; mode < 4; ++mode) {
+    for (int mode = 0; mode < 6; ++mode) {
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, pair_fn(dtype, (mode & 1) ? MODE_REDUCE_SCATTER : MODE_ALLREDUCE, mode >= 2), kPairThreads,
-            (size_t)hand_bytes);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pair_fn(dtype, kPairModes[mode % 3], mode >= 3),
+                                                          kPairThreads, (size_t)hand_bytes);
         if (e != cudaSuccess) return e;
         if (per_sm < best) best = per_sm;
     }
@@ -422,7 +442,7 @@ cudaError_t launch_ring_pair(const RingParams &p, int dtype, cudaStream_t st)
     RingParams copy = p;
     if (copy.chunk_stride == 0) copy.chunk_stride = copy.chunk;
     void *args[] = {(void *)&copy};
-    const unsigned blocks = (unsigned)(p.P / 2 * p.S);
+    const unsigned blocks = (unsigned)(p.P / 2 * p.S) * (p.mode == MODE_RS_BIDIR ? 2u : 1u);
     return cudaLaunchCooperativeKernel(pair_fn(dtype, copy.mode, copy.debug_serial != 0), dim3(blocks),
                                        dim3((unsigned)kPairThreads), args, (size_t)copy.hand_bytes, st);
 }

@@ -30,7 +30,8 @@
 // kernel's phase-shifted slice rings.
 //
 // Usage: ring_protocol_model MODE P S SEGMENTS LAUNCHES N_PER_RANK [early_notify|stagger]
-//   MODE: allreduce | reduce_scatter | all_gather | rs_bidir | allreduce_pair | reduce_scatter_pair
+//   MODE: allreduce | reduce_scatter | all_gather | rs_bidir | allreduce_pair | reduce_scatter_pair |
+//         rs_bidir_pair
 // Exit status 0 with "ok" when every launch produced the expected result.
 #include <atomic>
 #include <chrono>
@@ -137,47 +138,58 @@ void block(const Launch &L, int h, int r, int j)
     }
 }
 
-void pair_block(const Launch &L, int m, int j)
+// Thread (h, m, j): ranks 2m and 2m+1 of ring h (h = 1 runs towards higher
+// ranks; the bidirectional mode's h = 0 runs towards lower ones).  rL is fed
+// by its partner in the thread, rR by the neighbouring thread.
+void pair_block(const Launch &L, int h, int m, int j)
 {
     const int P = L.P, S = L.S;
-    const int r0 = 2 * m, r1 = 2 * m + 1, lrank = (r0 - 1 + P) % P, rrank = (r1 + 1) % P;
+    const bool bidir = L.mode == RS_BIDIR, rightward = h == 1;
+    const int r0 = 2 * m, r1 = 2 * m + 1;
+    const int rL = rightward ? r1 : r0, rR = rightward ? r0 : r1;
+    const int up = rightward ? (r0 - 1 + P) % P : (r1 + 1) % P, down = rightward ? (r1 + 1) % P : (r0 - 1 + P) % P;
+    auto chunk_of = [&](int r, int s) {
+        return bidir ? (rightward ? (r - 1 - s + 2 * P) % P : (r + 1 + s) % P) : (r - s - 2 + 2 * P) % P;
+    };
     const uint32_t E0 = L.epoch->load(std::memory_order_relaxed);
     if (L.stagger && j % 3) std::this_thread::sleep_for(std::chrono::microseconds(50 * (j % 3)));
-    std::atomic<uint32_t> *my_rows = L.sig + ((size_t)j * P + r0) * L.rows * P;
-    std::atomic<uint32_t> *to_rows = L.sig + ((size_t)j * P + rrank) * L.rows * P;
-    const size_t c = L.chunk;
-    uint32_t *s0 = L.data + (size_t)r0 * L.stride, *s1 = L.data + (size_t)r1 * L.stride;
-    const uint32_t *sl = L.data + (size_t)lrank * L.stride;
+    const size_t row_h = bidir ? (size_t)h * L.nsteps : 0;
+    std::atomic<uint32_t> *my_rows = L.sig + (((size_t)j * P + rR) * L.rows + row_h) * P;
+    std::atomic<uint32_t> *to_rows = L.sig + (((size_t)j * P + down) * L.rows + row_h) * P;
+    const size_t c = L.chunk, half = c / 2;
+    const size_t range_lo = bidir ? (h == 0 ? 0 : half) : 0, range_n = bidir ? (h == 0 ? half : c - half) : c;
+    uint32_t *s0 = L.data + (size_t)rR * L.stride, *s1 = L.data + (size_t)rL * L.stride;
+    const uint32_t *sl = L.data + (size_t)up * L.stride;
     std::vector<uint32_t> hand;
     for (int q = 0; q < L.segments; ++q) {
-        const size_t seg_lo = part_begin(c, q, L.segments);
-        const size_t seg_n = part_begin(c, q + 1, L.segments) - seg_lo;
+        const size_t seg_lo = range_lo + part_begin(range_n, q, L.segments);
+        const size_t seg_n = range_lo + part_begin(range_n, q + 1, L.segments) - seg_lo;
         const size_t lo = seg_lo + part_begin(seg_n, j, S);
         const size_t n = seg_lo + part_begin(seg_n, j + 1, S) - lo;
         const uint32_t V = E0 + 1u + (uint32_t)q;
         const size_t h = n / 2;   // head of the slice handed from rank r0 to r1 in private memory
         hand.assign(h, 0u);
-        auto notify = [&](int row) { to_rows[(size_t)row * P + r1].store(V, std::memory_order_release); };
+        auto notify = [&](int row) { to_rows[(size_t)row * P + rL].store(V, std::memory_order_release); };
         for (int g = 0; g < L.nsteps; ++g) {
             const bool notify_next = g + 1 < L.nsteps;
             const bool last = g == L.nsteps - 1;
             if (L.early_notify && notify_next) notify(g + 1);
-            // rank r1: needs only rank r0's previous step (this thread)
+            // rank rL: needs only rank rR's previous step (this thread)
             if (g < P - 1) {
-                const int k = (r1 - g - 2 + 2 * P) % P;
-                uint32_t *dst = (L.mode == REDUCE_SCATTER && g == P - 2) ? L.out + (size_t)r1 * c : s1 + (size_t)k * c;
+                const int k = chunk_of(rL, g);
+                uint32_t *dst = (L.mode != ALLREDUCE && g == P - 2) ? L.out + (size_t)k * c : s1 + (size_t)k * c;
                 for (size_t i = 0; i < n; ++i) {
                     const uint32_t a = (i < h && g >= 1) ? hand[i] : s0[(size_t)k * c + lo + i];
                     dst[lo + i] = a + s1[(size_t)k * c + lo + i];
                 }
             } else {
-                const int k = (r1 - 1 - (g - (P - 1)) + 2 * P) % P;
+                const int k = (rL - 1 - (g - (P - 1)) + 2 * P) % P;
                 for (size_t i = 0; i < n; ++i) s1[(size_t)k * c + lo + i] = i < h ? hand[i] : s0[(size_t)k * c + lo + i];
             }
             if (!L.early_notify && notify_next) notify(g + 1);
-            // rank r0: waits for thread m-1 (rank r0's left neighbour)
+            // rank rR: waits for the neighbouring thread (rank rR's upstream neighbour)
             if (g > 0) {
-                std::atomic<uint32_t> &f = my_rows[(size_t)g * P + lrank];
+                std::atomic<uint32_t> &f = my_rows[(size_t)g * P + up];
                 for (long spins = 0; !reached(f.load(std::memory_order_acquire), V); ++spins) {
                     if (spins > 400000000L) {
                         std::fprintf(stderr, "wait gave up: pair %d step %d slice %d\n", m, g, j);
@@ -187,11 +199,11 @@ void pair_block(const Launch &L, int m, int j)
                 }
             }
             if (g < P - 1) {
-                const int k = (r0 - g - 2 + 2 * P) % P;
+                const int k = chunk_of(rR, g);
                 for (size_t i = 0; i < n; ++i) {
                     const uint32_t v = sl[(size_t)k * c + lo + i] + s0[(size_t)k * c + lo + i];
-                    if (L.mode == REDUCE_SCATTER && g == P - 2) {
-                        L.out[(size_t)r0 * c + lo + i] = v;
+                    if (L.mode != ALLREDUCE && g == P - 2) {
+                        L.out[(size_t)k * c + lo + i] = v;
                     } else if (g == P - 2) {
                         s0[(size_t)k * c + lo + i] = v;
                         if (i < h) hand[i] = v;
@@ -202,7 +214,7 @@ void pair_block(const Launch &L, int m, int j)
                     }
                 }
             } else {
-                const int k = (r0 - 1 - (g - (P - 1)) + 2 * P) % P;
+                const int k = (rR - 1 - (g - (P - 1)) + 2 * P) % P;
                 for (size_t i = 0; i < n; ++i) {
                     const uint32_t v = sl[(size_t)k * c + lo + i];
                     s0[(size_t)k * c + lo + i] = v;
@@ -226,7 +238,7 @@ int main(int argc, char **argv)
         return 2;
     }
     const std::string ms = argv[1];
-    const bool pair = ms == "allreduce_pair" || ms == "reduce_scatter_pair";
+    const bool pair = ms == "allreduce_pair" || ms == "reduce_scatter_pair" || ms == "rs_bidir_pair";
     const Mode mode = (ms == "allreduce" || ms == "allreduce_pair") ? ALLREDUCE
                       : (ms == "reduce_scatter" || ms == "reduce_scatter_pair") ? REDUCE_SCATTER
                       : ms == "all_gather" ? ALL_GATHER : RS_BIDIR;
@@ -262,11 +274,12 @@ int main(int argc, char **argv)
             data = x;
         }
         Launch L{mode, pair, P, S, G, rows, nsteps, chunk, data.data(), slot, in.data(), out.data(), sig.data(),
-                 &epoch, &done, pair ? P / 2 * S : P * S * halves, early, stagger};
+                 &epoch, &done, pair ? P / 2 * S * halves : P * S * halves, early, stagger};
         std::vector<std::thread> th;
         if (pair) {
-            for (int m = 0; m < P / 2; ++m)
-                for (int j = 0; j < S; ++j) th.emplace_back(pair_block, std::cref(L), m, j);
+            for (int h = 0; h < halves; ++h)
+                for (int m = 0; m < P / 2; ++m)
+                    for (int j = 0; j < S; ++j) th.emplace_back(pair_block, std::cref(L), halves == 2 ? h : 1, m, j);
         } else {
             for (int h = 0; h < halves; ++h)
                 for (int r = 0; r < P; ++r)

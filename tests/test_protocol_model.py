@@ -50,7 +50,7 @@ def test_protocol_is_race_free_and_correct(model, mode, P, S, G, launches, n):
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr[-2000:]
 
 
-@pytest.mark.parametrize("mode", ["allreduce_pair", "reduce_scatter_pair"])
+@pytest.mark.parametrize("mode", ["allreduce_pair", "reduce_scatter_pair", "rs_bidir_pair"])
 @pytest.mark.parametrize("P,S,G,launches,n", [(2, 1, 1, 3, 8), (2, 3, 2, 2, 998), (4, 3, 1, 3, 1204),
                                               (6, 2, 3, 2, 1506), (8, 4, 2, 2, 4096)])
 def test_pair_protocol_is_race_free_and_correct(model, mode, P, S, G, launches, n):
@@ -62,7 +62,7 @@ def test_pair_protocol_is_race_free_and_correct(model, mode, P, S, G, launches, 
 
 
 @pytest.mark.parametrize("mode", ["allreduce", "reduce_scatter", "rs_bidir", "allreduce_pair",
-                                  "reduce_scatter_pair"])
+                                  "reduce_scatter_pair", "rs_bidir_pair"])
 def test_staggered_slice_starts_are_race_free(model, mode):
     """Slice rings that start at different times (the kernel's phase-shifted
     rings) keep the protocol race-free and the results exact."""
@@ -72,7 +72,7 @@ def test_staggered_slice_starts_are_race_free(model, mode):
 
 
 @pytest.mark.parametrize("mode", ["allreduce", "reduce_scatter", "all_gather", "rs_bidir", "allreduce_pair",
-                                  "reduce_scatter_pair"])
+                                  "reduce_scatter_pair", "rs_bidir_pair"])
 def test_early_notify_is_reported(model, mode):
     """Planted error: signalling the next step before this step's stores lets
     the neighbour read a chunk while it is written; ThreadSanitizer must say so."""
