@@ -36,25 +36,31 @@ std::mutex g_mu;
 
 constexpr int kMaxDevices = 64;
 // One ring step touches a chunk of every rank.  When those P chunks exceed
-// kL2NoSplitBytes, the chunks are split into segments of at most
-// kDefaultL2LiveBytes run one after another, so the partial sums of a step
-// stay in L2 until the next step reads them.  Both measured on GB300
-// (126 MB L2): up to 64 MiB of live chunks one pass is fastest (each segment
-// adds 2(P-1) signal steps); above it, 48 MiB segments beat 32, 64 and
-// 96 MiB by 1-7 % (checked at P = 8, 16 and 32 with 16 MiB chunks).
+// kL2NoSplitBytes, the chunks are split into segments run one after another,
+// so the partial sums of a step stay in L2 until the next step reads them.
+// Segment budgets measured on GB300 (126 MB L2; each segment adds 2(P-1)
+// signal steps): up to 64 MiB of live chunks one pass is fastest; above it,
+// k_ring runs best with 48 MiB segments (beating 32, 64 and 96 MiB by 1-7 %
+// at P = 8, 16 and 32 with 16 MiB chunks), k_ring_pair -- which keeps the
+// in-block hop's heads out of L2 -- with 64 MiB ones (P = 8 / 16 / 32:
+// 24 MiB 0.515 / 2.15 / 9.14 ms, 32 MiB 0.436 / 1.87 / 7.74, 48 MiB
+// 0.410 / 1.79 / 7.02, 64 MiB 0.388 / 1.70 / 6.57, 96 MiB 0.389 / 1.76 /
+// 6.69).
 constexpr size_t kDefaultL2LiveBytes = 48ull << 20;
+constexpr size_t kPairL2LiveBytes = 64ull << 20;
 constexpr size_t kL2NoSplitBytes = 64ull << 20;
 
-// Tuning knob, read once from the environment: RC_L2_LIVE_BYTES (bytes;
-// unset or malformed = the default above; 0 = never segment).
-size_t l2_live_bytes()
+// Tuning knob, read once from the environment: RC_L2_LIVE_BYTES (bytes; 0 =
+// never segment); unset or malformed: the kernel's default above (returned
+// as SIZE_MAX here).
+size_t l2_live_bytes_setting()
 {
     static const size_t v = [] {
         const char *e = getenv("RC_L2_LIVE_BYTES");
-        if (!e || !*e) return kDefaultL2LiveBytes;
+        if (!e || !*e) return SIZE_MAX;
         char *end = nullptr;
         const unsigned long long x = strtoull(e, &end, 10);
-        return (end && *end == 0) ? (size_t)x : kDefaultL2LiveBytes;
+        return (end && *end == 0) ? (size_t)x : SIZE_MAX;
     }();
     return v;
 }
@@ -335,7 +341,9 @@ int plan_ring(rc::RingParams &p, int dtype, DeviceState *st, int allow_pair = 1)
         rc_ = choose_slices(st->max_blocks[dtype], p.P * rings, ring_elems, ring_elems * es, &p.S);
     if (rc_) return rc_;
     {
-        const size_t live = (size_t)p.P * p.chunk * es, budget = l2_live_bytes();
+        const size_t setting = l2_live_bytes_setting();
+        const size_t dflt = p.pair ? kPairL2LiveBytes : kDefaultL2LiveBytes;
+        const size_t live = (size_t)p.P * p.chunk * es, budget = setting == SIZE_MAX ? dflt : setting;
         const bool split = budget && (live > kL2NoSplitBytes || budget < kDefaultL2LiveBytes);
         size_t G = split ? (live + budget - 1) / budget : 1;
         const size_t max_g = ring_elems / ((size_t)p.S * rc::kSliceGranule); // keep every slice non-empty
