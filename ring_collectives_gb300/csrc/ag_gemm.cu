@@ -46,7 +46,13 @@ constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
 constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;   // 16 KiB
 constexpr int B_STAGE = BN * BK * 2;   // 32 KiB
-constexpr int STAGING = 16384;         // gather staging buffer (x2)
+// Gather staging buffer bytes (two of them).  Measured on GB300 (P=8,
+// 8192x4096x4096, one box): 4 KiB 0.177 ms, 8 KiB 0.171, 16 KiB 0.169;
+// larger does not fit beside three 64 KiB operand stages.
+#ifndef RC_AG_GEMM_STAGING
+#define RC_AG_GEMM_STAGING 16384
+#endif
+constexpr int STAGING = RC_AG_GEMM_STAGING; // gather staging buffer (x2)
 constexpr int PIECE_ROWS = 16;         // rows per gather unit (one ready flag each)
 constexpr int THREADS = 256;
 constexpr int TMEM_COLS = 512;         // two 128x256 fp32 accumulators
