@@ -231,8 +231,14 @@ int current_device(int *dev_out, DeviceState **st_out)
                 e = rc::ring_max_coresident(dt, rc::kRingThreads, dev, &st.max_blocks[dt]);
                 if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
                 if (pair_enabled()) {
+                    // Without a usable launch shape for the two-rank kernel
+                    // (e.g. a shared-memory setting this device cannot grant)
+                    // every ring collective runs on k_ring instead.
                     e = rc::ring_pair_max_coresident(dt, dev, pair_smem_bytes(), &st.pair_blocks[dt]);
-                    if (e != cudaSuccess) return cuda_fail(e, "occupancy query (pair kernel)");
+                    if (e != cudaSuccess) {
+                        (void)cudaGetLastError();
+                        st.pair_blocks[dt] = 0;
+                    }
                 }
             }
         }

@@ -386,6 +386,8 @@ for P, c, dt in ((8, 64 * 500 + 8, torch.float32), (5, 64 * 333, torch.bfloat16)
     agi = x[:, :c].contiguous()
     ago = torch.zeros((P, P * c), dtype=dt, device="cuda")
     rc.ring_all_gather(agi.cuda(), ago)
+    ob = torch.empty((P, c), dtype=dt, device="cuda")
+    rc.ring_reduce_scatter_bidir(x.cuda(), ob)
     assert rc.ring_status() == 0, rc.ring_last_error()
     name = {torch.float32: "f32", torch.bfloat16: "bf16", torch.int32: "i32"}[dt]
     def npv(t):
@@ -395,6 +397,7 @@ for P, c, dt in ((8, 64 * 500 + 8, torch.float32), (5, 64 * 333, torch.bfloat16)
     assert np.array_equal(npv(b), oracle.ring_allreduce(xn.copy(), name)), ("allreduce", P, c, name)
     assert np.array_equal(npv(o), oracle.reduce_scatter(xn.copy(), name)), ("reduce_scatter", P, c, name)
     assert np.array_equal(npv(ago), oracle.all_gather(npv(agi), name)), ("all_gather", P, c, name)
+    assert np.array_equal(npv(ob), oracle.reduce_scatter_bidir(xn.copy(), name)), ("bidir", P, c, name)
 print("ok")
 """
 
@@ -467,6 +470,23 @@ def test_stagger_settings_child(groups):
     env = dict(os.environ, RC_RING_STAGGER=groups)
     r = subprocess.run([sys.executable, "-c", _SEGMENT_CHILD, ROOT], env=env, capture_output=True, text=True,
                        timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("env", [{"RC_RING_PAIR": "0"}, {"RC_PAIR_SMEM": "0"}, {"RC_PAIR_SMEM": "8192"},
+                                 {"RC_PAIR_SMEM": "163840"}])
+def test_ring_kernel_settings_child(env):
+    """The same collectives with one rank per thread block everywhere
+    (RC_RING_PAIR=0), and with two-rank blocks that hand no head over in
+    shared memory, a small head (8 KiB: most of every slice through the
+    slots) or a large one (160 KiB: one block per SM, whole slices in
+    shared memory): always the oracle's bits."""
+    import os
+    import subprocess
+    import sys
+    from tests.conftest import ROOT
+    r = subprocess.run([sys.executable, "-c", _SEGMENT_CHILD, ROOT], env=dict(os.environ, **env),
+                       capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
 
 
