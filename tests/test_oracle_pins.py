@@ -560,3 +560,52 @@ def test_gemm_rs_oracle_integer_exact_and_p1():
     assert np.array_equal(exact, full.astype(np.float64))
     out1, _, _, _ = oracle.gemm_rs(A[:1], B[:1, :2])
     assert np.array_equal(oracle.f32_from_bf16(out1[0]), (Ai[0] @ Bi[0, :2].T).astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_nan_and_infinity_positions_follow_the_ieee_closed_form(dtype):
+    """Where an element's result is NaN is fixed by IEEE arithmetic alone,
+    whatever the fold order: NaN exactly where some rank holds a NaN, or
+    some rank holds +inf and another -inf; otherwise +inf (-inf) where an
+    infinity of one sign is present; otherwise finite.  Pins the oracle's
+    all-reduce, both reduce-scatters and psum against that closed form
+    (the library is held to the same positions on the GPU)."""
+    P, c = 6, 40
+    N = P * c
+    g = np.random.default_rng(17)
+    x = g.standard_normal((P, N)).astype(np.float32)
+    pos = g.choice(N, 24, replace=False)
+    for i, p_ in enumerate(pos):
+        r = int(g.integers(P))
+        if i % 4 == 0:
+            x[r, p_] = np.nan
+        elif i % 4 == 1:
+            x[r, p_] = np.inf
+            x[(r + 1) % P, p_] = -np.inf
+        elif i % 4 == 2:
+            x[r, p_] = np.inf
+        else:
+            x[r, p_] = -np.inf
+    nan = np.isnan(x).any(0) | ((x == np.inf).any(0) & (x == -np.inf).any(0))
+    pinf = ~nan & (x == np.inf).any(0)
+    ninf = ~nan & (x == -np.inf).any(0)
+    if dtype == "bf16":
+        xo = oracle.bf16_from_f32(x)
+        tof = oracle.f32_from_bf16
+    else:
+        xo = x
+        tof = np.asarray
+
+    def check(got, cols):
+        f = tof(got)
+        assert np.array_equal(np.isnan(f), np.broadcast_to(nan[cols], f.shape))
+        assert np.array_equal(f == np.inf, np.broadcast_to(pinf[cols], f.shape))
+        assert np.array_equal(f == -np.inf, np.broadcast_to(ninf[cols], f.shape))
+
+    check(oracle.ring_allreduce(xo.copy(), dtype), slice(None))
+    check(oracle.psum(xo.copy(), dtype), slice(None))
+    rs = oracle.reduce_scatter(xo.copy(), dtype)        # out[r] = chunk r
+    bd = oracle.reduce_scatter_bidir(xo.copy(), dtype)
+    for r in range(P):
+        check(rs[r], slice(r * c, (r + 1) * c))
+        check(bd[r], slice(r * c, (r + 1) * c))
