@@ -18,9 +18,10 @@
 //               and releases smem stages / accumulators with tcgen05.commit.
 //   warp 2      allocates TMEM (512 columns) and, on one thread, runs the
 //               gather producer: 16-row pieces of the shards are copied into
-//               A_g with bulk copies through two 16 KiB staging buffers, in
+//               A_g with bulk copies through 32 KiB of staging buffers, in
 //               the order the consumers need them, and each piece publishes
-//               its ready flag (st.release of the launch epoch).
+//               its ready flag (st.release of the launch epoch).  (The
+//               CTA-pair form below gathers on part of the grid only.)
 //   warps 4-7   epilogue: TMEM -> registers (tcgen05.ld), fp32 -> bf16 (RNE),
 //               stores to C, then free the accumulator for the MMA warp.
 // Rows of the own rank are read straight from its shard (local data, no
@@ -53,6 +54,47 @@ constexpr int B_STAGE = BN * BK * 2;   // 32 KiB
 #define RC_AG_GEMM_STAGING 16384
 #endif
 constexpr int STAGING = RC_AG_GEMM_STAGING; // gather staging buffer (x2)
+// CTA-pair form: the A producer looks at the ready flags of its next tile
+// half-way through the current one and then every RC_AG_POLL_EVERY stages
+// until it sees them set (0: only the one look half-way through).
+#ifndef RC_AG_POLL_EVERY
+#define RC_AG_POLL_EVERY 4
+#endif
+constexpr int POLL_EVERY = RC_AG_POLL_EVERY > 0 ? RC_AG_POLL_EVERY : 1 << 20;
+// Gather copies with L2 eviction hints (1): other ranks' shard rows, read
+// once, are loaded evict_first so that they do not push the GEMM's operands
+// out of L2.
+#ifndef RC_AG_GATHER_HINT
+#define RC_AG_GATHER_HINT 1
+#endif
+// CTA-pair form: the gather's staging space (2 x STAGING bytes) as a ring of
+// RC_AG_GATHER_BUFS buffers, all but one of them loading at any time.
+#ifndef RC_AG_GATHER_BUFS
+#define RC_AG_GATHER_BUFS 4
+#endif
+constexpr int GB = RC_AG_GATHER_BUFS;
+// CTA-pair form: C, which nothing reads in the launch, is stored
+// evict_first (RC_AG_C_POLICY 1; 0 normal), so that the 64 MiB it streams
+// through L2 does not push out operand rows still to be read.
+#ifndef RC_AG_C_POLICY
+#define RC_AG_C_POLICY 1
+#endif
+constexpr int C_POL = RC_AG_C_POLICY ? kStEvictFirst : kStNormal;
+// CTA-pair form, who gathers.  When the tiles do not divide evenly, pairs
+// numbered below total_tiles % npairs run one tile more than the rest.  Per
+// round of gather units, each CTA of such a pair takes RC_AG_GATHER_NW units
+// and each CTA of the other pairs RC_AG_GATHER_SW: the gather's bulk copies
+// share the SM's copy engine with the GEMM's operand loads, so they go where
+// the SM has time to spare.
+#ifndef RC_AG_GATHER_NW
+#define RC_AG_GATHER_NW 0
+#endif
+#ifndef RC_AG_GATHER_SW
+#define RC_AG_GATHER_SW 1
+#endif
+static_assert(RC_AG_GATHER_NW >= 0 && RC_AG_GATHER_SW >= 1, "every round needs a gathering CTA");
+constexpr int GCH = 2 * STAGING / GB;   // bytes per gather buffer
+static_assert(GB >= 2 && GB <= 8 && GCH % 16 == 0, "gather ring: 2..8 buffers of whole 16-byte units");
 constexpr int PIECE_ROWS = 16;         // rows per gather unit (one ready flag each)
 constexpr int THREADS = 256;
 constexpr int TMEM_COLS = 512;         // two 128x256 fp32 accumulators
@@ -81,14 +123,15 @@ constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 // lane's row of C.  Each lane owns a row, so a warp's store touches 32 rows;
 // 32-byte stores fill whole sectors (measured on GB300: the 16-byte form
 // costs the epilogue about twice the store time).
+template <int POL = kStNormal>
 __device__ __forceinline__ void store_row32(char *dst, const uint32_t (&v)[32], bool st32)
 {
     uint32_t b[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) b[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
     if (st32) {
-        st8<kStNormal>(dst, make_uint4(b[0], b[1], b[2], b[3]), make_uint4(b[4], b[5], b[6], b[7]));
-        st8<kStNormal>(dst + 32, make_uint4(b[8], b[9], b[10], b[11]), make_uint4(b[12], b[13], b[14], b[15]));
+        st8<POL>(dst, make_uint4(b[0], b[1], b[2], b[3]), make_uint4(b[4], b[5], b[6], b[7]));
+        st8<POL>(dst + 32, make_uint4(b[8], b[9], b[10], b[11]), make_uint4(b[12], b[13], b[14], b[15]));
     } else {
 #pragma unroll
         for (int w = 0; w < 4; ++w) st_v4(dst + w * 16, make_uint4(b[4 * w], b[4 * w + 1], b[4 * w + 2], b[4 * w + 3]));
@@ -150,6 +193,22 @@ __device__ bool wait_block_flags(const uint32_t *f, uint32_t E, const Abort &ab,
         }
         __nanosleep(64);
     }
+}
+
+// One non-blocking look at the ready flags of a 128-row block of A_g: true
+// (after an acquire fence, as in wait_block_flags) if all of them have
+// reached the launch's epoch.
+__device__ bool poll_block_flags(const uint32_t *f, uint32_t E)
+{
+    constexpr int NF = BM / PIECE_ROWS;
+    uint32_t v[NF];
+#pragma unroll
+    for (int q = 0; q < NF; ++q) v[q] = ld_relaxed_gpu(f + q);
+    bool all = true;
+#pragma unroll
+    for (int q = 0; q < NF; ++q) all = all && epoch_reached(v[q], E);
+    if (all) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    return all;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -376,7 +435,24 @@ __global__ void __launch_bounds__(THREADS, 1)
 // bytes per clock per SM that tiled TMA loads reach on GB300), the even CTA
 // issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and both CTAs drain
 // their own 128 rows of D.  Each CTA waits only on the ready flags of its own
-// 128 A rows; the gather producer runs in every CTA, as in the one-CTA form.
+// 128 A rows.  What differs from the one-CTA form (measured on GB300, P=8,
+// 8192x4096x4096, CUDA events over 30 back-to-back calls):
+//  * the A producer looks at the next tile's flags from half-way through the
+//    current tile (a flag round trip at the tile boundary left the MMA idle:
+//    0.1633 -> 0.1604 ms);
+//  * the gather streams each unit through a ring of 4 staging buffers with 3
+//    loads in flight (one load at a time ran at ~10 GB/s per CTA), loading
+//    other ranks' rows evict_first;
+//  * the gather runs on the CTAs of the pairs with one tile fewer: its bulk
+//    copies share the SM's copy engine with the operand loads, and on the
+//    pairs that set the launch's length it slowed the first tiles by ~3 us
+//    each (0.1591 ms with every CTA gathering, 0.1580 with a 1:3 share,
+//    0.1551 with the spare pairs alone);
+//  * C is stored evict_first (0.1592 -> 0.1552 ms).
+// Without the gather and its waits the same kernel takes 0.1433 ms, as much
+// as cuBLAS on the plain GEMM; in-kernel clock stamps put the SM clock at
+// 1.6-1.9 GHz during the launch (the power limit), so tiles after the first
+// run at ~94 % of the tensor pipe's per-cycle peak.
 constexpr int PM = 256, PN = 256, HM = 128, HN = 128;
 constexpr int BK2 = RC_GEMM_PAIR_BK;     // K per stage: KSUB2 64-column swizzled sub-tiles
 constexpr int KSUB2 = BK2 / 64;
@@ -401,11 +477,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t bars = smem_u32(bars_g);
     const uint32_t full_bar = bars, empty_bar = bars + 8 * STAGES2;
     const uint32_t tfull_bar = bars + 16 * STAGES2, tempty_bar = tfull_bar + 16;
-    const uint32_t gat_bar = tempty_bar + 16;
-    const uint32_t drain_bar = gat_bar + 16;
-    uint32_t *tmem_slot = (uint32_t *)(bars_g + 16 * STAGES2 + 56);
-    int *abort_flag = (int *)(bars_g + 16 * STAGES2 + 60);
-    uint32_t *epoch_slot = (uint32_t *)(bars_g + 16 * STAGES2 + 64);
+    const uint32_t gat_bar = tempty_bar + 16;          // GB gather buffers
+    const uint32_t drain_bar = gat_bar + 8 * GB;
+    uint32_t *tmem_slot = (uint32_t *)(bars_g + 16 * STAGES2 + 40 + 8 * GB);
+    int *abort_flag = (int *)(bars_g + 16 * STAGES2 + 44 + 8 * GB);
+    uint32_t *epoch_slot = (uint32_t *)(bars_g + 16 * STAGES2 + 48 + 8 * GB);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t cta = cluster_ctarank();
@@ -418,8 +494,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar + 8 * a, 1);
             mbar_init(tempty_bar + 8 * a, 8);   // four epilogue warps of each CTA
-            mbar_init(gat_bar + 8 * a, 1);
         }
+        for (int b = 0; b < GB; ++b) mbar_init(gat_bar + 8 * b, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         *epoch_slot = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
@@ -461,6 +537,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // ---------------- TMA producer (both CTAs): this CTA's halves of A and B
         uint32_t stage = 0, phase = 0;
         int issued[STAGES2] = {};
+        bool next_ready = false;   // the next tile's flags were already seen set (and acquired)
         for (int t = pair; t < p.total_tiles && !*(volatile int *)abort_flag; t += npairs) {
             int m, n;
             tile_of(p, t, m, n);
@@ -468,8 +545,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int src_rank = row0 / p.M_r;
             const bool own = src_rank == p.rank;
             if (!own && a_producer) {
-                if (!wait_block_flags(&p.flags[(row0 / BM) * (BM / PIECE_ROWS)], E, ab, 1)) break;
+                if (!next_ready && !wait_block_flags(&p.flags[(row0 / BM) * (BM / PIECE_ROWS)], E, ab, 1)) break;
                 fence_proxy_async_global();
+            }
+            // Looks at the next tile's flags: at the boundary the MMA has
+            // only the last STAGES2 stages of this tile queued, less work than
+            // one flag round trip plus one load; from half-way through the
+            // tile on, each round trip hides behind the queued stages.  If no
+            // look sees them set, the wait stays at the boundary.
+            next_ready = false;
+            const uint32_t *next_flags = nullptr;
+            if (a_producer && t + npairs < p.total_tiles) {
+                int mn, nn;
+                tile_of(p, t + npairs, mn, nn);
+                const int nrow0 = mn * PM + (int)cta * HM;
+                if (nrow0 / p.M_r != p.rank) next_flags = &p.flags[(nrow0 / BM) * (BM / PIECE_ROWS)];
             }
             const int row_in_shard = row0 % p.M_r;
             bool ok = true;
@@ -499,6 +589,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     stage = 0;
                     phase ^= 1u;
                 }
+                if (next_flags && !next_ready && kb >= ksteps / 2 && (kb - ksteps / 2) % POLL_EVERY == 0)
+                    next_ready = poll_block_flags(next_flags, E);
             }
             if (!ok) break;
         }
@@ -547,33 +639,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tc_commit_pair_mc(drain_bar, 1);
         wait_bar(drain_bar, 0, ab, 10, true);
     } else if (warp == 2 && lane == 0) {
-        // ---------------- gather producer (every CTA; units spread over the whole grid)
+        // ---------------- gather producer (units shared out by RC_AG_GATHER_NW / _SW)
+        // Each unit streams through a ring of GB staging buffers: a load
+        // (global -> shared) per buffer in flight, and a buffer is refilled
+        // once the store (shared -> A_g) of its previous chunk has read it.
         const size_t row_bytes = (size_t)p.K * 2;
         const size_t unit_bytes = (size_t)PIECE_ROWS * row_bytes;
-        uint32_t gphase[2] = {0, 0};
-        uint64_t piece_no = 0;
-        for (int u = blockIdx.x; u < p.units && !*(volatile int *)abort_flag; u += gridDim.x) {
+        const int nch = (int)((unit_bytes + GCH - 1) / GCH);
+        const uint64_t pol_once = policy_evict_first();
+        uint32_t gph = 0;   // bit b: parity of gather buffer b's next completion
+        const int full_pairs = p.total_tiles % npairs;
+        const int nw = full_pairs ? RC_AG_GATHER_NW : 1, sw = full_pairs ? RC_AG_GATHER_SW : 1;
+        const int n_full = 2 * full_pairs;                                // CTAs of the pairs with the extra tile
+        const int per_round = n_full * nw + ((int)gridDim.x - n_full) * sw;
+        const bool spare = (int)blockIdx.x >= n_full;
+        const int my_w = spare ? sw : nw;
+        const int first = spare ? n_full * nw + ((int)blockIdx.x - n_full) * sw : (int)blockIdx.x * nw;
+        for (int i = 0; my_w > 0 && !*(volatile int *)abort_flag; ++i) {
+            const int u = first + (i / my_w) * per_round + i % my_w;   // increasing in i
+            if (u >= p.units) break;
             int mb, piece;
             unit_of(p, u, mb, piece);
             const int row = mb * BM + piece * PIECE_ROWS;
             const int src_rank = row / p.M_r;
             const char *src = p.a_shards + (size_t)src_rank * p.a_stride + (size_t)(row % p.M_r) * row_bytes;
             char *dst = p.a_gathered + (size_t)row * row_bytes;
+            // Other ranks' rows are read once here (the GEMM reads them from
+            // A_g); the own rank's rows are also the GEMM's operand.
+            const bool once = RC_AG_GATHER_HINT && src_rank != p.rank;
+            auto chunk_bytes = [&](int c) -> uint32_t {
+                const size_t off = (size_t)c * GCH;
+                return (uint32_t)(unit_bytes - off < (size_t)GCH ? unit_bytes - off : (size_t)GCH);
+            };
+            auto load = [&](int c) {
+                const int b = c % GB;
+                mbar_expect_tx(gat_bar + 8 * b, chunk_bytes(c));
+                if (once)
+                    bulk_g2s_hint(sStage + b * GCH, src + (size_t)c * GCH, chunk_bytes(c), gat_bar + 8 * b, pol_once);
+                else
+                    bulk_g2s(sStage + b * GCH, src + (size_t)c * GCH, chunk_bytes(c), gat_bar + 8 * b);
+            };
+            int issued = 0;
+            for (; issued < nch && issued < GB; ++issued) load(issued);
             bool ok = true;
-            for (size_t off = 0; off < unit_bytes; off += STAGING, ++piece_no) {
-                const uint32_t bytes = (uint32_t)((unit_bytes - off) < (size_t)STAGING ? (unit_bytes - off) : STAGING);
-                const int b = (int)(piece_no & 1);
-                if (piece_no >= 2) bulk_wait_read1();
-                mbar_expect_tx(gat_bar + 8 * b, bytes);
-                bulk_g2s(sStage + b * STAGING, src + off, bytes, gat_bar + 8 * b);
-                if (!wait_bar(gat_bar + 8 * b, gphase[b], ab, 5)) {
-                    wait_bar(gat_bar + 8 * b, gphase[b], ab, 11, true);
+            for (int c = 0; c < nch; ++c) {
+                const int b = c % GB;
+                if (!wait_bar(gat_bar + 8 * b, (gph >> b) & 1u, ab, 5)) {
+                    // leave no load in flight: chunks c .. issued-1, one per buffer
+                    for (int d = c; d < issued; ++d) {
+                        const int bd = d % GB;
+                        wait_bar(gat_bar + 8 * bd, (gph >> bd) & 1u, ab, 11, true);
+                        gph ^= 1u << bd;
+                    }
                     ok = false;
                     break;
                 }
-                gphase[b] ^= 1u;
-                bulk_s2g(dst + off, sStage + b * STAGING, bytes);
+                gph ^= 1u << b;
+                bulk_s2g(dst + (size_t)c * GCH, sStage + b * GCH, chunk_bytes(c));
                 bulk_commit();
+                if (c >= 1 && issued < nch) {   // chunk c-1's buffer, once its store has read it
+                    bulk_wait_read1();
+                    load(issued++);
+                }
             }
             bulk_wait_all();
             if (!ok) break;
@@ -603,10 +730,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             for (int cc = 0; cc < PN / 32; cc += 2) {
                 tmem_wait_ld32(va);
                 tmem_ld32_async(trow + (cc + 1) * 32, vb);
-                store_row32(crow + cc * 64, va, p.st32);
+                store_row32<C_POL>(crow + cc * 64, va, p.st32);
                 tmem_wait_ld32(vb);
                 if (cc + 2 < PN / 32) tmem_ld32_async(trow + (cc + 2) * 32, va);
-                store_row32(crow + (cc + 1) * 64, vb, p.st32);
+                store_row32<C_POL>(crow + (cc + 1) * 64, vb, p.st32);
             }
             tc_fence_before();
             __syncwarp();
