@@ -424,6 +424,20 @@ int ring_set_slices(int slices);
 int ring_debug_skip_notify(int rank, int step);
 
 /*
+ * Test hook for failure detection in the all-gather + GEMM: the next
+ * ag_gemm, ag_gemm_kn or ag_gemm_ex launch on any thread copies the gather
+ * piece that starts at A_g row `row` (a multiple of 16) but never publishes
+ * its ready flag.  If those rows belong to another rank than the caller's,
+ * the tiles that read them wait until the time bound, ring_status() (or
+ * ring_status_ex() for a caller's workspace) reports RC_ERR_TIMEOUT, C is
+ * undefined and the device stays usable; every role of the kernel stops
+ * with no copy or MMA left in flight.  A row that starts no piece, or one of
+ * the caller's own rows (read from its shard, never waited on), has no
+ * effect.  -1 cancels a pending skip.  Errors: RC_ERR_INVALID (row < -1).
+ */
+int ag_gemm_debug_skip_piece(int row);
+
+/*
  * Tracing hook: while dev_buf is set (a device buffer of `bytes` bytes), every
  * ring launch (the entry points listed for ring_debug_skip_notify) writes
  * three %globaltimer stamps (ns) per rank, slice and global step g, at word

@@ -29,7 +29,7 @@ __all__ = [
     "ring_status_ex", "ring_all_gather_ex", "ring_all_gather_workspace_bytes", "ring_reduce_scatter_ex",
     "ring_reduce_scatter_workspace_bytes", "ring_reduce_scatter_bidir_ex", "ring_reduce_scatter_bidir_workspace_bytes",
     "ag_gemm_ex", "ag_gemm_kn", "ag_gemm_workspace_bytes", "RC_B_NK", "RC_B_KN", "gemm_rs_ex", "gemm_rs_workspace_bytes",
-    "ring_last_error", "ring_set_timeout_ms", "ring_set_slices", "ring_debug_skip_notify",
+    "ring_last_error", "ring_set_timeout_ms", "ring_set_slices", "ring_debug_skip_notify", "ag_gemm_debug_skip_piece",
     "ring_debug_set_trace", "ring_debug_l2_rate", "ring_finalize", "library_path", "load",
 ]
 
@@ -73,6 +73,7 @@ _SIGNATURES = {
     "ring_set_timeout_ms": ([_u], _i),
     "ring_set_slices": ([_i], _i),
     "ring_debug_skip_notify": ([_i, _i], _i),
+    "ag_gemm_debug_skip_piece": ([_i], _i),
     "ring_debug_set_trace": ([_vp, _sz], _i),
     "ring_debug_l2_rate": ([_vp, _vp, _vp, _sz, _i, _i, _vp], _i),
     "ring_finalize": ([], _i),
@@ -433,6 +434,12 @@ def ring_set_slices(slices: int) -> None:
 
 def ring_debug_skip_notify(rank: int, step: int) -> None:
     _check(load().ring_debug_skip_notify(rank, step))
+
+
+def ag_gemm_debug_skip_piece(row: int) -> None:
+    """The next ag_gemm launch never publishes the ready flag of the gather
+    piece starting at A_g row `row`; -1 cancels (see include/ringcoll.h)."""
+    _check(load().ag_gemm_debug_skip_piece(row))
 
 
 def ring_finalize() -> None:

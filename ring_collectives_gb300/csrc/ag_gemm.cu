@@ -34,6 +34,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -112,6 +113,7 @@ struct Params {
     int g_total_m, g_per_pe;   // gather schedule, in 128-row blocks (8 units of 16 rows each)
     int st32;                  // 1: rows of C start on 32-byte boundaries (full-sector stores)
     int b_kn;                  // 1: B is stored [K][N] (MN-major operand), 0: [N][K] (K-major)
+    int skip_row;              // test hook: the piece starting at this A_g row is never published (-1: none)
     unsigned long long timeout_ns;
 };
 
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             bulk_wait_all();              // this unit's rows are in A_g
             if (!ok) break;
             fence_proxy_async_global();   // async-proxy writes before the generic release
-            st_release_gpu(&p.flags[mb * (BM / PIECE_ROWS) + piece], E);
+            if (row != p.skip_row) st_release_gpu(&p.flags[mb * (BM / PIECE_ROWS) + piece], E);
         }
         bulk_wait_all();
     } else if (warp >= 4) {
@@ -705,7 +707,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             bulk_wait_all();
             if (!ok) break;
             fence_proxy_async_global();
-            st_release_gpu(&p.flags[mb * (BM / PIECE_ROWS) + piece], E);
+            if (row != p.skip_row) st_release_gpu(&p.flags[mb * (BM / PIECE_ROWS) + piece], E);
         }
         bulk_wait_all();
     } else if (warp >= 4) {
@@ -828,6 +830,8 @@ static int make_map_k2(CUtensorMap *map, const void *ptr, int rank, const cuuint
 
 // Tuning knob, read once from the environment: RC_GEMM_PAIRS=0 keeps the
 // one-CTA kernel even where the CTA-pair form applies.
+static std::atomic<int> g_skip_row{-1};   // ag_gemm_debug_skip_piece
+
 static bool pair_tiles_enabled()
 {
     static const bool v = [] {
@@ -931,6 +935,7 @@ static int ag_gemm_run(const void *a_shards, size_t a_stride, void *a_gathered, 
         }
     }
 
+    p.skip_row = g_skip_row.exchange(-1);
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -1010,6 +1015,13 @@ extern "C" int ag_gemm_ex(const void *a_shards, size_t a_stride, void *a_gathere
     if (!workspace) return rc::set_error(RC_ERR_INVALID, "null workspace");
     return ag_gemm_run(a_shards, a_stride, a_gathered, B, b_layout, C, P, rank, M_r, N, K, workspace, ws_bytes,
                        stream);
+}
+
+extern "C" int ag_gemm_debug_skip_piece(int row)
+{
+    if (row < -1) return rc::set_error(RC_ERR_INVALID, "row %d below -1", row);
+    rc::ag::g_skip_row.store(row);
+    return RC_OK;
 }
 
 // Header + one ready flag per gather unit (PIECE_ROWS rows of A_g).

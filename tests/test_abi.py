@@ -74,6 +74,11 @@ def test_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert _call(lib, "ring_all_gather", fake, sz(64), vp(0x20000), sz(64), 4, sz(16), 0, vp(0)) == RC_ERR_INVALID
     # reduce_scatter out overlapping bufs
     assert _call(lib, "ring_reduce_scatter", fake, sz(4096), vp(0x10010), sz(64), 4, sz(16), 0, vp(0)) == RC_ERR_INVALID
+    # fault-injection hooks: bad arguments are refused, -1 cancels
+    assert _call(lib, "ag_gemm_debug_skip_piece", -2) == RC_ERR_INVALID
+    assert _call(lib, "ag_gemm_debug_skip_piece", -1) == 0
+    assert _call(lib, "ring_debug_skip_notify", -2, 0) == RC_ERR_INVALID
+    assert _call(lib, "ring_debug_skip_notify", -1, -1) == 0
     # timeout bounds
     assert _call(lib, "ring_set_timeout_ms", ctypes.c_uint(0)) == RC_ERR_INVALID
 

@@ -128,6 +128,53 @@ def test_ag_gemm_repeated_calls_and_ranks():
             assert torch.equal(C, ref)
 
 
+def test_ag_gemm_few_spare_pairs_carry_the_gather():
+    """P=8, M_r=1024, N=1792: 224 tiles of 256x256.  On a 152-SM GB300 (76 CTA
+    pairs) 72 pairs run 3 tiles and 4 pairs run 2, and the gather goes to the
+    8 CTAs of those 4 pairs alone: A_g bit for bit, C within the bound on
+    sampled rows (every M block) and columns."""
+    P, M_r, K, N = 8, 1024, 256, 1792
+    a, b, ag, C = run(P, M_r, K, N, rank=6, seed=13)
+    assert torch.equal(ag.view(P, M_r, K).cpu(), a)
+    A_bits = synthetic.bf16_bits(a).reshape(P * M_r, K)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.arange(0, P * M_r, 64) + rng.integers(0, 64, P * M_r // 64))
+    cols = np.unique(np.concatenate([np.arange(0, N, 256) + rng.integers(0, 256, N // 256), rng.integers(0, N, 120)]))
+    check_c(A_bits, synthetic.bf16_bits(b), bits(C)[np.ix_(rows, cols)], rows, cols)
+
+
+@pytest.mark.parametrize("P,M_r,K,N,rank", [(4, 256, 256, 512, 1), (8, 256, 128, 768, 7), (3, 128, 192, 256, 2)])
+def test_missing_ready_flag_times_out_and_device_stays_usable(P, M_r, K, N, rank):
+    """Failure detection: a gather piece whose ready flag is never published
+    (ag_gemm_debug_skip_piece, on the host) makes the tiles that read it wait
+    until the time bound; every role of the kernel stops, ring_status()
+    reports RC_ERR_TIMEOUT once, and the next call is exact.  CTA pairs (M_r a
+    multiple of 256) and the one-CTA form."""
+    a, b = synthetic.ag_gemm_inputs(P=P, M_r=M_r, K=K, N=N, seed=21)
+    ad, bd = a.to(DEV), b.to(DEV)
+    A_bits = synthetic.bf16_bits(a).reshape(P * M_r, K)
+    ag = torch.zeros((P * M_r, K), dtype=torch.bfloat16, device=DEV)
+    C = torch.zeros((P * M_r, N), dtype=torch.bfloat16, device=DEV)
+    rc.ring_set_timeout_ms(100)
+    try:
+        rc.ag_gemm_debug_skip_piece(((rank + 1) % P) * M_r + 16)   # a piece of another rank's rows
+        rc.ag_gemm(ad, ag, bd, C, rank)
+        assert rc.ring_status() == rc.RC_ERR_TIMEOUT
+        assert rc.ring_status() == rc.RC_OK          # read and cleared
+        rc.ag_gemm_debug_skip_piece(rank * M_r)     # the caller's own rows: never waited on
+        rc.ag_gemm(ad, ag, bd, C, rank)
+        assert rc.ring_status() == rc.RC_OK, rc.ring_last_error()
+        ag.zero_()
+        C.zero_()
+        rc.ag_gemm(ad, ag, bd, C, rank)
+        assert rc.ring_status() == rc.RC_OK, rc.ring_last_error()
+    finally:
+        rc.ring_set_timeout_ms(2000)
+        rc.ag_gemm_debug_skip_piece(-1)
+    assert np.array_equal(bits(ag), A_bits)
+    check_c(A_bits, synthetic.bf16_bits(b), bits(C))
+
+
 def test_ag_gemm_rejects_bad_shapes():
     a = torch.zeros((2, 100, 64), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(rc.RingError):

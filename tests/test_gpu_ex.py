@@ -158,6 +158,31 @@ def bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def test_ag_gemm_ex_timeout_reported_on_its_workspace():
+    P, M_r, K, N, rank = 4, 256, 256, 512, 1
+    a, b = synthetic.ag_gemm_inputs(P=P, M_r=M_r, K=K, N=N, seed=45)
+    ad, bd = a.to(DEV), b.to(DEV)
+    ws = zeros_ws(rc.ag_gemm_workspace_bytes(P, M_r))
+    ag = torch.zeros((P * M_r, K), dtype=torch.bfloat16, device=DEV)
+    C = torch.zeros((P * M_r, N), dtype=torch.bfloat16, device=DEV)
+    ref = torch.empty_like(C)
+    rc.ag_gemm(ad, torch.empty_like(ag), bd, ref, rank)
+    assert rc.ring_status() == rc.RC_OK
+    rc.ring_set_timeout_ms(100)
+    try:
+        rc.ag_gemm_debug_skip_piece(2 * M_r)
+        rc.ag_gemm_ex(ad, ag, bd, C, rank, ws)
+        assert rc.ring_status_ex(ws) == rc.RC_ERR_TIMEOUT
+        assert rc.ring_status() == rc.RC_OK
+        rc.ag_gemm_ex(ad, ag, bd, C, rank, ws)
+        assert rc.ring_status_ex(ws) == rc.RC_OK, rc.ring_last_error()
+    finally:
+        rc.ring_set_timeout_ms(2000)
+        rc.ag_gemm_debug_skip_piece(-1)
+    assert np.array_equal(bits(ag), oracle.ag_gather(synthetic.bf16_bits(a)))
+    assert np.array_equal(bits(C), bits(ref))
+
+
 @pytest.mark.parametrize("P,M_r,K,N", [(4, 256, 256, 512), (3, 128, 192, 256)])
 def test_ag_gemm_ex_two_streams(P, M_r, K, N):
     """CTA-pair shape and single-CTA shape; two ranks' views on two streams."""
