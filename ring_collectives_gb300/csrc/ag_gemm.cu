@@ -650,8 +650,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int nch = (int)((unit_bytes + GCH - 1) / GCH);
         const uint64_t pol_once = policy_evict_first();
         uint32_t gph = 0;   // bit b: parity of gather buffer b's next completion
+        // The shares apply when the pairs with one tile fewer hold at least a
+        // fifth of the grid: fewer CTAs could not copy the units as fast as
+        // the consumers read them (one unit per CTA every ~6-8 us against
+        // ~76 per 20 us wave at P=8, 8192x4096x4096), so then every CTA
+        // gathers alike.
         const int full_pairs = p.total_tiles % npairs;
-        const int nw = full_pairs ? RC_AG_GATHER_NW : 1, sw = full_pairs ? RC_AG_GATHER_SW : 1;
+        const bool shares = full_pairs > 0 && 5 * 2 * (npairs - full_pairs) >= (int)gridDim.x;
+        const int nw = shares ? RC_AG_GATHER_NW : 1, sw = shares ? RC_AG_GATHER_SW : 1;
         const int n_full = 2 * full_pairs;                                // CTAs of the pairs with the extra tile
         const int per_round = n_full * nw + ((int)gridDim.x - n_full) * sw;
         const bool spare = (int)blockIdx.x >= n_full;

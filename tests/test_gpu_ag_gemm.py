@@ -128,12 +128,14 @@ def test_ag_gemm_repeated_calls_and_ranks():
             assert torch.equal(C, ref)
 
 
-def test_ag_gemm_few_spare_pairs_carry_the_gather():
-    """P=8, M_r=1024, N=1792: 224 tiles of 256x256.  On a 152-SM GB300 (76 CTA
-    pairs) 72 pairs run 3 tiles and 4 pairs run 2, and the gather goes to the
-    8 CTAs of those 4 pairs alone: A_g bit for bit, C within the bound on
-    sampled rows (every M block) and columns."""
-    P, M_r, K, N = 8, 1024, 256, 1792
+@pytest.mark.parametrize("N", [1792, 2304])
+def test_ag_gemm_uneven_tile_counts(N):
+    """P=8, M_r=1024, N=1792 or 2304: 224 or 288 tiles of 256x256.  On a
+    152-SM GB300 (76 CTA pairs) 224 tiles leave only 4 pairs with a tile
+    fewer (8 CTAs, too few to carry the gather, so every CTA gathers) and 288
+    tiles leave 16 (32 CTAs, which gather alone): A_g bit for bit, C within
+    the bound on sampled rows (every M block) and columns."""
+    P, M_r, K = 8, 1024, 256
     a, b, ag, C = run(P, M_r, K, N, rank=6, seed=13)
     assert torch.equal(ag.view(P, M_r, K).cpu(), a)
     A_bits = synthetic.bf16_bits(a).reshape(P * M_r, K)
