@@ -20,8 +20,9 @@
 //               gather producer: 16-row pieces of the shards are copied into
 //               A_g with bulk copies through 32 KiB of staging buffers, in
 //               the order the consumers need them, and each piece publishes
-//               its ready flag (st.release of the launch epoch).  (The
-//               CTA-pair form below gathers on part of the grid only.)
+//               its ready flag (st.release of the launch epoch); see
+//               gather_units.  (The CTA-pair form below gathers on part of
+//               the grid only.)
 //   warps 4-7   epilogue: TMEM -> registers (tcgen05.ld), fp32 -> bf16 (RNE),
 //               stores to C, then free the accumulator for the MMA warp.
 // Rows of the own rank are read straight from its shard (local data, no
@@ -55,7 +56,7 @@ constexpr int B_STAGE = BN * BK * 2;   // 32 KiB
 #define RC_AG_GEMM_STAGING 16384
 #endif
 constexpr int STAGING = RC_AG_GEMM_STAGING; // gather staging buffer (x2)
-// CTA-pair form: the A producer looks at the ready flags of its next tile
+// The A producer looks at the ready flags of its next tile
 // half-way through the current one and then every RC_AG_POLL_EVERY stages
 // until it sees them set (0: only the one look half-way through).
 #ifndef RC_AG_POLL_EVERY
@@ -68,13 +69,13 @@ constexpr int POLL_EVERY = RC_AG_POLL_EVERY > 0 ? RC_AG_POLL_EVERY : 1 << 20;
 #ifndef RC_AG_GATHER_HINT
 #define RC_AG_GATHER_HINT 1
 #endif
-// CTA-pair form: the gather's staging space (2 x STAGING bytes) as a ring of
+// The gather's staging space (2 x STAGING bytes) as a ring of
 // RC_AG_GATHER_BUFS buffers, all but one of them loading at any time.
 #ifndef RC_AG_GATHER_BUFS
 #define RC_AG_GATHER_BUFS 4
 #endif
 constexpr int GB = RC_AG_GATHER_BUFS;
-// CTA-pair form: C, which nothing reads in the launch, is stored
+// C, which nothing reads in the launch, is stored
 // evict_first (RC_AG_C_POLICY 1; 0 normal), so that the 64 MiB it streams
 // through L2 does not push out operand rows still to be read.
 #ifndef RC_AG_C_POLICY
@@ -213,6 +214,78 @@ __device__ bool poll_block_flags(const uint32_t *f, uint32_t E)
     return all;
 }
 
+// Gather producer (one thread per CTA): copies gather units into A_g and
+// publishes each unit's ready flag (st.release of the launch epoch).  This
+// CTA takes units first, first+1, ..., first+w-1, then the same w units
+// per_round further on, and so on.  Each unit (PIECE_ROWS rows) streams
+// through a ring of GB staging buffers at sStage with barriers at gat_bar: a
+// load (global -> shared) per buffer in flight, and a buffer refilled once
+// the store (shared -> A_g) of its previous chunk has read it.  Other
+// ranks' rows, read once here, are loaded evict_first.  Bounded waits; on
+// a failure every load still in flight lands before the function returns.
+__device__ void gather_units(const Params &p, uint32_t sStage, uint32_t gat_bar, const Abort &ab,
+                             const int *abort_flag, uint32_t E, int first, int per_round, int w)
+{
+    const size_t row_bytes = (size_t)p.K * 2;
+    const size_t unit_bytes = (size_t)PIECE_ROWS * row_bytes;
+    const int nch = (int)((unit_bytes + GCH - 1) / GCH);
+    const uint64_t pol_once = policy_evict_first();
+    uint32_t gph = 0;   // bit b: parity of gather buffer b's next completion
+    for (int i = 0; w > 0 && !*(volatile const int *)abort_flag; ++i) {
+        const int u = first + (i / w) * per_round + i % w;   // increasing in i
+        if (u >= p.units) break;
+        int mb, piece;
+        unit_of(p, u, mb, piece);
+        const int row = mb * BM + piece * PIECE_ROWS;     // row of A_g
+        const int src_rank = row / p.M_r;
+        const char *src = p.a_shards + (size_t)src_rank * p.a_stride + (size_t)(row % p.M_r) * row_bytes;
+        char *dst = p.a_gathered + (size_t)row * row_bytes;
+        // Other ranks' rows are read once here (the GEMM reads them from
+        // A_g); the own rank's rows are also the GEMM's operand.
+        const bool once = RC_AG_GATHER_HINT && src_rank != p.rank;
+        auto chunk_bytes = [&](int c) -> uint32_t {
+            const size_t off = (size_t)c * GCH;
+            return (uint32_t)(unit_bytes - off < (size_t)GCH ? unit_bytes - off : (size_t)GCH);
+        };
+        auto load = [&](int c) {
+            const int b = c % GB;
+            mbar_expect_tx(gat_bar + 8 * b, chunk_bytes(c));
+            if (once)
+                bulk_g2s_hint(sStage + b * GCH, src + (size_t)c * GCH, chunk_bytes(c), gat_bar + 8 * b, pol_once);
+            else
+                bulk_g2s(sStage + b * GCH, src + (size_t)c * GCH, chunk_bytes(c), gat_bar + 8 * b);
+        };
+        int issued = 0;
+        for (; issued < nch && issued < GB; ++issued) load(issued);
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+            const int b = c % GB;
+            if (!wait_bar(gat_bar + 8 * b, (gph >> b) & 1u, ab, 5)) {
+                // leave no load in flight: chunks c .. issued-1, one per buffer
+                for (int d = c; d < issued; ++d) {
+                    const int bd = d % GB;
+                    wait_bar(gat_bar + 8 * bd, (gph >> bd) & 1u, ab, 11, true);
+                    gph ^= 1u << bd;
+                }
+                ok = false;
+                break;
+            }
+            gph ^= 1u << b;
+            bulk_s2g(dst + (size_t)c * GCH, sStage + b * GCH, chunk_bytes(c));
+            bulk_commit();
+            if (c >= 1 && issued < nch) {   // chunk c-1's buffer, once its store has read it
+                bulk_wait_read1();
+                load(issued++);
+            }
+        }
+        bulk_wait_all();              // this unit's rows are in A_g
+        if (!ok) break;
+        fence_proxy_async_global();   // async-proxy writes before the generic release
+        if (row != p.skip_row) st_release_gpu(&p.flags[mb * (BM / PIECE_ROWS) + piece], E);
+    }
+    bulk_wait_all();
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     k_ag_gemm(const __grid_constant__ CUtensorMap map_ag, const __grid_constant__ CUtensorMap map_sh,
               const __grid_constant__ CUtensorMap map_b, const Params p)
@@ -228,11 +301,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t bars = smem_u32(bars_g);
     const uint32_t full_bar = bars, empty_bar = bars + 8 * STAGES;
     const uint32_t tfull_bar = bars + 16 * STAGES, tempty_bar = tfull_bar + 16;
-    const uint32_t gat_bar = tempty_bar + 16;
-    uint32_t *tmem_slot = (uint32_t *)(bars_g + 16 * STAGES + 48);
-    int *abort_flag = (int *)(bars_g + 16 * STAGES + 52);
-    uint32_t *epoch_slot = (uint32_t *)(bars_g + 16 * STAGES + 56);
-    const uint32_t drain_bar = bars + 16 * STAGES + 64;
+    const uint32_t gat_bar = tempty_bar + 16;          // GB gather buffers
+    const uint32_t drain_bar = gat_bar + 8 * GB;
+    uint32_t *tmem_slot = (uint32_t *)(bars_g + 16 * STAGES + 40 + 8 * GB);
+    int *abort_flag = (int *)(bars_g + 16 * STAGES + 44 + 8 * GB);
+    uint32_t *epoch_slot = (uint32_t *)(bars_g + 16 * STAGES + 48 + 8 * GB);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -243,8 +316,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar + 8 * a, 1);
             mbar_init(tempty_bar + 8 * a, 4);   // one arrive per epilogue warp
-            mbar_init(gat_bar + 8 * a, 1);
         }
+        for (int b = 0; b < GB; ++b) mbar_init(gat_bar + 8 * b, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         *epoch_slot = ld_relaxed_gpu(&p.hdr->epoch) + 1u;
@@ -272,14 +345,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- TMA producer
         uint32_t stage = 0, phase = 0;
         int issued[STAGES] = {0, 0, 0, 0};
+        bool next_ready = false;   // the next tile's flags were already seen set (and acquired)
         for (int t = blockIdx.x; t < p.total_tiles && !*(volatile int *)abort_flag; t += gridDim.x) {
             int m, n;
             tile_of(p, t, m, n);
             const int src_rank = (m * BM) / p.M_r;
             const bool own = src_rank == p.rank;
             if (!own) {
-                if (!wait_block_flags(&p.flags[m * (BM / PIECE_ROWS)], E, ab, 1)) break;
+                if (!next_ready && !wait_block_flags(&p.flags[m * (BM / PIECE_ROWS)], E, ab, 1)) break;
                 fence_proxy_async_global(); // the generic-proxy flags order the async-proxy reads below
+            }
+            // the next tile's flags, looked at from half-way through this tile (as in the pair form)
+            next_ready = false;
+            const uint32_t *next_flags = nullptr;
+            if (t + (int)gridDim.x < p.total_tiles) {
+                int mn, nn;
+                tile_of(p, t + (int)gridDim.x, mn, nn);
+                if ((mn * BM) / p.M_r != p.rank) next_flags = &p.flags[mn * (BM / PIECE_ROWS)];
             }
             const int row_in_shard = (m * BM) % p.M_r;
             bool ok = true;
@@ -302,6 +384,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     stage = 0;
                     phase ^= 1u;
                 }
+                if (next_flags && !next_ready && kb >= ksteps / 2 && (kb - ksteps / 2) % POLL_EVERY == 0)
+                    next_ready = poll_block_flags(next_flags, E);
             }
             if (!ok) break;
         }
@@ -352,40 +436,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_commit(drain_bar);
         wait_bar(drain_bar, 0, ab, 10, true);
     } else if (warp == 2 && lane == 0) {
-        // ---------------- gather producer
-        const size_t row_bytes = (size_t)p.K * 2;
-        const size_t unit_bytes = (size_t)PIECE_ROWS * row_bytes;
-        uint32_t gphase[2] = {0, 0};
-        uint64_t piece_no = 0;
-        for (int u = blockIdx.x; u < p.units && !*(volatile int *)abort_flag; u += gridDim.x) {
-            int mb, piece;
-            unit_of(p, u, mb, piece);
-            const int row = mb * BM + piece * PIECE_ROWS;     // row of A_g
-            const int src_rank = row / p.M_r;
-            const char *src = p.a_shards + (size_t)src_rank * p.a_stride + (size_t)(row % p.M_r) * row_bytes;
-            char *dst = p.a_gathered + (size_t)row * row_bytes;
-            bool ok = true;
-            for (size_t off = 0; off < unit_bytes; off += STAGING, ++piece_no) {
-                const uint32_t bytes = (uint32_t)((unit_bytes - off) < (size_t)STAGING ? (unit_bytes - off) : STAGING);
-                const int b = (int)(piece_no & 1);
-                if (piece_no >= 2) bulk_wait_read1(); // the store that last used buffer b has read it
-                mbar_expect_tx(gat_bar + 8 * b, bytes);
-                bulk_g2s(sStage + b * STAGING, src + off, bytes, gat_bar + 8 * b);
-                if (!wait_bar(gat_bar + 8 * b, gphase[b], ab, 5)) {
-                    wait_bar(gat_bar + 8 * b, gphase[b], ab, 11, true); // the load must land before exit
-                    ok = false;
-                    break;
-                }
-                gphase[b] ^= 1u;
-                bulk_s2g(dst + off, sStage + b * STAGING, bytes);
-                bulk_commit();
-            }
-            bulk_wait_all();              // this unit's rows are in A_g
-            if (!ok) break;
-            fence_proxy_async_global();   // async-proxy writes before the generic release
-            if (row != p.skip_row) st_release_gpu(&p.flags[mb * (BM / PIECE_ROWS) + piece], E);
-        }
-        bulk_wait_all();
+        // ---------------- gather producer (every CTA alike)
+        gather_units(p, sStage, gat_bar, ab, abort_flag, E, (int)blockIdx.x, (int)gridDim.x, 1);
     } else if (warp >= 4) {
         // ---------------- epilogue
         const int q = warp - 4;            // TMEM lane quadrant of this warp
@@ -407,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int cc = 0; cc < BN / 32; ++cc) {
                 uint32_t v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + cc * 32, v);
-                store_row32(crow + cc * 64, v, p.st32);
+                store_row32<C_POL>(crow + cc * 64, v, p.st32);
             }
             tc_fence_before();
             __syncwarp();
@@ -437,20 +489,21 @@ __global__ void __launch_bounds__(THREADS, 1)
 // bytes per clock per SM that tiled TMA loads reach on GB300), the even CTA
 // issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and both CTAs drain
 // their own 128 rows of D.  Each CTA waits only on the ready flags of its own
-// 128 A rows.  What differs from the one-CTA form (measured on GB300, P=8,
-// 8192x4096x4096, CUDA events over 30 back-to-back calls):
+// 128 A rows.  Measured on GB300 (P=8, 8192x4096x4096, CUDA events over 30
+// back-to-back calls), in both forms:
 //  * the A producer looks at the next tile's flags from half-way through the
 //    current tile (a flag round trip at the tile boundary left the MMA idle:
 //    0.1633 -> 0.1604 ms);
 //  * the gather streams each unit through a ring of 4 staging buffers with 3
 //    loads in flight (one load at a time ran at ~10 GB/s per CTA), loading
 //    other ranks' rows evict_first;
+//  * C is stored evict_first (0.1592 -> 0.1552 ms).
+// And in the pair form only:
 //  * the gather runs on the CTAs of the pairs with one tile fewer: its bulk
 //    copies share the SM's copy engine with the operand loads, and on the
 //    pairs that set the launch's length it slowed the first tiles by ~3 us
 //    each (0.1591 ms with every CTA gathering, 0.1580 with a 1:3 share,
-//    0.1551 with the spare pairs alone);
-//  * C is stored evict_first (0.1592 -> 0.1552 ms).
+//    0.1551 with the spare pairs alone).
 // Without the gather and its waits the same kernel takes 0.1433 ms, as much
 // as cuBLAS on the plain GEMM; in-kernel clock stamps put the SM clock at
 // 1.6-1.9 GHz during the launch (the power limit), so tiles after the first
@@ -642,14 +695,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         wait_bar(drain_bar, 0, ab, 10, true);
     } else if (warp == 2 && lane == 0) {
         // ---------------- gather producer (units shared out by RC_AG_GATHER_NW / _SW)
-        // Each unit streams through a ring of GB staging buffers: a load
-        // (global -> shared) per buffer in flight, and a buffer is refilled
-        // once the store (shared -> A_g) of its previous chunk has read it.
-        const size_t row_bytes = (size_t)p.K * 2;
-        const size_t unit_bytes = (size_t)PIECE_ROWS * row_bytes;
-        const int nch = (int)((unit_bytes + GCH - 1) / GCH);
-        const uint64_t pol_once = policy_evict_first();
-        uint32_t gph = 0;   // bit b: parity of gather buffer b's next completion
         // The shares apply when the pairs with one tile fewer hold at least a
         // fifth of the grid: fewer CTAs could not copy the units as fast as
         // the consumers read them (one unit per CTA every ~6-8 us against
@@ -661,61 +706,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int n_full = 2 * full_pairs;                                // CTAs of the pairs with the extra tile
         const int per_round = n_full * nw + ((int)gridDim.x - n_full) * sw;
         const bool spare = (int)blockIdx.x >= n_full;
-        const int my_w = spare ? sw : nw;
         const int first = spare ? n_full * nw + ((int)blockIdx.x - n_full) * sw : (int)blockIdx.x * nw;
-        for (int i = 0; my_w > 0 && !*(volatile int *)abort_flag; ++i) {
-            const int u = first + (i / my_w) * per_round + i % my_w;   // increasing in i
-            if (u >= p.units) break;
-            int mb, piece;
-            unit_of(p, u, mb, piece);
-            const int row = mb * BM + piece * PIECE_ROWS;
-            const int src_rank = row / p.M_r;
-            const char *src = p.a_shards + (size_t)src_rank * p.a_stride + (size_t)(row % p.M_r) * row_bytes;
-            char *dst = p.a_gathered + (size_t)row * row_bytes;
-            // Other ranks' rows are read once here (the GEMM reads them from
-            // A_g); the own rank's rows are also the GEMM's operand.
-            const bool once = RC_AG_GATHER_HINT && src_rank != p.rank;
-            auto chunk_bytes = [&](int c) -> uint32_t {
-                const size_t off = (size_t)c * GCH;
-                return (uint32_t)(unit_bytes - off < (size_t)GCH ? unit_bytes - off : (size_t)GCH);
-            };
-            auto load = [&](int c) {
-                const int b = c % GB;
-                mbar_expect_tx(gat_bar + 8 * b, chunk_bytes(c));
-                if (once)
-                    bulk_g2s_hint(sStage + b * GCH, src + (size_t)c * GCH, chunk_bytes(c), gat_bar + 8 * b, pol_once);
-                else
-                    bulk_g2s(sStage + b * GCH, src + (size_t)c * GCH, chunk_bytes(c), gat_bar + 8 * b);
-            };
-            int issued = 0;
-            for (; issued < nch && issued < GB; ++issued) load(issued);
-            bool ok = true;
-            for (int c = 0; c < nch; ++c) {
-                const int b = c % GB;
-                if (!wait_bar(gat_bar + 8 * b, (gph >> b) & 1u, ab, 5)) {
-                    // leave no load in flight: chunks c .. issued-1, one per buffer
-                    for (int d = c; d < issued; ++d) {
-                        const int bd = d % GB;
-                        wait_bar(gat_bar + 8 * bd, (gph >> bd) & 1u, ab, 11, true);
-                        gph ^= 1u << bd;
-                    }
-                    ok = false;
-                    break;
-                }
-                gph ^= 1u << b;
-                bulk_s2g(dst + (size_t)c * GCH, sStage + b * GCH, chunk_bytes(c));
-                bulk_commit();
-                if (c >= 1 && issued < nch) {   // chunk c-1's buffer, once its store has read it
-                    bulk_wait_read1();
-                    load(issued++);
-                }
-            }
-            bulk_wait_all();
-            if (!ok) break;
-            fence_proxy_async_global();
-            if (row != p.skip_row) st_release_gpu(&p.flags[mb * (BM / PIECE_ROWS) + piece], E);
-        }
-        bulk_wait_all();
+        gather_units(p, sStage, gat_bar, ab, abort_flag, E, first, per_round, spare ? sw : nw);
     } else if (warp >= 4) {
         // ---------------- epilogue (both CTAs): this CTA's 128 rows of the pair tile
         const int q = warp - 4;
