@@ -69,6 +69,13 @@ struct Params {
 
 // Tile t -> (m block, n block); n-major within an m block keeps a tile row's
 // A operands hot in L2.
+// The reduced output, which nothing reads in the launch, is stored
+// evict_first (1) so that it does not push operand rows out of L2; 0: normal.
+#ifndef RC_GRS_OUT_POLICY
+#define RC_GRS_OUT_POLICY 1
+#endif
+constexpr int OUT_POL = RC_GRS_OUT_POLICY ? kStEvictFirst : kStNormal;
+
 __device__ __forceinline__ void tile_of(const Params &p, int t, int &m, int &n)
 {
     m = t / p.n_tiles;
@@ -233,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (p.st32) {
 #pragma unroll
                 for (int w = 0; w < BN / 16; ++w)   // one full 32-byte sector per lane and store
-                    st8<kStNormal>(dst + w * 32, make_uint4(acc[8 * w], acc[8 * w + 1], acc[8 * w + 2], acc[8 * w + 3]),
+                    st8<OUT_POL>(dst + w * 32, make_uint4(acc[8 * w], acc[8 * w + 1], acc[8 * w + 2], acc[8 * w + 3]),
                                    make_uint4(acc[8 * w + 4], acc[8 * w + 5], acc[8 * w + 6], acc[8 * w + 7]));
             } else {
 #pragma unroll
@@ -303,12 +310,6 @@ constexpr int CW2 = PN / (EPI2 / 4);     // accumulator columns per epilogue war
 #ifndef RC_GRS_STORE_IN_FOLD
 #define RC_GRS_STORE_IN_FOLD 1
 #endif
-// The reduced output, which nothing reads in the launch, is stored
-// evict_first (1) so that it does not push operand rows out of L2; 0: normal.
-#ifndef RC_GRS_OUT_POLICY
-#define RC_GRS_OUT_POLICY 1
-#endif
-constexpr int OUT_POL = RC_GRS_OUT_POLICY ? kStEvictFirst : kStNormal;
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
     k_gemm_rs2(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const Params p)
