@@ -11,8 +11,10 @@
 // One persistent cooperative launch, one 256-thread block per SM:
 //   warp 0      TMA producer: A and B tiles (128x64 and 256x64 bf16, 128-byte
 //               swizzle) into a 4-stage shared-memory ring.  Before the first
-//               A tile of an M block that came from another rank it waits
-//               (ld.acquire, bounded) on that block's ready flags.
+//               A tile of an M block that came from another rank it needs
+//               that block's ready flags set: it looks at them from half-way
+//               through the previous tile on and, if it has not seen them by
+//               the tile boundary, waits there (acquire, bounded).
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256,
 //               K=16, bf16 x bf16 -> fp32) into one of two TMEM accumulators
 //               and releases smem stages / accumulators with tcgen05.commit.
@@ -24,7 +26,8 @@
 //               gather_units.  (The CTA-pair form below gathers on part of
 //               the grid only.)
 //   warps 4-7   epilogue: TMEM -> registers (tcgen05.ld), fp32 -> bf16 (RNE),
-//               stores to C, then free the accumulator for the MMA warp.
+//               stores to C (evict_first), then free the accumulator for
+//               the MMA warp.
 // Rows of the own rank are read straight from its shard (local data, no
 // wait); rows of other ranks come from A_g once their flags are set.
 //
