@@ -25,6 +25,8 @@
 // Shared-memory form (any P or alignment): a block stages a tile of TE
 // positions of all P slots in shared memory, then computes each output and
 // stores it.  Each position is independent, so both forms are in place.
+#include <cstdlib>
+
 #include "dev.cuh"
 #include "internal.h"
 #include "ringcoll.h"
@@ -327,18 +329,38 @@ static const void *fold_reg_any(int dtype, int order, int P)
     return dtype == 0 ? fold_reg_fn<0, 1>(P) : dtype == 1 ? fold_reg_fn<1, 1>(P) : fold_reg_fn<2, 1>(P);
 }
 
+// Knob, read once: RC_FOLD_BLOCKS = blocks per SM of the register fold
+// (unset or malformed: the rule in launch_fold).
+static int fold_blocks_setting()
+{
+    static const int v = [] {
+        const char *e = getenv("RC_FOLD_BLOCKS");
+        if (!e || !*e) return 0;
+        char *end = nullptr;
+        const long x = strtol(e, &end, 10);
+        return (end && *end == 0 && x >= 1 && x <= 16) ? (int)x : 0;
+    }();
+    return v;
+}
+
 cudaError_t launch_fold(char *data, size_t stride, int P, size_t N, size_t chunk, int dtype, int order, int sm_count,
                         cudaStream_t st)
 {
     const int es = dtype == 1 ? 2 : 4;
     const void *rf = ((((uintptr_t)data) | stride) & 31u) == 0 ? fold_reg_any(dtype, order, P) : nullptr;
     if (rf) {
-        // as many 256-thread blocks as fit on the GPU at once (grid-stride loop)
+        // 256-thread blocks over a grid-stride loop: as many per SM as fit, but
+        // no more than keep ~64 KiB of loads in flight per SM (each thread holds
+        // P vectors of 32 bytes: max(1, 8/P) blocks).  Measured on GB300 at P=8
+        // x 64 MiB fp32, ring order: 2 blocks per SM 0.1679 ms, 1 block
+        // 0.1637 ms (the psum order, whose registers allow 1 block, 0.1636).
         static int per_sm[3][2][9] = {};
         int &occ = per_sm[dtype][order][P];
         if (occ == 0) {
             cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rf, kFoldRegThreads, 0);
             if (e != cudaSuccess) return e;
+            const int cap = fold_blocks_setting() > 0 ? fold_blocks_setting() : (8 / P > 1 ? 8 / P : 1);
+            if (occ > cap) occ = cap;
             if (occ < 1) occ = 1;
         }
         const size_t vecs = N * es / 32 + 1;
