@@ -63,3 +63,18 @@ def test_committed_profiles_are_well_formed(bench):
             assert re.search(r"^kernel_source_sha256_16: [0-9a-f]{16}$", text, re.M), name
             assert re.search(r"^dram_bytes_per_launch: \d+$", text, re.M), name
     assert seen >= 9
+
+
+def test_every_measured_row_has_a_profile_of_the_current_source(bench):
+    """The bench line attaches DRAM traffic to a row only while its committed
+    ncu summary was taken on the kernel source in the tree; a kernel change
+    without a new capture would silently drop the figure, so every row that
+    reports traffic must find one here."""
+    ring = ["f32_64mib", "bf16_64mib", "weak"]
+    rows = {"reduce_scatter_bf16_64mib": bench.KERNEL_SOURCES, "reduce_scatter_bidir_bf16_64mib": bench.KERNEL_SOURCES,
+            "all_gather_f32_8mib": bench.KERNEL_SOURCES, "ppermute_f32_64mib": bench.KERNEL_SOURCES,
+            "fused_f32_64mib": bench.FOLD_SOURCES, "psum_f32_64mib": bench.FOLD_SOURCES}
+    for w in ring:
+        assert bench.profiled_traffic(w) is not None, f"profiles/ring_allreduce_{w}.md"
+    for name, sources in rows.items():
+        assert bench.profiled_traffic(name, sources, prefix="") is not None, f"profiles/{name}.md"
