@@ -405,7 +405,11 @@ int ring_set_timeout_ms(unsigned ms);
  * the host entry point's segment size; RC_GEMM_PAIRS=0 keeps the one-CTA
  * GEMM kernels; RC_RING_STAGGER=G (default 3, 1 = off) starts slice j of a
  * ring all-reduce or reduce-scatter (j % G) times a fifth of its first
- * step's estimated time later.
+ * step's estimated time later; RC_RING_PAIR=0 keeps the one-rank-per-block
+ * ring kernel at even P as well; RC_PAIR_SMEM sets the bytes of a slice's
+ * head that the two-rank kernel hands over in shared memory per block;
+ * RC_FOLD_BLOCKS sets the blocks per SM of the single-pass all-reduces
+ * (default max(1, 8/P)).
  */
 int ring_set_slices(int slices);
 
